@@ -1,0 +1,203 @@
+/*
+ * qlinear.h — C ABI of libqlinear.so: the fine-grained-scaled FP8 linear layer
+ * on GB300 (sm_103a).
+ *
+ * Two operations, each a CUDA kernel launched on the caller's stream:
+ *   - the FP8 cast (per token in 1x128 / 1x32 groups, or per 128x128 block),
+ *   - the block-scaled FP8 GEMM D = A * B^T (bf16 output for fwd/dgrad,
+ *     fp32 output, optionally accumulated, for wgrad).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *     allocates no device memory and never frees caller memory.
+ *   - Strides are in ELEMENTS of the tensor's own type (bf16/fp32: 2/4 bytes,
+ *     e4m3: 1 byte, scales: 4 bytes), signed 64-bit. A "view" (any strides) of
+ *     a larger buffer may be passed; only the view's elements are written
+ *     (bytes outside it are never touched).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *     asynchronous: no call synchronises the host. Arguments are validated on
+ *     the host before any launch; an invalid call launches nothing.
+ *   - Errors are returned as ql_status; no exception crosses the ABI.
+ *     Device-side wait time-outs are recorded in a device status word that
+ *     ql_device_status() reads (that call synchronises the given stream).
+ *   - E4M3 means the OCP E4M3FN byte format (max 448, no infinities).
+ */
+#ifndef QLINEAR_H
+#define QLINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* ql_stream_t;   /* same type as cudaStream_t */
+
+typedef enum {
+    QL_OK = 0,
+    QL_ERR_INVALID_ARG = 1,     /* null pointer, negative size, bad enum value */
+    QL_ERR_UNSUPPORTED = 2,     /* valid request this build does not implement */
+    QL_ERR_ALIGNMENT = 3,       /* pointer / stride alignment the kernel needs is not met */
+    QL_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed */
+    QL_ERR_DEVICE_TIMEOUT = 5   /* a kernel's bounded wait ran out (see ql_device_status) */
+} ql_status;
+
+typedef enum { QL_BF16 = 0, QL_F32 = 1 } ql_dtype;
+
+/* Scale-factor storage (the use_ue8m0 / use_packed_ue8m0 options of
+ * "deep-gemm: fused per-token FP8 cast in Triton (fused_per_token_cast_to_fp8),
+ * version 3" [description]):
+ *   QL_SF_FP32          fp32 scale = fl32(amax / 448)
+ *   QL_SF_UE8M0         fp32 tensor holding 2^ceil(log2(amax / 448)) (a power of two)
+ *   QL_SF_PACKED_UE8M0  int32 words, 4 biased-exponent bytes per word along the
+ *                       group axis: group g is byte (g % 4), little-endian, of
+ *                       word g / 4; bytes of groups past the last are 0.
+ * QL_CAST_RECIP_OF_SCALE may be OR-ed into the format of a cast with
+ * QL_SF_FP32: the quantisation factor is then fl32(1 / scale) instead of the
+ * default fl32(448 / amax) (both correctly rounded). */
+typedef enum { QL_SF_FP32 = 0, QL_SF_UE8M0 = 1, QL_SF_PACKED_UE8M0 = 2 } ql_sf_format;
+#define QL_CAST_RECIP_OF_SCALE 0x100
+
+/* Human-readable name of a status code (static storage). */
+const char* ql_status_string(ql_status s);
+
+/* ---------------------------------------------------------------------------
+ * fp8_cast_per_token
+ * Per-token cast of "DeepGEMM Essentials: High-Performance FP8 Matrix
+ * Multiplication" Part 3, with the options of "deep-gemm: fused per-token FP8
+ * cast in Triton (fused_per_token_cast_to_fp8), version 3" [description]
+ * (gran_k, UE8M0, packed UE8M0, in-place out / out_sf).
+ *
+ * For each row i and group g (columns [g*gran_k, min(n, (g+1)*gran_k))):
+ *   amax   = max(max_j |x[i,j]|, fl32(1e-4))      (exact, fp32)
+ *   scale  = fl32(amax / 448), rounded up to a power of two for UE8M0 formats
+ *   factor = fl32(448 / amax) for QL_SF_FP32 (fl32(1/scale) with
+ *            QL_CAST_RECIP_OF_SCALE); 1/scale (exact) for UE8M0 formats
+ *   out[i,j] = E4M3_rn(fl32(x[i,j] * factor))  (sign kept; |.| <= 448)
+ * The result is bit-exact (data and scale bytes).
+ *
+ *   x            [m, n] bf16 or fp32, element (i,j) at x[i*x_stride_m + j*x_stride_n].
+ *                A transposed view (x_stride_m == 1) casts along the other axis:
+ *                this is how the wgrad operands (dY^T, X^T) are produced.
+ *   gran_k       32 or 128.
+ *   fmt          ql_sf_format, optionally | QL_CAST_RECIP_OF_SCALE.
+ *   out          [m, n] E4M3 bytes at out[i*out_stride_m + j*out_stride_n].
+ *   out_sf       [m, ceil(n/gran_k)] fp32 at out_sf[i*sf_stride_m + g*sf_stride_g],
+ *                or for QL_SF_PACKED_UE8M0 [m, ceil(ceil(n/gran_k)/4)] int32 words
+ *                at out_sf[i*sf_stride_m + w*sf_stride_g]. sf_stride_m == 1 with
+ *                sf_stride_g a multiple of 4 gives the M-major, TMA-aligned
+ *                layout the GEMM's LHS scales use (Part 5).
+ * Fast paths: x_stride_n == 1 (rows contiguous) or x_stride_m == 1 (transposed),
+ * with out_stride_n == 1; any other strides use a slower generic kernel.
+ * m == 0 or n == 0 is a no-op. Returns QL_ERR_INVALID_ARG for null pointers with
+ * m*n > 0, negative sizes, gran_k not in {32,128}, or an unknown format.
+ * ------------------------------------------------------------------------- */
+ql_status fp8_cast_per_token(const void* x, ql_dtype x_dtype, int64_t m, int64_t n,
+                             int64_t x_stride_m, int64_t x_stride_n,
+                             int gran_k, int fmt,
+                             uint8_t* out, int64_t out_stride_m, int64_t out_stride_n,
+                             void* out_sf, int64_t sf_stride_m, int64_t sf_stride_g,
+                             ql_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * fp8_cast_per_block
+ * 128x128 block cast of "DeepGEMM Essentials" Part 4 (the RHS / weight cast).
+ * Same arithmetic as fp8_cast_per_token with the group being a 128x128 block
+ * (edge blocks partial). Scales fp32 [ceil(m/128), ceil(n/128)] at
+ * out_sf[r*sf_stride_r + c*sf_stride_c]; fmt is QL_SF_FP32 or QL_SF_UE8M0
+ * (optionally | QL_CAST_RECIP_OF_SCALE with QL_SF_FP32).
+ * Either view may be transposed: x_stride_m == 1 reads x column-wise, and
+ * out_stride_m == 1 writes the data transposed; since a block's amax does not
+ * depend on orientation, passing out = W^T's storage with transposed strides
+ * and out_sf with swapped strides yields cast_per_block(W^T) in the same pass
+ * (the dgrad operand of "[Help] Starter script for nn.Linear for fwd,bwd").
+ * ------------------------------------------------------------------------- */
+ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t n,
+                             int64_t x_stride_m, int64_t x_stride_n, int fmt,
+                             uint8_t* out, int64_t out_stride_m, int64_t out_stride_n,
+                             float* out_sf, int64_t sf_stride_r, int64_t sf_stride_c,
+                             ql_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gemm_fp8_nt_bf16
+ * D = A * B^T of "DeepGEMM Essentials" Parts 1 and 6 (gemm_fp8_fp8_bf16_nt),
+ * with the scale semantics of "[Help] Starter script for nn.Linear for fwd,bwd"
+ * (maintainer's reply: the RHS scale grid is read row-wise, one row
+ * (1, ceil(k/128)) per 128-row block of B, for every K block):
+ *
+ *   D[i,j] = bf16_rn( sum_kb sa[i,kb] * sb[j/128,kb] * sum_{k in kb} A[i,k] B[j,k] )
+ *
+ * accumulated in fp32, one promotion per 128-wide K block.
+ *   a    [m, k] E4M3, row stride lda bytes (K contiguous).
+ *   sfa  [m, ceil(k/128)] scales at sfa[i*sfa_stride_m + kb*sfa_stride_k]
+ *        (fp32 values for QL_SF_FP32 / QL_SF_UE8M0; for QL_SF_PACKED_UE8M0
+ *        int32 words with kb -> byte kb%4 of word kb/4, i.e. stride_k counts words).
+ *   b    [n, k] E4M3, row stride ldb bytes.
+ *   sfb  [ceil(n/128), ceil(k/128)] at sfb[r*sfb_stride_n + kb*sfb_stride_k], same format.
+ *   d    [m, n] bf16 at d[i*ldd + j].
+ *   workspace / ws_bytes: reserved, may be NULL / 0 (ql_gemm_workspace_size returns 0).
+ * Requirements (QL_ERR_ALIGNMENT otherwise): a, b 16-byte aligned; lda, ldb
+ * multiples of 16; k a multiple of 16 (the tensor-memory-access unit moves
+ * 16-byte rows). m == 0 or n == 0 is a no-op; k == 0 writes D = 0.
+ * ------------------------------------------------------------------------- */
+ql_status gemm_fp8_nt_bf16(const uint8_t* a, int64_t lda, const void* sfa,
+                           int64_t sfa_stride_m, int64_t sfa_stride_k,
+                           const uint8_t* b, int64_t ldb, const void* sfb,
+                           int64_t sfb_stride_n, int64_t sfb_stride_k,
+                           int fmt, uint16_t* d, int64_t ldd,
+                           int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t ws_bytes, ql_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gemm_fp8_wgrad_fp32
+ * The weight-gradient GEMM (wgrad_gemm_fp8_fp8_fp32_nt) of "[Help] Starter
+ * script for nn.Linear for fwd,bwd" and "DeepGEMM Essentials" Parts 12-13:
+ * both operands carry 1x128 per-row scales along K (K = tokens), output fp32:
+ *
+ *   D[i,j] (+)= sum_kb sa[i,kb] * sb[j,kb] * sum_{k in kb} A[i,k] B[j,k]
+ *
+ *   sfb  [n, ceil(k/128)] at sfb[j*sfb_stride_n + kb*sfb_stride_k].
+ *   d    [m, n] fp32 at d[i*ldd + j]; accumulate != 0 adds to the existing D.
+ * Other arguments and requirements as gemm_fp8_nt_bf16.
+ * ------------------------------------------------------------------------- */
+ql_status gemm_fp8_wgrad_fp32(const uint8_t* a, int64_t lda, const void* sfa,
+                              int64_t sfa_stride_m, int64_t sfa_stride_k,
+                              const uint8_t* b, int64_t ldb, const void* sfb,
+                              int64_t sfb_stride_n, int64_t sfb_stride_k,
+                              int fmt, float* d, int64_t ldd,
+                              int64_t m, int64_t n, int64_t k, int accumulate,
+                              void* workspace, size_t ws_bytes, ql_stream_t stream);
+
+/* Workspace bytes a GEMM of this shape needs (0 in this build). */
+size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k);
+
+/* ---------------------------------------------------------------------------
+ * Knobs ("DeepGEMM Essentials" Part 15: get_num_sms / set_num_sms).
+ * The GEMM's persistent grid uses at most this many SMs (default: all SMs of
+ * the current device). ql_set_num_sms(n <= 0) restores the default.
+ * The setting is process-wide.
+ * ------------------------------------------------------------------------- */
+ql_status ql_set_num_sms(int num_sms);
+int ql_get_num_sms(void);
+
+/* Tile width (columns of D per tile) of the GEMM: 32, 64, 128 or 256; 0
+ * (default) lets the library choose from the shape. Process-wide; meant for
+ * tuning and for tests that exercise every tile width. */
+ql_status ql_set_gemm_block_n(int block_n);
+
+/* Time limit of every bounded wait inside the GEMM kernel, in milliseconds
+ * (default 2000). After it runs out the kernel records QL_ERR_DEVICE_TIMEOUT,
+ * drains its own copies, frees its tensor memory and returns. Process-wide. */
+ql_status ql_set_wait_limit_ms(int ms);
+
+/* Synchronises `stream`, then returns and clears the device status word:
+ * QL_OK, or QL_ERR_DEVICE_TIMEOUT if any kernel's bounded wait ran out since
+ * the last call; QL_ERR_CUDA if the synchronisation itself failed. */
+ql_status ql_device_status(ql_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QLINEAR_H */

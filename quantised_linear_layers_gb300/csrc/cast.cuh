@@ -1,0 +1,36 @@
+// Launch arguments of the cast kernels (validated by the C ABI layer).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ql {
+
+struct CastTokenArgs {
+    const void* x;
+    bool is_bf16;
+    int64_t m, n, sxm, sxn;
+    int gran;      // 32 | 128
+    int fmt;       // 0 fp32, 1 UE8M0 (fp32 storage), 2 packed UE8M0
+    bool recip;    // factor = 1 / scale (fp32 format only)
+    uint8_t* out;
+    int64_t som, son;
+    void* sf;
+    int64_t ssm, ssg;
+};
+
+struct CastBlockArgs {
+    const void* x;
+    bool is_bf16;
+    int64_t m, n, sxm, sxn;
+    int fmt;       // 0 fp32, 1 UE8M0 (fp32 storage)
+    bool recip;
+    uint8_t* out;
+    int64_t som, son;
+    float* sf;
+    int64_t ssr, ssc;
+};
+
+cudaError_t launch_cast_per_token(const CastTokenArgs& a, cudaStream_t st, int num_sms);
+cudaError_t launch_cast_per_block(const CastBlockArgs& a, cudaStream_t st);
+
+}  // namespace ql

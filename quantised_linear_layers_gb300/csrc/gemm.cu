@@ -1,0 +1,500 @@
+// Block-scaled FP8 GEMM for sm_103a: D = A * B^T.
+//
+// "DeepGEMM Essentials: High-Performance FP8 Matrix Multiplication" Parts 1, 6
+// (gemm_fp8_fp8_bf16_nt) and 12-13 (wgrad_gemm_fp8_fp8_fp32_nt); scale
+// semantics of "[Help] Starter script for nn.Linear for fwd,bwd" (maintainer's
+// reply: one row (1, ceil(k/128)) of the RHS scale grid per 128-row block of B,
+// used for all K blocks):
+//
+//   D[i,j] = sum_kb sa[i,kb] * sb(j,kb) * P_kb[i,j],  P_kb = sum_{k in kb} A[i,k] B[j,k]
+//
+// Design (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer: A tile [128 x 128 B] and B tile [BN x 128 B] per
+//               128-wide K block into a STAGES-deep shared-memory ring
+//               (128-byte swizzle).
+//   warp 1      owns tensor memory; one elected lane issues four
+//               tcgen05.mma.kind::f8f6f4 (K = 32 each) per K block into a fresh
+//               TMEM accumulator stage, then commits to free the smem stage and
+//               to publish the stage to the math warps.
+//   warps 2-3   scale loaders: sa[128 rows] and sb (one value per 128-column
+//               block, or one per column for wgrad) of each K block into a
+//               shared-memory scale ring (any scale strides; packed UE8M0 is
+//               decoded here).
+//   warps 4-11  two math warpgroups: each thread owns one accumulator row and
+//               BN/2 columns in registers; per K block it reads P_kb from TMEM
+//               (tcgen05.ld) and promotes acc += (sa*sb) * P_kb with packed
+//               fp32x2 FMAs; after the last K block it writes bf16 (or fp32,
+//               optionally accumulated) output.
+// Tiles are 128 x BN (BN in {256,128,64,32}), visited in grouped raster order
+// (GROUP_M m-blocks share each n-block sweep) for L2 reuse. Every wait is
+// bounded in time; on a time-out the CTA raises the device status word,
+// drains its own copies and MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "gemm.cuh"
+
+namespace ql {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kMathThreads = 256;
+constexpr int BM = 128;
+constexpr int BK = 128;         // K block = scale granularity
+constexpr int kScaleSlots = 8;
+
+template <int BN, bool PER_ROW_B>
+struct Cfg {
+    static constexpr int kStageA = BM * BK;                  // bytes
+    static constexpr int kStageB = BN * BK;
+    static constexpr int kStageBytes = kStageA + kStageB;
+    static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int kTmemStages = (512 / BN) < 4 ? (512 / BN) : 4;
+    static constexpr int kTmemColsUsed = kTmemStages * BN;
+    static constexpr int kTmemCols = kTmemColsUsed <= 32 ? 32 : (kTmemColsUsed <= 64 ? 64 : (kTmemColsUsed <= 128 ? 128 : (kTmemColsUsed <= 256 ? 256 : 512)));
+    static constexpr int kSbPerSlot = PER_ROW_B ? BN : 4;
+    static constexpr int kSlotFloats = BM + kSbPerSlot;
+    static constexpr int kColsPerThread = BN / 2;
+    // shared memory layout (offsets from a 1024-aligned base)
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kStageA;
+    static constexpr int kOffScale = kOffB + kStages * kStageB;
+    static constexpr int kOffBar = kOffScale + kScaleSlots * kSlotFloats * 4;
+    static constexpr int kNumBars = 2 * kStages + 2 * kTmemStages + 2 * kScaleSlots + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kColsPerThread % 16 == 0, "columns per thread");
+};
+
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb) {
+    const int group_size = p.group_m * p.tiles_n;
+    const int group = t / group_size;
+    const int first_m = group * p.group_m;
+    const int rem = p.tiles_m - first_m;
+    const int gm = rem < p.group_m ? rem : p.group_m;
+    const int w = t - group * group_size;
+    mb = first_m + w % gm;
+    nb = w / gm;
+}
+
+__device__ __forceinline__ float decode_scale(const void* base, int fmt, int64_t row_off, int kb, int64_t sk) {
+    if (fmt != 2) return __ldg(static_cast<const float*>(base) + row_off + kb * sk);
+    const uint32_t w = __ldg(static_cast<const uint32_t*>(base) + row_off + (kb >> 2) * sk);
+    const uint32_t e = (w >> (8 * (kb & 3))) & 0xFFu;
+    return __uint_as_float(e ? (e << 23) : 0x00400000u);   // 2^(e-127)
+}
+
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+    return static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
+}
+
+// acc2 = p2 * s2 + acc2 on two fp32 lanes at once
+__device__ __forceinline__ void fma2(uint64_t& acc2, uint64_t p2, uint64_t s2) {
+    asm volatile("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(p2), "l"(s2));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a2, uint64_t b2) {
+    uint64_t r;
+    asm volatile("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a2), "l"(b2));
+    return r;
+}
+
+// Reads N (16, 32 or 64) consecutive fp32 accumulator columns of this warp's
+// 32 TMEM lanes and waits for them.
+template <int N>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&v)[N]) {
+    if constexpr (N == 16) {
+        tmem_ld_32x32b_x16(taddr, v);
+    } else if constexpr (N == 32) {
+        tmem_ld_32x32b_x32(taddr, v);
+    } else {
+        static_assert(N == 64, "16, 32 or 64 columns");
+        tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+    }
+    tmem_wait_ld(v);
+}
+
+// Bounded wait whose outcome is the same for every lane of the warp (the
+// .sync.aligned tensor-memory loads that follow need a converged warp).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl)) != 0;
+}
+
+template <int BN, bool PER_ROW_B, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const GemmParams p) {
+    using C = Cfg<BN, PER_ROW_B>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem + C::kOffA;
+    uint8_t* sB = smem + C::kOffB;
+    float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* full = bars;
+    uint64_t* empty = full + C::kStages;
+    uint64_t* tfull = empty + C::kStages;
+    uint64_t* tempty = tfull + C::kTmemStages;
+    uint64_t* sfull = tempty + C::kTmemStages;
+    uint64_t* sempty = sfull + kScaleSlots;
+    uint64_t* done_bar = sempty + kScaleSlots;
+    uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < C::kTmemStages; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], kMathThreads); }
+        for (int s = 0; s < kScaleSlots; ++s) { mbar_init(&sfull[s], 32); mbar_init(&sempty[s], kMathThreads); }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmap_a); tma_prefetch_desc(&tmap_b); }
+    if (warp == 1) { tmem_alloc(tmem_base_sm, C::kTmemCols); tmem_relinquish(); }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_base_sm;
+
+    const WaitCtl ctl{abort_flag, p.dev_status, p.wait_limit_ns};
+    const int num_tiles = p.tiles_m * p.tiles_n;
+    const int num_kb = p.num_kb;
+
+    if (warp < 4) {
+        regs_dealloc<56>();
+        if (warp == 0) {
+            // ---------------- TMA producer ----------------
+            if (elect_one()) {
+                uint32_t it = 0;
+                bool ok = true;
+                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    int mb, nb;
+                    tile_coords(t, p, mb, nb);
+                    for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                        const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
+                        if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                        tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], kb * BK, mb * BM);
+                        tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, nb * BN);
+                    }
+                }
+                if (!ok) {
+                    // drain: every stage whose load was issued completes its phase
+                    const uint32_t first = it > (uint32_t)C::kStages ? it - C::kStages : 0u;
+                    for (uint32_t j = first; j < it; ++j)
+                        mbar_wait_drain(&full[j % C::kStages], (j / C::kStages) & 1u, p.wait_limit_ns);
+                }
+            }
+            __syncwarp();
+        } else if (warp == 1) {
+            // ---------------- MMA issuer ----------------
+            if (elect_one()) {
+                constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+                uint32_t it = 0, tc = 0;
+                bool ok = true;
+                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    for (int kb = 0; kb < num_kb; ++kb, ++it, ++tc) {
+                        const uint32_t ts = tc % C::kTmemStages, tph = (tc / C::kTmemStages) & 1u;
+                        if (!mbar_wait(&tempty[ts], tph ^ 1u, ctl)) { ok = false; break; }
+                        tc_fence_after_sync();
+                        const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
+                        if (!mbar_wait(&full[s], ph, ctl)) { ok = false; break; }
+                        tc_fence_after_sync();
+                        const uint64_t adesc = sw128_kmajor_desc(smem_addr(sA + s * C::kStageA));
+                        const uint64_t bdesc = sw128_kmajor_desc(smem_addr(sB + s * C::kStageB));
+                        const uint32_t d_tmem = tmem_base + ts * BN;
+#pragma unroll
+                        for (int k4 = 0; k4 < BK / 32; ++k4)   // +32 bytes along K = +2 in the address field
+                            mma_e4m3(d_tmem, adesc + 2 * k4, bdesc + 2 * k4, idesc, k4 > 0 ? 1u : 0u);
+                        mma_commit(&empty[s]);
+                        mma_commit(&tfull[ts]);
+                    }
+                }
+                // all MMAs issued by this thread have completed before tensor memory is freed
+                mma_commit(done_bar);
+                mbar_wait_drain(done_bar, 0, p.wait_limit_ns);
+            }
+            __syncwarp();
+        } else {
+            // ---------------- scale loaders (warps 2, 3: alternate K blocks) ----------------
+            const uint32_t mine = static_cast<uint32_t>(warp - 2);
+            uint32_t g = 0;
+            bool ok = true;
+            const int64_t nblocks_b = (p.n + 127) / 128;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, p, mb, nb);
+                const int64_t m0 = static_cast<int64_t>(mb) * BM, n0 = static_cast<int64_t>(nb) * BN;
+                for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                    if ((g & 1u) != mine) continue;
+                    const uint32_t slot = g % kScaleSlots, ph = (g / kScaleSlots) & 1u;
+                    if (!warp_wait(&sempty[slot], ph ^ 1u, ctl)) { ok = false; break; }
+                    float* dst = sScale + slot * C::kSlotFloats;
+                    float va[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int64_t row = m0 + lane + 32 * i;
+                        va[i] = row < p.m ? decode_scale(p.sfa, p.fmt, row * p.sam, kb, p.sak) : 0.0f;
+                    }
+                    if constexpr (PER_ROW_B) {
+                        float vb[BN / 32];
+#pragma unroll
+                        for (int i = 0; i < BN / 32; ++i) {
+                            const int64_t col = n0 + lane + 32 * i;
+                            vb[i] = col < p.n ? decode_scale(p.sfb, p.fmt, col * p.sbn, kb, p.sbk) : 0.0f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < BN / 32; ++i) dst[BM + lane + 32 * i] = vb[i];
+                    } else {
+                        if (lane < (BN + 127) / 128) {
+                            const int64_t r = n0 / 128 + lane;
+                            dst[BM + lane] = r < nblocks_b ? decode_scale(p.sfb, p.fmt, r * p.sbn, kb, p.sbk) : 0.0f;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = va[i];
+                    mbar_arrive(&sfull[slot]);
+                }
+            }
+        }
+    } else {
+        regs_alloc<224>();
+        // ---------------- math warpgroups: promotion + epilogue ----------------
+        constexpr int CPT = C::kColsPerThread;
+        const int wg = (warp - 4) >> 2;          // column half
+        const int q = warp & 3;                  // TMEM lane quarter
+        const int r_local = q * 32 + lane;       // accumulator row in the tile
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        const bool vec_store = p.vec_store != 0;
+        float acc[CPT];
+        uint32_t g = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
+            for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                const uint32_t slot = g % kScaleSlots, sph = (g / kScaleSlots) & 1u;
+                const uint32_t ts = g % C::kTmemStages, tph = (g / C::kTmemStages) & 1u;
+                if (!warp_wait(&sfull[slot], sph, ctl)) { ok = false; break; }
+                const float* src = sScale + slot * C::kSlotFloats;
+                const float sa = src[r_local];
+                if (!warp_wait(&tfull[ts], tph, ctl)) { ok = false; break; }
+                tc_fence_after_sync();
+                const uint32_t tcol = tmem_base + lane_base + ts * BN + wg * CPT;
+                constexpr int U = CPT < 64 ? CPT : 64;     // columns per TMEM read round
+                if constexpr (!PER_ROW_B) {
+                    const float sab = sa * src[BM + ((BN == 256) ? wg : 0)];
+                    const uint64_t s2 = pack2(sab, sab);
+#pragma unroll
+                    for (int c0 = 0; c0 < CPT; c0 += U) {
+                        uint32_t v[U];
+                        tmem_load_cols<U>(tcol + c0, v);
+                        if (c0 + U == CPT) {              // last read of this stage
+                            tc_fence_before_sync();
+                            mbar_arrive(&tempty[ts]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < U; j += 2) {
+                            uint64_t a2 = pack2(acc[c0 + j], acc[c0 + j + 1]);
+                            fma2(a2, pack2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2);
+                            acc[c0 + j] = __uint_as_float(static_cast<uint32_t>(a2));
+                            acc[c0 + j + 1] = __uint_as_float(static_cast<uint32_t>(a2 >> 32));
+                        }
+                    }
+                    mbar_arrive(&sempty[slot]);
+                } else {
+                    const uint64_t sa2 = pack2(sa, sa);
+#pragma unroll
+                    for (int c0 = 0; c0 < CPT; c0 += U) {
+                        uint32_t v[U];
+                        tmem_load_cols<U>(tcol + c0, v);
+                        if (c0 + U == CPT) {
+                            tc_fence_before_sync();
+                            mbar_arrive(&tempty[ts]);
+                        }
+                        const float* sbp = src + BM + wg * CPT + c0;
+#pragma unroll
+                        for (int j = 0; j < U; j += 2) {
+                            const uint64_t s2 = mul2(sa2, pack2(sbp[j], sbp[j + 1]));
+                            uint64_t a2 = pack2(acc[c0 + j], acc[c0 + j + 1]);
+                            fma2(a2, pack2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2);
+                            acc[c0 + j] = __uint_as_float(static_cast<uint32_t>(a2));
+                            acc[c0 + j + 1] = __uint_as_float(static_cast<uint32_t>(a2 >> 32));
+                        }
+                    }
+                    mbar_arrive(&sempty[slot]);
+                }
+            }
+            if (!ok) break;
+            // ---------------- epilogue ----------------
+            const int64_t row = static_cast<int64_t>(mb) * BM + r_local;
+            const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
+            if (row < p.m) {
+                if constexpr (!OUT_F32) {
+                    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
+#pragma unroll
+                    for (int j = 0; j < CPT; j += 8) {
+                        const int64_t c = col0 + j;
+                        if (vec_store && c + 8 <= p.n) {
+                            uint4 u;
+                            __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[j], acc[j + 1]);
+                            __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
+                            __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
+                            u.x = *reinterpret_cast<uint32_t*>(&h0);
+                            u.y = *reinterpret_cast<uint32_t*>(&h1);
+                            u.z = *reinterpret_cast<uint32_t*>(&h2);
+                            u.w = *reinterpret_cast<uint32_t*>(&h3);
+                            *reinterpret_cast<uint4*>(drow + c) = u;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (c + e < p.n) drow[c + e] = __float2bfloat16_rn(acc[j + e]);
+                        }
+                    }
+                } else {
+                    float* drow = static_cast<float*>(p.d) + row * p.ldd;
+#pragma unroll
+                    for (int j = 0; j < CPT; j += 4) {
+                        const int64_t c = col0 + j;
+                        if (vec_store && c + 4 <= p.n) {
+                            float4 o = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                            if (p.accumulate) {
+                                const float4 old = *reinterpret_cast<const float4*>(drow + c);
+                                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+                            }
+                            *reinterpret_cast<float4*>(drow + c) = o;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (c + e < p.n) drow[c + e] = p.accumulate ? drow[c + e] + acc[j + e] : acc[j + e];
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D uint8 tensor [rows, cols] (cols contiguous, row stride ld bytes), box
+// [box_rows, 128 bytes], 128-byte swizzle, zero fill out of bounds.
+bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool PER_ROW_B, bool OUT_F32>
+cudaError_t launch_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
+    using Cf = Cfg<BN, PER_ROW_B>;
+    CUtensorMap ta, tb;
+    if (!make_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)) return cudaErrorInvalidValue;
+    if (!make_kmajor_map(&tb, L.b, L.n, L.k, L.ldb, BN)) return cudaErrorInvalidValue;
+    p.tiles_m = static_cast<int>((L.m + BM - 1) / BM);
+    p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
+    const int tiles = p.tiles_m * p.tiles_n;
+    int grid = tiles < num_sms ? tiles : num_sms;
+    auto kern = gemm_fp8_kernel<BN, PER_ROW_B, OUT_F32>;
+    static bool attr_done = false;   // per instantiation
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    kern<<<grid, kThreads, Cf::kSmemBytes, st>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+template <bool PER_ROW_B, bool OUT_F32>
+cudaError_t dispatch_bn(int bn, const GemmLaunch& L, const GemmParams& p, cudaStream_t st, int num_sms) {
+    switch (bn) {
+        case 256: return launch_t<256, PER_ROW_B, OUT_F32>(L, p, st, num_sms);
+        case 128: return launch_t<128, PER_ROW_B, OUT_F32>(L, p, st, num_sms);
+        case 64: return launch_t<64, PER_ROW_B, OUT_F32>(L, p, st, num_sms);
+        default: return launch_t<32, PER_ROW_B, OUT_F32>(L, p, st, num_sms);
+    }
+}
+
+}  // namespace
+
+int choose_block_n(int64_t m, int64_t n, int num_sms) {
+    const int64_t tm = (m + BM - 1) / BM;
+    const int cands[4] = {256, 128, 64, 32};
+    for (int i = 0; i < 4; ++i) {
+        const int64_t tiles = tm * ((n + cands[i] - 1) / cands[i]);
+        if (tiles >= num_sms) return cands[i];
+    }
+    return 32;
+}
+
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
+    GemmParams p{};
+    p.m = L.m;
+    p.n = L.n;
+    p.num_kb = static_cast<int>((L.k + BK - 1) / BK);
+    p.sfa = L.sfa;
+    p.sam = L.sam;
+    p.sak = L.sak;
+    p.sfb = L.sfb;
+    p.sbn = L.sbn;
+    p.sbk = L.sbk;
+    p.fmt = L.fmt;
+    p.d = L.d;
+    p.ldd = L.ldd;
+    p.accumulate = L.accumulate;
+    p.group_m = 16;
+    p.dev_status = L.dev_status;
+    p.wait_limit_ns = L.wait_limit_ns;
+    const int64_t es = L.out_f32 ? 4 : 2;
+    p.vec_store = ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && (L.ldd * es) % 16 == 0) ? 1 : 0;
+    const int bn = L.block_n > 0 ? L.block_n : choose_block_n(L.m, L.n, num_sms);
+    if (L.out_f32) return dispatch_bn<true, true>(bn, L, p, st, num_sms);
+    return dispatch_bn<false, false>(bn, L, p, st, num_sms);
+}
+
+}  // namespace ql

@@ -1,0 +1,224 @@
+"""Thin ctypes binding over libqlinear.so (include/qlinear.h).
+
+Argument marshalling only: every step of the cast and the GEMM runs in the
+library's CUDA kernels. torch supplies device memory and the current stream.
+If the library is missing or cannot be loaded every op raises; there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqlinear.so")
+
+QL_BF16, QL_F32 = 0, 1
+SF_FP32, SF_UE8M0, SF_PACKED_UE8M0 = 0, 1, 2
+CAST_RECIP_OF_SCALE = 0x100
+
+_lock = threading.Lock()
+_lib = None
+
+_i64, _vp, _int, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+_SIGS = {
+    "fp8_cast_per_token": [_vp, _int, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp],
+    "fp8_cast_per_block": [_vp, _int, _i64, _i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp],
+    "gemm_fp8_nt_bf16": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
+                         _i64, _i64, _i64, _vp, _sz, _vp],
+    "gemm_fp8_wgrad_fp32": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
+                            _i64, _i64, _i64, _int, _vp, _sz, _vp],
+    "ql_gemm_workspace_size": [_i64, _i64, _i64],
+    "ql_set_num_sms": [_int],
+    "ql_get_num_sms": [],
+    "ql_set_wait_limit_ms": [_int],
+    "ql_set_gemm_block_n": [_int],
+    "ql_device_status": [_vp],
+    "ql_status_string": [_int],
+}
+
+
+class QLError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg}")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libqlinear.so (raises if it is missing: no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"libqlinear.so not found at {path}; run quantised_linear_layers_gb300.build.build()")
+            lib = ctypes.CDLL(path)
+            for name, args in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = _int
+            lib.ql_status_string.restype = ctypes.c_char_p
+            lib.ql_gemm_workspace_size.restype = _sz
+            _lib = lib
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        msg = load_library().ql_status_string(status).decode()
+        raise QLError(fn, status, msg)
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _dtype_code(x: torch.Tensor) -> int:
+    if x.dtype == torch.bfloat16:
+        return QL_BF16
+    if x.dtype == torch.float32:
+        return QL_F32
+    raise TypeError(f"input must be bfloat16 or float32, got {x.dtype}")
+
+
+def _bytes8(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"expected an E4M3 (float8_e4m3fn or uint8) tensor, got {t.dtype}")
+    return t
+
+
+def _ceil(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def sf_shape(n: int, gran_k: int, fmt: int) -> int:
+    """Number of scale columns per row: groups, or int32 words for packed UE8M0."""
+    g = _ceil(n, gran_k)
+    return _ceil(g, 4) if (fmt & 0xFF) == SF_PACKED_UE8M0 else g
+
+
+def empty_sf(m: int, cols: int, fmt: int, device, mn_major: bool = False) -> torch.Tensor:
+    """Scale tensor [m, cols]; mn_major gives the M-major, TMA-aligned layout
+    (stride (1, align(m, 4)))."""
+    dt = torch.int32 if (fmt & 0xFF) == SF_PACKED_UE8M0 else torch.float32
+    if not mn_major:
+        return torch.empty((m, cols), dtype=dt, device=device)
+    ld = _ceil(max(m, 1), 4) * 4
+    return torch.empty((cols, ld), dtype=dt, device=device).t()[:m]
+
+
+def fp8_cast_per_token(x: torch.Tensor, gran_k: int = 128, fmt: int = SF_FP32, recip: bool = False,
+                       out: torch.Tensor | None = None, out_sf: torch.Tensor | None = None,
+                       sf_mn_major: bool = False):
+    """Per-token FP8 cast of a 2-D bf16/fp32 tensor (any strides).
+
+    Returns (data float8_e4m3fn [m, n], scales). ``out`` / ``out_sf`` may be
+    views of larger buffers; only their elements are written."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D")
+    m, n = x.shape
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float8_e4m3fn, device=x.device)
+    if out_sf is None:
+        out_sf = empty_sf(m, sf_shape(n, gran_k, fmt), fmt, x.device, sf_mn_major)
+    _bytes8(out)
+    code = fmt | (CAST_RECIP_OF_SCALE if recip else 0)
+    st = load_library().fp8_cast_per_token(
+        x.data_ptr(), _dtype_code(x), m, n, x.stride(0), x.stride(1), gran_k, code,
+        out.data_ptr(), out.stride(0), out.stride(1), out_sf.data_ptr(), out_sf.stride(0), out_sf.stride(1),
+        _stream(x))
+    _check("fp8_cast_per_token", st)
+    return out, out_sf
+
+
+def fp8_cast_per_block(x: torch.Tensor, fmt: int = SF_FP32, recip: bool = False,
+                       out: torch.Tensor | None = None, out_sf: torch.Tensor | None = None):
+    """128x128 block FP8 cast. Returns (data [m, n], scales fp32 [ceil(m/128), ceil(n/128)]).
+    ``out`` / ``out_sf`` may be transposed views (e.g. ``wt.t()``) to write W^T's cast."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D")
+    m, n = x.shape
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float8_e4m3fn, device=x.device)
+    if out_sf is None:
+        out_sf = torch.empty((_ceil(m, 128), _ceil(n, 128)), dtype=torch.float32, device=x.device)
+    _bytes8(out)
+    code = fmt | (CAST_RECIP_OF_SCALE if recip else 0)
+    st = load_library().fp8_cast_per_block(
+        x.data_ptr(), _dtype_code(x), m, n, x.stride(0), x.stride(1), code,
+        out.data_ptr(), out.stride(0), out.stride(1), out_sf.data_ptr(), out_sf.stride(0), out_sf.stride(1),
+        _stream(x))
+    _check("fp8_cast_per_block", st)
+    return out, out_sf
+
+
+def _gemm_args(a, sfa, b, sfb):
+    _bytes8(a)
+    _bytes8(b)
+    if a.dim() != 2 or b.dim() != 2 or a.stride(1) != 1 or b.stride(1) != 1:
+        raise ValueError("a and b must be 2-D with contiguous K")
+    if a.shape[1] != b.shape[1]:
+        raise ValueError("a and b must share K")
+    return a.shape[0], b.shape[0], a.shape[1]
+
+
+def gemm_fp8_nt_bf16(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor,
+                     fmt: int = SF_FP32, out: torch.Tensor | None = None) -> torch.Tensor:
+    """D = A B^T, bf16 [m, n]: A [m, k] with 1x128 scales sfa [m, ceil(k/128)],
+    B [n, k] with 128x128 scales sfb [ceil(n/128), ceil(k/128)] (packed UE8M0:
+    int32 words along K)."""
+    m, n, k = _gemm_args(a, sfa, b, sfb)
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    if out.dtype != torch.bfloat16 or out.stride(1) != 1:
+        raise ValueError("out must be bf16 with contiguous rows")
+    st = load_library().gemm_fp8_nt_bf16(
+        a.data_ptr(), a.stride(0), sfa.data_ptr(), sfa.stride(0), sfa.stride(1),
+        b.data_ptr(), b.stride(0), sfb.data_ptr(), sfb.stride(0), sfb.stride(1),
+        fmt, out.data_ptr(), out.stride(0), m, n, k, None, 0, _stream(a))
+    _check("gemm_fp8_nt_bf16", st)
+    return out
+
+
+def gemm_fp8_wgrad_fp32(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor,
+                        out: torch.Tensor | None = None, accumulate: bool = False,
+                        fmt: int = SF_FP32) -> torch.Tensor:
+    """D (+)= A B^T, fp32 [m, n]: both operands with 1x128 per-row scales along K."""
+    m, n, k = _gemm_args(a, sfa, b, sfb)
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate needs an existing out")
+        out = torch.empty((m, n), dtype=torch.float32, device=a.device)
+    if out.dtype != torch.float32 or out.stride(1) != 1:
+        raise ValueError("out must be fp32 with contiguous rows")
+    st = load_library().gemm_fp8_wgrad_fp32(
+        a.data_ptr(), a.stride(0), sfa.data_ptr(), sfa.stride(0), sfa.stride(1),
+        b.data_ptr(), b.stride(0), sfb.data_ptr(), sfb.stride(0), sfb.stride(1),
+        fmt, out.data_ptr(), out.stride(0), m, n, k, int(bool(accumulate)), None, 0, _stream(a))
+    _check("gemm_fp8_wgrad_fp32", st)
+    return out
+
+
+def set_num_sms(n: int) -> None:
+    _check("ql_set_num_sms", load_library().ql_set_num_sms(int(n)))
+
+
+def get_num_sms() -> int:
+    return int(load_library().ql_get_num_sms())
+
+
+def set_gemm_block_n(bn: int) -> None:
+    _check("ql_set_gemm_block_n", load_library().ql_set_gemm_block_n(int(bn)))
+
+
+def set_wait_limit_ms(ms: int) -> None:
+    _check("ql_set_wait_limit_ms", load_library().ql_set_wait_limit_ms(int(ms)))
+
+
+def device_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device status code."""
+    s = torch.cuda.current_stream(device).cuda_stream
+    return int(load_library().ql_device_status(s))

@@ -1,0 +1,105 @@
+"""The C ABI boundary, without a GPU: libqlinear.so builds for sm_103a, loads,
+exports every function include/qlinear.h declares, and rejects invalid
+arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qlinear.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\([^;{]*\)\s*;", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantised_linear_layers_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path), path
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fp8_cast_per_token", "fp8_cast_per_block", "gemm_fp8_nt_bf16", "gemm_fp8_wgrad_fp32",
+                     "ql_status_string", "ql_set_num_sms", "ql_get_num_sms", "ql_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    cdll, path = lib
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, f"not exported: {missing}"
+    for n in declared_functions():
+        assert hasattr(cdll, n)
+
+
+def test_library_targets_sm103a(lib):
+    _, path = lib
+    out = subprocess.run(["cuobjdump", "--list-elf", path], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_status_strings(lib):
+    cdll, _ = lib
+    cdll.ql_status_string.restype = ctypes.c_char_p
+    assert cdll.ql_status_string(0) == b"QL_OK"
+    for s in range(1, 6):
+        assert cdll.ql_status_string(s).startswith(b"QL_ERR_")
+
+
+def test_host_validation_rejects_before_cuda(lib):
+    """These calls must return QL_ERR_INVALID_ARG from host checks alone."""
+    from quantised_linear_layers_gb300 import ops
+    ops.load_library()
+    L = ops.load_library()
+    p = ctypes.c_void_p(16)
+    # gran_k 64 is not supported
+    assert L.fp8_cast_per_token(p, 0, 4, 256, 256, 1, 64, 0, p, 256, 1, p, 2, 1, None) == 1
+    # negative size
+    assert L.fp8_cast_per_token(p, 0, -1, 256, 256, 1, 128, 0, p, 256, 1, p, 2, 1, None) == 1
+    # unknown format, recip with UE8M0
+    assert L.fp8_cast_per_token(p, 0, 4, 256, 256, 1, 128, 7, p, 256, 1, p, 2, 1, None) == 1
+    assert L.fp8_cast_per_token(p, 0, 4, 256, 256, 1, 128, 0x101, p, 256, 1, p, 2, 1, None) == 1
+    # bad dtype; null pointers
+    assert L.fp8_cast_per_token(p, 9, 4, 256, 256, 1, 128, 0, p, 256, 1, p, 2, 1, None) == 1
+    assert L.fp8_cast_per_token(None, 0, 4, 256, 256, 1, 128, 0, p, 256, 1, p, 2, 1, None) == 1
+    # block cast: packed format is not a block format
+    assert L.fp8_cast_per_block(p, 0, 4, 256, 256, 1, 2, p, 256, 1, p, 2, 1, None) == 1
+    # empty problems are no-ops (no CUDA call)
+    assert L.fp8_cast_per_token(None, 0, 0, 256, 256, 1, 128, 0, None, 256, 1, None, 2, 1, None) == 0
+    assert L.gemm_fp8_nt_bf16(None, 16, None, 1, 1, None, 16, None, 1, 1, 0, None, 16, 0, 16, 16, None, 0,
+                              None) == 0
+    # GEMM: bad format, null operands, short leading dimension
+    assert L.gemm_fp8_nt_bf16(p, 32, p, 1, 1, p, 32, p, 1, 1, 5, p, 8, 4, 8, 32, None, 0, None) == 1
+    assert L.gemm_fp8_nt_bf16(None, 32, p, 1, 1, p, 32, p, 1, 1, 0, p, 8, 4, 8, 32, None, 0, None) == 1
+    assert L.gemm_fp8_nt_bf16(p, 16, p, 1, 1, p, 32, p, 1, 1, 0, p, 8, 4, 8, 32, None, 0, None) == 1
+    # misaligned operand pointer / leading dimension
+    q = ctypes.c_void_p(24)
+    assert L.gemm_fp8_nt_bf16(q, 32, p, 1, 1, p, 32, p, 1, 1, 0, p, 8, 4, 8, 32, None, 0, None) == 3
+    assert L.gemm_fp8_nt_bf16(p, 40, p, 1, 1, p, 32, p, 1, 1, 0, p, 8, 4, 8, 32, None, 0, None) == 3
+    assert L.ql_set_gemm_block_n(48) == 1
+    assert L.ql_set_wait_limit_ms(0) == 1
+
+
+def test_ops_fail_loudly_without_library(tmp_path):
+    from quantised_linear_layers_gb300 import ops
+    import quantised_linear_layers_gb300.ops as mod
+    saved = mod._lib
+    mod._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="not found"):
+            ops.load_library(str(tmp_path / "missing.so"))
+    finally:
+        mod._lib = saved

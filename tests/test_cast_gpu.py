@@ -1,0 +1,205 @@
+"""GPU parity of the FP8 casts against the CPU oracle: bit-exact data and scales.
+
+Cases follow "deep-gemm: fused per-token FP8 cast in Triton
+(fused_per_token_cast_to_fp8), version 3" [Results, Tests]: bf16 and fp32
+input, group 32 and 128, fp32 / UE8M0 / packed-UE8M0 scales, shapes 1x512,
+7x4096, 129x7168, 64x1000 (partial last group), 3000x4096, an all-zero group
+and very large values; writing into views of a larger buffer leaves the rest
+untouched. Plus the hidden-4096 token sweep and the 128x128 block cast of
+"DeepGEMM Essentials: High-Performance FP8 Matrix Multiplication" Part 4.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import np_bytes, np_input, np_sf
+from quantised_linear_layers_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [torch.bfloat16, torch.float32]
+GRANS = [32, 128]
+FMTS = [0, 1, 2]
+MATRIX_SHAPES = [(1, 512), (7, 4096), (129, 7168), (64, 1000), (3000, 4096)]
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from quantised_linear_layers_gb300 import build, ops as o
+    build.build()
+    o.load_library()
+    return o
+
+
+def make_x(m, n, dtype, gran, huge=True):
+    x = syn.randn_row_exp(m, n, seed=syn.SEED_X, dtype=dtype)
+    syn.plant_edges(x, gran, zero_group=True, huge_row=(m // 2 if huge and m > 1 else None))
+    return x
+
+
+def assert_cast_equal(orc, ops, x, gran, fmt, recip=False, sf_mn_major=False):
+    q, s = ops.fp8_cast_per_token(x.cuda(), gran, fmt, recip=recip, sf_mn_major=sf_mn_major)
+    oq, os_ = orc.cast_per_token(np_input(x), gran, fmt, recip=recip)
+    gq = np_bytes(q)
+    bad = np.argwhere(gq != oq)
+    assert bad.size == 0, f"{len(bad)} data bytes differ; first {bad[0]}: gpu {gq[tuple(bad[0])]:#x} oracle {oq[tuple(bad[0])]:#x}"
+    gs = np_sf(s)
+    assert gs.shape == os_.shape
+    assert np.array_equal(gs.view(np.uint32), np.ascontiguousarray(os_).view(np.uint32)), "scale bytes differ"
+
+
+@pytest.mark.parametrize("shape", MATRIX_SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
+@pytest.mark.parametrize("fmt", FMTS, ids=["fp32", "ue8m0", "packed"])
+@pytest.mark.parametrize("gran", GRANS)
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
+def test_cast_matrix_60(orc, ops, dtype, gran, fmt, shape):
+    m, n = shape
+    assert_cast_equal(orc, ops, make_x(m, n, dtype, gran), gran, fmt)
+
+
+@pytest.mark.parametrize("tokens", [1, 64, 512, 4096, 16384])
+@pytest.mark.parametrize("fmt", FMTS, ids=["fp32", "ue8m0", "packed"])
+@pytest.mark.parametrize("gran", GRANS)
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
+def test_cast_token_sweep_hidden4096(orc, ops, dtype, gran, fmt, tokens):
+    assert_cast_equal(orc, ops, make_x(tokens, 4096, dtype, gran), gran, fmt)
+
+
+@pytest.mark.parametrize("shape", [(7, 4096), (64, 1000), (3000, 4096)])
+def test_cast_recip_of_scale_variant(orc, ops, shape):
+    assert_cast_equal(orc, ops, make_x(*shape, torch.bfloat16, 128), 128, 0, recip=True)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_cast_mn_major_scales(orc, ops, fmt):
+    x = make_x(129, 7168, torch.bfloat16, 128)
+    q, s = ops.fp8_cast_per_token(x.cuda(), 128, fmt, sf_mn_major=True)
+    assert s.stride(0) == 1 and s.stride(1) % 4 == 0
+    oq, os_ = orc.cast_per_token(np_input(x), 128, fmt)
+    assert np.array_equal(np_bytes(q), oq)
+    assert np.array_equal(np.ascontiguousarray(np_sf(s)).view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
+def test_cast_into_views_leaves_rest_untouched(orc, ops, dtype, fmt):
+    m, n = 7, 4096
+    x = make_x(m, n, dtype, 128)
+    parent = syn.random_bytes(16 * 8192, seed=99).cuda()
+    ref_parent = parent.clone()
+    out = parent.view(16, 8192)[3:3 + m, 128:128 + n].view(torch.float8_e4m3fn)
+    cols = -(-n // 128) if fmt != 2 else -(-(-(-n // 128)) // 4)
+    sbuf = syn.random_bytes(4 * 40 * 80, seed=98).cuda().view(torch.int32).view(40, 80)
+    ref_sbuf = sbuf.clone()
+    sview = sbuf[2:2 + m, 1:1 + 2 * cols:2]
+    if fmt != 2:
+        sview = sview.view(torch.float32)
+    ops.fp8_cast_per_token(x.cuda(), 128, fmt, out=out, out_sf=sview)
+    oq, os_ = orc.cast_per_token(np_input(x), 128, fmt)
+    assert np.array_equal(np_bytes(out), oq)
+    assert np.array_equal(np.ascontiguousarray(np_sf(sview)).view(np.uint32), os_.view(np.uint32))
+    mask = torch.ones(16, 8192, dtype=torch.bool, device="cuda")
+    mask[3:3 + m, 128:128 + n] = False
+    assert torch.equal(parent.view(16, 8192)[mask], ref_parent.view(16, 8192)[mask])
+    smask = torch.ones(40, 80, dtype=torch.bool, device="cuda")
+    smask[2:2 + m, 1:1 + 2 * cols:2] = False
+    assert torch.equal(sbuf[smask], ref_sbuf[smask])
+
+
+@pytest.mark.parametrize("gran", GRANS)
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(4096, 1024), (300, 200), (7168, 640)])
+def test_cast_transposed_view(orc, ops, dtype, gran, fmt, shape):
+    """Cast of x^T (x_stride_m == 1): the wgrad operands dY^T and X^T."""
+    t_rows, feats = shape
+    x = make_x(t_rows, feats, dtype, gran, huge=False)
+    xt = x.t()                                            # [feats, tokens], stride (1, feats)
+    q, s = ops.fp8_cast_per_token(x.cuda().t(), gran, fmt)
+    oq, os_ = orc.cast_per_token(np_input(x).T, gran, fmt)
+    assert np.array_equal(np_bytes(q), oq)
+    assert np.array_equal(np.ascontiguousarray(np_sf(s)).view(np.uint32), os_.view(np.uint32))
+    assert xt.shape == q.shape
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_cast_generic_strides(orc, ops, fmt):
+    base = make_x(64, 2000, torch.bfloat16, 32, huge=False)
+    q, s = ops.fp8_cast_per_token(base.cuda()[:, ::2], 32, fmt)   # strides (2000, 2)
+    oq, os_ = orc.cast_per_token(np_input(base)[:, ::2], 32, fmt)
+    assert np.array_equal(np_bytes(q), oq)
+    assert np.array_equal(np.ascontiguousarray(np_sf(s)).view(np.uint32), os_.view(np.uint32))
+
+
+def test_cast_misaligned_rows_take_scalar_path(orc, ops):
+    base = make_x(33, 4100, torch.bfloat16, 128, huge=False)
+    xv = base[:, 3:3 + 4095]                              # odd offset and width
+    q, s = ops.fp8_cast_per_token(base.cuda()[:, 3:3 + 4095], 128, 2)
+    oq, os_ = orc.cast_per_token(np_input(base)[:, 3:3 + 4095], 128, 2)
+    assert xv.shape == q.shape
+    assert np.array_equal(np_bytes(q), oq)
+    assert np.array_equal(np_sf(s).view(np.uint32), os_.view(np.uint32))
+
+
+def test_cast_empty_is_noop(ops):
+    x = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
+    q, s = ops.fp8_cast_per_token(x, 128, 0)
+    assert q.shape == (0, 512)
+    x = torch.empty((5, 0), dtype=torch.bfloat16, device="cuda")
+    q, s = ops.fp8_cast_per_token(x, 128, 0)
+    assert q.shape == (5, 0)
+
+
+def test_cast_invalid_arguments(ops):
+    x = torch.zeros((4, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ops.QLError) as e:
+        ops.fp8_cast_per_token(x, 64, 0)
+    assert e.value.status == 1
+    with pytest.raises(ops.QLError):
+        ops.fp8_cast_per_token(x, 128, 1, recip=True)
+    with pytest.raises(ops.QLError):
+        ops.fp8_cast_per_block(x, 2)
+
+
+# ---------------------------------------------------------------- block cast
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(256, 512), (300, 200), (4096, 7168), (1, 130)])
+def test_block_cast(orc, ops, dtype, fmt, shape):
+    w = syn.randn(shape, seed=syn.SEED_W, dtype=dtype, mul=0.02)
+    if shape[0] > 200:
+        w[128:256, 0:128] = 0                             # an all-zero block
+    q, s = ops.fp8_cast_per_block(w.cuda(), fmt)
+    oq, os_ = orc.cast_per_block(np_input(w), fmt)
+    assert np.array_equal(np_bytes(q), oq)
+    assert np.array_equal(np_sf(s).view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("shape", [(4096, 7168), (300, 200)])
+def test_block_cast_writes_transpose(orc, ops, fmt, shape):
+    """cast_per_block(W^T) written in the same pass (dgrad operand); equals the
+    oracle's cast of the transposed view."""
+    m, n = shape
+    w = syn.randn(shape, seed=syn.SEED_W, mul=0.02)
+    wt_store = torch.empty((n, m), dtype=torch.float8_e4m3fn, device="cuda")
+    st_store = torch.empty((-(-n // 128), -(-m // 128)), dtype=torch.float32, device="cuda")
+    ops.fp8_cast_per_block(w.cuda(), fmt, out=wt_store.t(), out_sf=st_store.t())
+    oq, os_ = orc.cast_per_block(np.ascontiguousarray(np_input(w).T), fmt)
+    assert np.array_equal(np_bytes(wt_store), oq)
+    assert np.array_equal(np_sf(st_store).view(np.uint32), os_.view(np.uint32))
+    # reading a transposed input view gives the same bytes
+    q2, s2 = ops.fp8_cast_per_block(w.cuda().t(), fmt)
+    assert torch.equal(q2.view(torch.uint8), wt_store.view(torch.uint8))
+    assert torch.equal(s2, st_store)
+
+
+def test_block_cast_large_weight_ue8m0(orc, ops):
+    """The 18432 x 7168 weight of the large cast+GEMM workload, UE8M0."""
+    w = syn.randn((18432, 7168), seed=syn.SEED_W, mul=0.02)
+    q, s = ops.fp8_cast_per_block(w.cuda(), 1)
+    oq, os_ = orc.cast_per_block(np_input(w), 1)
+    assert np.array_equal(np_bytes(q), oq)
+    assert np.array_equal(np_sf(s), os_)

@@ -1,0 +1,200 @@
+"""GPU parity of the block-scaled FP8 GEMM against the fp64 CPU oracle.
+
+D = A B^T ("DeepGEMM Essentials: High-Performance FP8 Matrix Multiplication"
+Parts 1, 6, 12-13; RHS scales read row-wise per "[Help] Starter script for
+nn.Linear for fwd,bwd"). The oracle takes the GPU cast's bytes as input, so
+the GEMM is judged alone (the casts are checked bit-exact elsewhere):
+relative Frobenius error <= 1e-3 and |err| <= 2^-7 |ref| + 1e-2 rms(ref).
+Where every partial sum is an exact fp32 integer the result must be exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import check_gemm, np_bytes, np_input, np_sf
+from quantised_linear_layers_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from quantised_linear_layers_gb300 import build, ops as o
+    build.build()
+    o.load_library()
+    yield o
+    o.set_gemm_block_n(0)
+    o.set_num_sms(0)
+
+
+def fwd_operands(ops, m, n, k, fmt, w_mul=1.0, seed_x=syn.SEED_X, seed_w=syn.SEED_W):
+    x = syn.randn((m, k), seed=seed_x)
+    w = syn.randn((n, k), seed=seed_w, mul=w_mul)
+    xq, xs = ops.fp8_cast_per_token(x.cuda(), 128, fmt, sf_mn_major=True)
+    wfmt = 1 if fmt == 2 else fmt                 # block scales: fp32-stored UE8M0
+    wq, ws = ops.fp8_cast_per_block(w.cuda(), wfmt)
+    if fmt == 2:                                  # pack the block scales' exponents along K
+        e = (ws.view(torch.int32) >> 23) & 0xFF
+        kb = ws.shape[1]
+        pad = (-kb) % 4
+        e = torch.nn.functional.pad(e, (0, pad)).view(ws.shape[0], -1, 4)
+        ws = (e[..., 0] | (e[..., 1] << 8) | (e[..., 2] << 16) | (e[..., 3] << 24)).contiguous()
+    return x, w, xq, xs, wq, ws
+
+
+def oracle_fwd(orc, xq, xs, wq, ws, fmt, rows=None):
+    return orc.gemm(np_bytes(xq), np_sf(xs), np_bytes(wq), np_sf(ws), fmt, rows=rows)
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2], ids=["fp32", "ue8m0", "packed"])
+def test_worked_128x256x512(orc, ops, fmt):
+    """The pages' first worked example: LHS [128, 512], RHS [256, 512]."""
+    x, w, xq, xs, wq, ws = fwd_operands(ops, 128, 256, 512, fmt)
+    d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    ref = oracle_fwd(orc, xq, xs, wq, ws, fmt)
+    check_gemm(d.float().cpu().numpy(), ref)
+    assert ops.device_status() == 0
+
+
+@pytest.mark.parametrize("bn", [32, 64, 128, 256])
+@pytest.mark.parametrize("shape", [(200, 300, 592), (128, 256, 512), (1, 40, 16), (257, 513, 1152)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_every_tile_width_ragged(orc, ops, bn, shape):
+    m, n, k = shape
+    ops.set_gemm_block_n(bn)
+    try:
+        x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, 0)
+        d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 0)
+    finally:
+        ops.set_gemm_block_n(0)
+    ref = oracle_fwd(orc, xq, xs, wq, ws, 0)
+    check_gemm(d.float().cpu().numpy(), ref, f"bn={bn} {shape}")
+
+
+@pytest.mark.parametrize("bn", [32, 64, 128, 256])
+def test_exact_small_integers(orc, ops, bn):
+    """Entries are exact E4M3 integers in [-8, 8] with unit scales: every
+    partial sum is an exact fp32 integer and |D| <= 256 is exact in bf16."""
+    m, n, k = 130, 260, 256
+    a = syn.e4m3_small_ints((m, k), seed=11, lo=-2, hi=2)
+    b = syn.e4m3_small_ints((n, k), seed=12, lo=-2, hi=2)
+    aq = a.to(torch.float8_e4m3fn).cuda()
+    bq = b.to(torch.float8_e4m3fn).cuda()
+    sa = torch.ones((m, 2), dtype=torch.float32, device="cuda")
+    sb = torch.ones((3, 2), dtype=torch.float32, device="cuda")
+    ops.set_gemm_block_n(bn)
+    try:
+        d = ops.gemm_fp8_nt_bf16(aq, sa, bq, sb, 0)
+    finally:
+        ops.set_gemm_block_n(0)
+    ref = (a.double() @ b.double().T).numpy()
+    assert np.abs(ref).max() <= 256
+    assert np.array_equal(d.double().cpu().numpy(), ref)
+
+
+def test_rhs_scale_grid_row_wise(orc, ops):
+    """Non-square scale grid with power-of-two scales: a transposed or
+    mis-indexed B scale grid changes the (exact) result."""
+    m, n, k = 64, 384, 640                        # grid [3, 5]
+    a = syn.e4m3_small_ints((m, k), seed=21)
+    b = syn.e4m3_small_ints((n, k), seed=22)
+    aq, bq = a.to(torch.float8_e4m3fn).cuda(), b.to(torch.float8_e4m3fn).cuda()
+    sa = torch.ones((m, 5), dtype=torch.float32, device="cuda")
+    sb = torch.tensor([[2.0 ** (i - 2 * j) for j in range(5)] for i in range(3)], dtype=torch.float32)
+    d = ops.gemm_fp8_nt_bf16(aq, sa, bq, sb.cuda(), 0)
+    ref = orc.gemm(np_bytes(aq), np_sf(sa), np_bytes(bq), sb.numpy(), 0)
+    check_gemm(d.float().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("m", [64, 128, 4096])
+@pytest.mark.parametrize("fmt", [0, 1], ids=["fp32", "ue8m0"])
+def test_linear_fwd_hidden7168(orc, ops, m, fmt):
+    """X [M, 7168] x W [4096, 7168]^T, W = randn * 0.02."""
+    n, k = 4096, 7168
+    x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, fmt, w_mul=0.02)
+    d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    rows = None if m <= 128 else np.random.default_rng(7).choice(m, 48, replace=False)
+    ref = oracle_fwd(orc, xq, xs, wq, ws, fmt, rows=rows)
+    got = d.float().cpu().numpy()
+    check_gemm(got if rows is None else got[rows], ref)
+
+
+def test_large_ue8m0_sampled_rows(orc, ops):
+    """X [16384, 7168] x W [18432, 7168]^T with UE8M0 scales, checked on
+    sampled rows (the oracle computes them one by one)."""
+    m, n, k = 16384, 18432, 7168
+    x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, 1, w_mul=0.02)
+    d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 1)
+    rows = np.sort(np.random.default_rng(3).choice(m, 12, replace=False))
+    rows[0] = 0
+    rows[-1] = m - 1
+    ref = oracle_fwd(orc, xq, xs, wq, ws, 1, rows=rows)
+    check_gemm(d[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_wgrad_fp32(orc, ops, accumulate, fmt):
+    """dW = dY^T X with both operands cast per token along the token axis
+    (K = tokens), fp32 output, optionally accumulated."""
+    T, K, N = 512, 1024, 384
+    x = syn.randn((T, K), seed=syn.SEED_X)
+    dy = syn.randn((T, N), seed=syn.SEED_DY)
+    aq, sa = ops.fp8_cast_per_token(dy.cuda().t(), 128, fmt)     # [N, T]
+    bq, sb = ops.fp8_cast_per_token(x.cuda().t(), 128, fmt)      # [K, T]
+    d0 = syn.randn((N, K), seed=5, dtype=torch.float32, mul=0.1).cuda()
+    out = d0.clone() if accumulate else torch.empty_like(d0)
+    ops.gemm_fp8_wgrad_fp32(aq, sa, bq, sb, out=out, accumulate=accumulate, fmt=fmt)
+    ref = orc.gemm(np_bytes(aq), np_sf(sa), np_bytes(bq), np_sf(sb), fmt, b_per_row=True,
+                   d_in=d0.double().cpu().numpy() if accumulate else None)
+    check_gemm(out.double().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("bn", [32, 64, 128, 256])
+def test_wgrad_exact_integers(orc, ops, bn):
+    m, n, k = 200, 300, 384
+    a = syn.e4m3_small_ints((m, k), seed=31)
+    b = syn.e4m3_small_ints((n, k), seed=32)
+    aq, bq = a.to(torch.float8_e4m3fn).cuda(), b.to(torch.float8_e4m3fn).cuda()
+    sa = torch.ones((m, 3), dtype=torch.float32, device="cuda")
+    sb = torch.ones((n, 3), dtype=torch.float32, device="cuda")
+    ops.set_gemm_block_n(bn)
+    try:
+        d = ops.gemm_fp8_wgrad_fp32(aq, sa, bq, sb)
+    finally:
+        ops.set_gemm_block_n(0)
+    assert np.array_equal(d.double().cpu().numpy(), (a.double() @ b.double().T).numpy())
+
+
+def test_zero_k_writes_zero(ops):
+    a = torch.empty((5, 0), dtype=torch.float8_e4m3fn, device="cuda")
+    b = torch.empty((7, 0), dtype=torch.float8_e4m3fn, device="cuda")
+    s = torch.empty((5, 0), dtype=torch.float32, device="cuda")
+    d = torch.full((5, 7), 3.0, dtype=torch.bfloat16, device="cuda")
+    ops.gemm_fp8_nt_bf16(a, s, b, s, 0, out=d)
+    assert torch.count_nonzero(d).item() == 0
+
+
+def test_num_sms_knob_same_result(orc, ops):
+    x, w, xq, xs, wq, ws = fwd_operands(ops, 512, 1024, 1024, 0)
+    d1 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 0)
+    full = ops.get_num_sms()
+    ops.set_num_sms(full // 2)
+    try:
+        assert ops.get_num_sms() == full // 2
+        d2 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 0)
+    finally:
+        ops.set_num_sms(0)
+    assert ops.get_num_sms() == full
+    assert torch.equal(d1, d2)
+
+
+def test_gemm_rejects_misaligned(ops):
+    a = torch.zeros((8, 48), dtype=torch.float8_e4m3fn, device="cuda")
+    b = torch.zeros((8, 48), dtype=torch.float8_e4m3fn, device="cuda")
+    s = torch.ones((8, 1), dtype=torch.float32, device="cuda")
+    with pytest.raises(ops.QLError) as e:
+        ops.gemm_fp8_nt_bf16(a[:, 8:40], s, b[:, 8:40], s, 0)       # base not 16-byte aligned
+    assert e.value.status == 3
