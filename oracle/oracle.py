@@ -74,6 +74,9 @@ def _load():
             lib.oracle_cast_per_block.argtypes = [
                 _vp, ctypes.c_int, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int,
                 _vp, _i64, _i64, _vp, _i64, _i64]
+            lib.oracle_round_bf16.restype = ctypes.c_double
+            lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_round_array.argtypes = [_vp, _i64, ctypes.c_int]
             lib.oracle_gemm.restype = ctypes.c_int
             lib.oracle_gemm.argtypes = [
                 _vp, _i64, _vp, _i64, _i64,
@@ -119,6 +122,16 @@ def e4m3_decode(b) -> np.ndarray:
     out = np.empty(b.shape, dtype=np.float64)
     _load().oracle_e4m3_decode_array(_ptr(b), b.size, _ptr(out))
     return out
+
+
+def round_output(v: np.ndarray, out: str) -> np.ndarray:
+    """Round exact (float64) results to the GEMM's output type: 'bf16' (round
+    to nearest even from the exact value), 'f32' (RNE) or 'f64' (unchanged)."""
+    v = np.array(v, dtype=np.float64, copy=True, order="C")
+    mode = {"f64": 0, "bf16": 1, "f32": 2}[out]
+    if mode:
+        _load().oracle_round_array(_ptr(v), v.size, mode)
+    return v
 
 
 def _dtype_code(x: np.ndarray) -> int:
@@ -173,11 +186,14 @@ def cast_per_block(x: np.ndarray, fmt: int, recip: bool = False,
 
 
 def gemm(a: np.ndarray, sfa: np.ndarray, b: np.ndarray, sfb: np.ndarray, fmt: int,
-         b_per_row: bool = False, kgran: int = 128, rows=None, d_in: np.ndarray | None = None):
+         b_per_row: bool = False, kgran: int = 128, rows=None, d_in: np.ndarray | None = None,
+         out: str = "f64"):
     """fp64 block-scaled D = A B^T over E4M3 bytes. Returns float64 [len(rows) or m, n].
 
     a: uint8 [m,k] (row stride may exceed k), b: uint8 [n,k]. sfa / sfb any
-    strides (float32, or int32 packed UE8M0 when fmt == 2)."""
+    strides (float32, or int32 packed UE8M0 when fmt == 2). ``out`` rounds the
+    exact result to the method's output type: 'bf16' for the fwd/dgrad GEMM
+    (Part 6 writes a bf16 output), 'f32' for wgrad (Parts 12-13), 'f64' none."""
     assert a.dtype == np.uint8 and b.dtype == np.uint8
     assert a.strides[1] == 1 and b.strides[1] == 1
     m, k = a.shape
@@ -202,4 +218,4 @@ def gemm(a: np.ndarray, sfa: np.ndarray, b: np.ndarray, sfb: np.ndarray, fmt: in
                              _ptr(d), n, dip, ldi)
     if rc != 0:
         raise ValueError("oracle_gemm: bad arguments")
-    return d
+    return round_output(d, out) if out != "f64" else d

@@ -132,6 +132,30 @@ void oracle_e4m3_decode_array(const uint8_t* b, int64_t n, double* out) {
 }
 
 /* ------------------------------------------------------------------------
+ * Output rounding of the GEMM. The fwd/dgrad GEMM writes bf16 (8 significant
+ * bits, bias 127): round to nearest, ties to even, directly from the exact
+ * (double) value. The wgrad GEMM writes fp32: (float) conversion is RNE.
+ * ---------------------------------------------------------------------- */
+double oracle_round_bf16(double v) {
+    if (v == 0.0 || isnan(v) || isinf(v)) return v;
+    double a = fabs(v);
+    int ex;
+    frexp(a, &ex);
+    int E = ex - 1;                /* a in [2^E, 2^(E+1)) */
+    if (E < -126) E = -126;        /* bf16 subnormals: quantum 2^-133 */
+    double quantum = ldexp(1.0, E - 7);
+    double r = nearbyint(a / quantum) * quantum;
+    return v < 0 ? -r : r;
+}
+
+void oracle_round_array(double* v, int64_t n, int mode) {
+    for (int64_t i = 0; i < n; ++i) {
+        if (mode == 1) v[i] = oracle_round_bf16(v[i]);
+        else if (mode == 2) v[i] = (double)(float)v[i];
+    }
+}
+
+/* ------------------------------------------------------------------------
  * Scalars of the cast.
  * ---------------------------------------------------------------------- */
 static float bf16_bits_to_float(uint16_t h) {

@@ -3,8 +3,10 @@
 D = A B^T ("DeepGEMM Essentials: High-Performance FP8 Matrix Multiplication"
 Parts 1, 6, 12-13; RHS scales read row-wise per "[Help] Starter script for
 nn.Linear for fwd,bwd"). The oracle takes the GPU cast's bytes as input, so
-the GEMM is judged alone (the casts are checked bit-exact elsewhere):
-relative Frobenius error <= 1e-3 and |err| <= 2^-7 |ref| + 1e-2 rms(ref).
+the GEMM is judged alone (the casts are checked bit-exact elsewhere). The
+reference is the exact product rounded to the output type (bf16 for fwd/dgrad,
+fp32 for wgrad); the GPU result must be within relative Frobenius error 1e-3
+of it and |err| <= 2^-7 |ref| + 1e-2 rms(ref) per element.
 Where every partial sum is an exact fp32 integer the result must be exact.
 """
 import numpy as np
@@ -45,7 +47,8 @@ def fwd_operands(ops, m, n, k, fmt, w_mul=1.0, seed_x=syn.SEED_X, seed_w=syn.SEE
 
 
 def oracle_fwd(orc, xq, xs, wq, ws, fmt, rows=None):
-    return orc.gemm(np_bytes(xq), np_sf(xs), np_bytes(wq), np_sf(ws), fmt, rows=rows)
+    """The method's output: the exact block-scaled product rounded to bf16."""
+    return orc.gemm(np_bytes(xq), np_sf(xs), np_bytes(wq), np_sf(ws), fmt, rows=rows, out="bf16")
 
 
 @pytest.mark.parametrize("fmt", [0, 1, 2], ids=["fp32", "ue8m0", "packed"])
@@ -104,7 +107,7 @@ def test_rhs_scale_grid_row_wise(orc, ops):
     sa = torch.ones((m, 5), dtype=torch.float32, device="cuda")
     sb = torch.tensor([[2.0 ** (i - 2 * j) for j in range(5)] for i in range(3)], dtype=torch.float32)
     d = ops.gemm_fp8_nt_bf16(aq, sa, bq, sb.cuda(), 0)
-    ref = orc.gemm(np_bytes(aq), np_sf(sa), np_bytes(bq), sb.numpy(), 0)
+    ref = orc.gemm(np_bytes(aq), np_sf(sa), np_bytes(bq), sb.numpy(), 0, out="bf16")
     check_gemm(d.float().cpu().numpy(), ref)
 
 
@@ -148,7 +151,7 @@ def test_wgrad_fp32(orc, ops, accumulate, fmt):
     out = d0.clone() if accumulate else torch.empty_like(d0)
     ops.gemm_fp8_wgrad_fp32(aq, sa, bq, sb, out=out, accumulate=accumulate, fmt=fmt)
     ref = orc.gemm(np_bytes(aq), np_sf(sa), np_bytes(bq), np_sf(sb), fmt, b_per_row=True,
-                   d_in=d0.double().cpu().numpy() if accumulate else None)
+                   d_in=d0.double().cpu().numpy() if accumulate else None, out="f32")
     check_gemm(out.double().cpu().numpy(), ref)
 
 

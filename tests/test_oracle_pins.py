@@ -447,3 +447,29 @@ def test_huge_values_no_overflow(orc):
         else:                                   # a power-of-two scale puts amax in (224, 448]
             assert np.all((mag >= 0x76) & (mag <= 0x7E))
     assert orc.overflow_count() == 0
+
+
+# ------------------------------------------------------- GEMM output rounding
+def test_bf16_output_rounding(orc):
+    """bf16 RNE of the exact result: equals torch's fp32 -> bf16 conversion on
+    fp32 values, and resolves ties in doubles to the even neighbour."""
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal(1_000_000).astype(np.float32) * np.float32(1e3)
+    ours = orc.round_output(v.astype(np.float64), "bf16")
+    assert np.array_equal(ours, torch.from_numpy(v).to(torch.bfloat16).double().numpy())
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 1 + 2.0 ** -8 + 2.0 ** -40,
+                     2.0 ** 100 * (1 + 2.0 ** -8)])
+    expect = np.array([1.0, 1 + 2.0 ** -6, -1.0, 1 + 2.0 ** -7, 2.0 ** 100])
+    assert np.array_equal(orc.round_output(ties, "bf16"), expect)
+    assert np.array_equal(orc.round_output(np.array([1 + 2.0 ** -30]), "f32"), np.array([1.0]))
+
+
+def test_gemm_output_rounding_option(orc):
+    x = syn.randn((64, 256), seed=syn.SEED_X)
+    w = syn.randn((128, 256), seed=syn.SEED_W)
+    qa, sa = orc.cast_per_token(bf16_bits(x), 128, orc.SF_FP32)
+    qb, sb = orc.cast_per_block(bf16_bits(w), orc.SF_FP32)
+    exact = orc.gemm(qa, sa, qb, sb, orc.SF_FP32)
+    rounded = orc.gemm(qa, sa, qb, sb, orc.SF_FP32, out="bf16")
+    assert np.array_equal(rounded, orc.round_output(exact, "bf16"))
+    assert np.max(np.abs(rounded - exact) / np.maximum(np.abs(exact), 1e-30)) <= 2.0 ** -8
