@@ -1,0 +1,406 @@
+"""Benchmark of the FP8 linear-layer hot path on GB300.
+
+One step = the per-token FP8 cast of X (1x128 groups, UE8M0 scales, written
+M-major) followed by the block-scaled GEMM D = X W^T (bf16 out), over the
+large cast+GEMM workload: X bf16 [16384, 7168] randn, W bf16 [18432, 7168]
+randn * 0.02 cast once to E4M3 with 128x128 UE8M0 block scales (outside the
+timed region, as a weight cast runs once per weight update). Inputs are
+synthetic and seeded; they are larger than L2, so no flush is needed.
+
+Prints one JSON line (rank 0). Keys: metric/value/unit (GEMM TFLOP/s of the
+whole step), ms_per_step, roofline (dominant kernel: the GEMM, against the
+dense FP8 peak = 2x the measured bf16 peak), cast (GB/s of the cast kernel
+against measured HBM bandwidth), cast_sweep (the pages' per-token cast
+point: 16384 tokens x 4096, group 32, packed UE8M0), e2e (host buffers,
+copies inside the timed region), cpu_baseline (the CPU oracle on a bounded
+sample), clocks (nvidia-smi during the timed region), gpu_launches.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica (rows are independent:
+weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "large_cast_gemm_16384x18432x7168_ue8m0"
+METRIC = "block-scaled FP8 GEMM TFLOP/s (% FP8 peak); per-token cast GB/s (% HBM)"
+UNIT = "TFLOP/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--m", type=int, default=16384)
+    ap.add_argument("--n", type=int, default=18432)
+    ap.add_argument("--k", type=int, default=7168)
+    ap.add_argument("--fmt", choices=["ue8m0", "packed", "fp32"], default="ue8m0")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-oracle sample time")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sus": p.get("bf16_tflops_sustained"),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+class CpuOracleSample:
+    """The CPU oracle on a bounded sample of the workload: the per-token cast
+    of a slice of X's rows and the fp64 GEMM of those rows against all of W.
+    W's block cast (once per weight update) is prepared before any timing,
+    as on the GPU."""
+
+    def __init__(self, n, k, fmt_code):
+        import numpy as np
+        import torch
+
+        import oracle
+        from quantised_linear_layers_gb300 import synthetic as syn
+
+        oracle.build()
+        self.o = oracle
+        self.n, self.k = n, k
+        self.fmt = oracle.SF_FP32 if fmt_code == 0 else oracle.SF_UE8M0
+        self.threads = oracle.num_threads()
+        w = syn.randn((n, k), seed=syn.SEED_W, mul=0.02)
+        self.wq, self.ws = oracle.cast_per_block(w.view(torch.int16).numpy().view(np.uint16), self.fmt)
+        self.rows = max(self.threads, 8)
+        x = syn.randn((self.rows, k), seed=syn.SEED_X)
+        self.xb = x.view(torch.int16).numpy().view(np.uint16)
+
+    def once(self) -> float:
+        t0 = time.perf_counter()
+        xq, xs = self.o.cast_per_token(self.xb, 128, self.fmt)
+        self.o.gemm(xq, xs, self.wq, self.ws, self.fmt, out="bf16")
+        return time.perf_counter() - t0
+
+    def run(self, target_s: float):
+        """Repeat the sample for about target_s seconds; returns (TFLOP/s, s, rows)."""
+        t = self.once()
+        reps, total = 1, t
+        while total < target_s and reps < 256:
+            total += self.once()
+            reps += 1
+        rows = self.rows * reps
+        return 2.0 * rows * self.n * self.k / total / 1e12, total, rows
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    import torch
+
+    from quantised_linear_layers_gb300 import build as qbuild
+    qbuild.build()
+    from quantised_linear_layers_gb300 import ops
+    from quantised_linear_layers_gb300 import synthetic as syn
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ops.load_library()
+    m, n, k = args.m, args.n, args.k
+    fmt = {"fp32": ops.SF_FP32, "ue8m0": ops.SF_UE8M0, "packed": ops.SF_PACKED_UE8M0}[args.fmt]
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16"]
+    fp8_peak_sus = 2.0 * pk["bf16_sus"] if pk["bf16_sus"] else None
+
+    x = syn.randn((m, k), seed=syn.SEED_X + 1000 * rank, device=str(dev))
+    w = syn.randn((n, k), seed=syn.SEED_W, mul=0.02, device=str(dev))
+    wq, ws = ops.fp8_cast_per_block(w, ops.SF_UE8M0 if fmt != ops.SF_FP32 else ops.SF_FP32)
+    if fmt == ops.SF_PACKED_UE8M0:
+        e = (ws.view(torch.int32) >> 23) & 0xFF
+        e = torch.nn.functional.pad(e, (0, (-e.shape[1]) % 4)).view(e.shape[0], -1, 4)
+        ws = (e[..., 0] | (e[..., 1] << 8) | (e[..., 2] << 16) | (e[..., 3] << 24)).contiguous()
+    del w
+    xq = torch.empty((m, k), dtype=torch.float8_e4m3fn, device=dev)
+    xs = ops.empty_sf(m, ops.sf_shape(k, 128, fmt), fmt, dev, mn_major=True)
+    d = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        ops.fp8_cast_per_token(x, 128, fmt, out=xq, out_sf=xs)
+        ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt, out=d)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(K):
+        ev[i][0].record()
+        ops.fp8_cast_per_token(x, 128, fmt, out=xq, out_sf=xs)
+        ev[i][1].record()
+        ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt, out=d)
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    cast_ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
+    gemm_ms = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(K)) / K
+    assert ops.device_status() == 0
+    total_ms = max_over_ranks(world, total_ms)
+    ms_step = total_ms / K
+    flops_step = 2.0 * m * n * k
+    value = flops_step * world * K / (total_ms / 1e3) / 1e12
+
+    sf_bytes = m * ops.sf_shape(k, 128, fmt) * 4
+    cast_bytes = m * k * 2 + m * k + sf_bytes
+    gemm_tflops = flops_step / (gemm_ms / 1e3) / 1e12
+    cast_gbs = cast_bytes / (cast_ms / 1e3) / 1e9
+
+    # the pages' per-token cast point: 16384 x 4096 bf16, group 32, packed UE8M0
+    sweep = None
+    if not args.no_sweep:
+        xs_in = syn.randn_row_exp(16384, 4096, device=str(dev))
+        sq = torch.empty((16384, 4096), dtype=torch.float8_e4m3fn, device=dev)
+        ssf = ops.empty_sf(16384, ops.sf_shape(4096, 32, 2), 2, dev)
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        for _ in range(5):
+            ops.fp8_cast_per_token(xs_in, 32, 2, out=sq, out_sf=ssf)
+        times_cold, times_hot = [], []
+        for _ in range(20):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            ops.fp8_cast_per_token(xs_in, 32, 2, out=sq, out_sf=ssf)
+            b.record()
+            torch.cuda.synchronize()
+            times_cold.append(a.elapsed_time(b))
+        for _ in range(20):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            ops.fp8_cast_per_token(xs_in, 32, 2, out=sq, out_sf=ssf)
+            b.record()
+            torch.cuda.synchronize()
+            times_hot.append(a.elapsed_time(b))
+        sb = 16384 * 4096 * 2 + 16384 * 4096 + 16384 * 32 * 4
+        tc = statistics.median(times_cold)
+        th = statistics.median(times_hot)
+        sweep = {"shape": [16384, 4096], "gran": 32, "scales": "packed_ue8m0", "bytes": sb,
+                 "us_cold_l2": round(tc * 1e3, 2), "gbs_cold_l2": round(sb / (tc / 1e3) / 1e9, 1),
+                 "frac_hbm_cold": round(sb / (tc / 1e3) / 1e9 / pk["hbm_gbs"], 3),
+                 "us_hot_l2": round(th * 1e3, 2), "pages_b200_eager_us": 38.7}
+        del xs_in, sq, ssf, flush
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.empty((m, k), dtype=torch.bfloat16, pin_memory=True)
+        xh.copy_(x.cpu())
+        dh = torch.empty((m, n), dtype=torch.bfloat16, pin_memory=True)
+        ke = min(K, 5)
+
+        def e2e_step():
+            x.copy_(xh, non_blocking=True)
+            step()
+            dh.copy_(d, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(ke):
+            e2e_step()
+        torch.cuda.synchronize()
+        te = max_over_ranks(world, time.perf_counter() - t0)
+        e2e = {"value": round(flops_step * world * ke / te / 1e12, 2), "unit": UNIT,
+               "h2d_bytes_per_step": m * k * 2, "d2h_bytes_per_step": m * n * 2, "steps": ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        sample = CpuOracleSample(n, k, fmt)
+        v, secs, rows = sample.run(args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": sample.threads, "kind": "oracle",
+               "sample": f"{rows} rows of X: per-token cast + fp64 GEMM against all {n} rows of W "
+                         f"(k={k}), {secs:.1f} s; W's block cast done before timing"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic (seeded randn; W randn*0.02)",
+            "config": {"workload": WORKLOAD, "m": m, "n": n, "k": k, "x_dtype": "bf16", "out_dtype": "bf16",
+                       "gran_k": 128, "scales": args.fmt, "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1),
+                         "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(gemm_tflops / fp8_peak, 4), "traffic": None,
+                         "kernel": "gemm_fp8_kernel", "peak_note": f"dense FP8 = 2 x {pk['source']} bf16 burst",
+                         "frac_of_sustained": round(gemm_tflops / fp8_peak_sus, 4) if fp8_peak_sus else None},
+            "gemm": {"ms": round(gemm_ms, 4), "tflops": round(gemm_tflops, 1)},
+            "cast": {"ms": round(cast_ms, 4), "bytes": cast_bytes, "gbs": round(cast_gbs, 1),
+                     "frac_hbm": round(cast_gbs / pk["hbm_gbs"], 4), "peak_gbs": pk["hbm_gbs"]},
+            "cast_sweep": sweep,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "gpu_launches": 2 * K,
+        }
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    """The CPU oracle timed on the host cores, on a bounded sample per step."""
+    if rank != 0:
+        return
+    m, n, k = args.m, args.n, args.k
+    fmt_code = {"fp32": 0, "ue8m0": 1, "packed": 2}[args.fmt]
+    per_step = max(1.0, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    sample = CpuOracleSample(n, k, fmt_code)
+    threads = sample.threads
+    for _ in range(args.warmup):
+        sample.once()
+    vals, secs, rows_total = [], 0.0, 0
+    for _ in range(args.steps):
+        v, s, rows = sample.run(per_step)
+        vals.append(v)
+        secs += s
+        rows_total += rows
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn; W randn*0.02)",
+        "config": {"workload": WORKLOAD, "m": m, "n": n, "k": k, "gran_k": 128, "scales": args.fmt},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"per step: a slice of X's rows cast + fp64 GEMM against all {n} rows of W; "
+                                   f"{rows_total} rows over {secs:.1f} s"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
