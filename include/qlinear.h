@@ -187,6 +187,14 @@ int ql_get_num_sms(void);
  * tuning and for tests that exercise every tile width. */
 ql_status ql_set_gemm_block_n(int block_n);
 
+/* GEMM promotion path. With UE8M0 scale formats (QL_SF_UE8M0,
+ * QL_SF_PACKED_UE8M0) the default (0) promotes inside the tensor core
+ * (block-scaled MMA, one power-of-two scale per row and 32-wide K slice);
+ * 1 forces the CUDA-core promotion path used for fp32 scales; 2 requests the
+ * block-scaled path (ignored for QL_SF_FP32). Both give results within the
+ * GEMM tolerance of each other. Process-wide; for tuning and tests. */
+ql_status ql_set_gemm_path(int path);
+
 /* Time limit of every bounded wait inside the GEMM kernel, in milliseconds
  * (default 2000). After it runs out the kernel records QL_ERR_DEVICE_TIMEOUT,
  * drains its own copies, frees its tensor memory and returns. Process-wide. */

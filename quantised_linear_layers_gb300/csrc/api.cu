@@ -21,6 +21,7 @@ __device__ uint32_t g_dev_status = 0;
 
 std::atomic<int> g_num_sms_override{0};
 std::atomic<int> g_block_n_override{0};
+std::atomic<int> g_gemm_path{0};
 std::atomic<int> g_wait_limit_ms{2000};
 
 struct DeviceInfo {
@@ -102,6 +103,7 @@ ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sa
     L.ldd = ldd;
     L.accumulate = accumulate ? 1 : 0;
     L.block_n = g_block_n_override.load();
+    L.path = g_gemm_path.load();
     L.dev_status = di.status;
     L.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ms.load()) * 1000000ull;
     return from_cuda(ql::launch_gemm(L, st, effective_sms(di)));
@@ -237,6 +239,12 @@ ql_status ql_set_gemm_block_n(int block_n) {
     if (block_n != 0 && block_n != 32 && block_n != 64 && block_n != 128 && block_n != 256)
         return QL_ERR_INVALID_ARG;
     g_block_n_override.store(block_n);
+    return QL_OK;
+}
+
+ql_status ql_set_gemm_path(int path) {
+    if (path < 0 || path > 2) return QL_ERR_INVALID_ARG;
+    g_gemm_path.store(path);
     return QL_OK;
 }
 

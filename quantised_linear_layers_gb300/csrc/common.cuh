@@ -173,6 +173,47 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// Block-scaled form: D(tmem) (+)= (A * 2^(sfa-127)) * (B * 2^(sfb-127))^T with
+// one UE8M0 scale per row and per 32 elements of K (scale_vec::1X), read from
+// tensor memory (byte selected by the instruction descriptor's scale IDs).
+__device__ __forceinline__ void mma_mxf8_block_scaled(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                      uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                      uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copies a 32-row x 16-byte shared-memory matrix into tensor memory at
+// `taddr`, replicated into all four 32-lane quarters (lanes r, 32+r, 64+r,
+// 96+r receive row r; four 32-bit columns).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled matrix of 16-byte rows stored
+// back to back: 8-row core matrices 128 bytes apart (stride offset), a single
+// core matrix along K (leading offset unused).
+__device__ __forceinline__ uint64_t rows16_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: B scale ID at [4,6),
+// A and B E4M3 (bits 7-9, 10-12 = 0), K-major, N >> 3 at [17,23), scale type
+// UE8M0 (bit 23 = 1), M >> 4 at [24,29), A scale ID at [29,31).
+__host__ __device__ constexpr uint32_t idesc_mxf8_ue8m0(uint32_t M, uint32_t N, uint32_t sfa_id, uint32_t sfb_id) {
+    return (sfb_id << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sfa_id << 29);
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {

@@ -37,6 +37,7 @@ _SIGS = {
     "ql_get_num_sms": [],
     "ql_set_wait_limit_ms": [_int],
     "ql_set_gemm_block_n": [_int],
+    "ql_set_gemm_path": [_int],
     "ql_device_status": [_vp],
     "ql_status_string": [_int],
 }
@@ -212,6 +213,11 @@ def get_num_sms() -> int:
 
 def set_gemm_block_n(bn: int) -> None:
     _check("ql_set_gemm_block_n", load_library().ql_set_gemm_block_n(int(bn)))
+
+
+def set_gemm_path(path: int) -> None:
+    """0 auto, 1 CUDA-core promotion, 2 block-scaled MMA (UE8M0 formats)."""
+    _check("ql_set_gemm_path", load_library().ql_set_gemm_path(int(path)))
 
 
 def set_wait_limit_ms(ms: int) -> None:

@@ -201,3 +201,81 @@ def test_gemm_rejects_misaligned(ops):
     with pytest.raises(ops.QLError) as e:
         ops.gemm_fp8_nt_bf16(a[:, 8:40], s, b[:, 8:40], s, 0)       # base not 16-byte aligned
     assert e.value.status == 3
+
+
+# ------------------------------------------------- block-scaled (UE8M0) path
+def _pow2_grid(rows, cols, seed, lo=-2, hi=2):
+    g = torch.Generator().manual_seed(seed)
+    return torch.pow(2.0, torch.randint(lo, hi + 1, (rows, cols), generator=g).float())
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["promotion", "block_scaled"])
+@pytest.mark.parametrize("bn", [32, 64, 128, 256])
+@pytest.mark.parametrize("k", [1024, 1152, 256])
+@pytest.mark.parametrize("packed", [False, True])
+def test_wgrad_exact_pow2_scales(orc, ops, path, bn, k, packed):
+    """Exact small-integer operands with a distinct power-of-two scale per row,
+    per K block and per column: every partial sum is exact in fp32, so the
+    fp32 output must equal the oracle exactly. A wrong tensor-memory scale
+    layout, scale ID or row mapping changes the result."""
+    m, n = 200, 300
+    kb = -(-k // 128)
+    a = syn.e4m3_small_ints((m, k), seed=41, lo=-4, hi=4)
+    b = syn.e4m3_small_ints((n, k), seed=42, lo=-4, hi=4)
+    aq, bq = a.to(torch.float8_e4m3fn).cuda(), b.to(torch.float8_e4m3fn).cuda()
+    sa, sb = _pow2_grid(m, kb, 43), _pow2_grid(n, kb, 44)
+    if packed:
+        def pack(s):
+            e = ((s.view(torch.int32) >> 23) & 0xFF)
+            e = torch.nn.functional.pad(e, (0, (-e.shape[1]) % 4)).view(e.shape[0], -1, 4)
+            return (e[..., 0] | (e[..., 1] << 8) | (e[..., 2] << 16) | (e[..., 3] << 24)).contiguous()
+        sa_dev, sb_dev, fmt = pack(sa).cuda(), pack(sb).cuda(), 2
+    else:
+        sa_dev, sb_dev, fmt = sa.cuda(), sb.cuda(), 1
+    ops.set_gemm_block_n(bn)
+    ops.set_gemm_path(path)
+    try:
+        d = ops.gemm_fp8_wgrad_fp32(aq, sa_dev, bq, sb_dev, fmt=fmt)
+    finally:
+        ops.set_gemm_block_n(0)
+        ops.set_gemm_path(0)
+    ref = orc.gemm(np_bytes(aq), sa.numpy(), np_bytes(bq), sb.numpy(), 1, b_per_row=True)
+    got = d.double().cpu().numpy()
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} mismatches; first {bad[0]} got {got[tuple(bad[0])]} ref {ref[tuple(bad[0])]}"
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["promotion", "block_scaled"])
+@pytest.mark.parametrize("bn", [32, 64, 128, 256])
+def test_fwd_exact_pow2_block_scales(orc, ops, path, bn):
+    """fwd form: 1x128 A scales and 128x128 B block scales, all powers of two,
+    exact integer operands: the bf16 output equals bf16_rn of the exact sum."""
+    m, n, k = 160, 384, 1152
+    kb = 9
+    a = syn.e4m3_small_ints((m, k), seed=51, lo=-3, hi=3)
+    b = syn.e4m3_small_ints((n, k), seed=52, lo=-3, hi=3)
+    aq, bq = a.to(torch.float8_e4m3fn).cuda(), b.to(torch.float8_e4m3fn).cuda()
+    sa, sb = _pow2_grid(m, kb, 53), _pow2_grid(3, kb, 54)
+    ops.set_gemm_block_n(bn)
+    ops.set_gemm_path(path)
+    try:
+        d = ops.gemm_fp8_nt_bf16(aq, sa.cuda(), bq, sb.cuda(), 1)
+    finally:
+        ops.set_gemm_block_n(0)
+        ops.set_gemm_path(0)
+    ref = orc.gemm(np_bytes(aq), sa.numpy(), np_bytes(bq), sb.numpy(), 1, out="bf16")
+    assert np.array_equal(d.double().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("fmt", [1, 2], ids=["ue8m0", "packed"])
+def test_block_scaled_matches_promotion_random(orc, ops, fmt):
+    x, w, xq, xs, wq, ws = fwd_operands(ops, 512, 768, 2048, fmt, w_mul=0.02)
+    ops.set_gemm_path(1)
+    try:
+        d1 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    finally:
+        ops.set_gemm_path(0)
+    d2 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    ref = oracle_fwd(orc, xq, xs, wq, ws, fmt)
+    check_gemm(d1.float().cpu().numpy(), ref, "promotion")
+    check_gemm(d2.float().cpu().numpy(), ref, "block-scaled")
