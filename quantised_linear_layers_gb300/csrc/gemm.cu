@@ -19,7 +19,7 @@
 //   warps 2-3   scale loaders: sa[128 rows] and sb (one value per 128-column
 //               block, or one per column for wgrad) of each K block into a
 //               shared-memory scale ring (any scale strides; packed UE8M0 is
-//               decoded here).
+//               decoded here), several K blocks per memory round trip.
 //   warps 4-11  two math warpgroups: each thread owns one accumulator row and
 //               BN/2 columns in registers; per K block it reads P_kb from TMEM
 //               (tcgen05.ld) and promotes acc += (sa*sb) * P_kb with packed
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int num_kb = p.num_kb;
 
     if (warp < 4) {
-        regs_dealloc<56>();
+        regs_dealloc<88>();   // 128 x 88 + 256 x 208 = 384 x 168 registers
         if (warp == 0) {
             // ---------------- TMA producer ----------------
             if (elect_one()) {
@@ -261,49 +261,69 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         } else {
-            // ---------------- scale loaders (warps 2, 3: alternate K blocks) ----------------
+            // ---------------- scale loaders ----------------
+            // Warps 2 and 3 take alternate runs of K blocks (four, or two when B
+            // has a scale per row); all loads of a run are issued before any
+            // is stored, so a run costs one memory round trip.
+            constexpr int kRun = PER_ROW_B ? 2 : 4;
+            constexpr int kSbLoads = PER_ROW_B ? BN / 32 : 1;
             const uint32_t mine = static_cast<uint32_t>(warp - 2);
-            uint32_t g = 0;
+            uint32_t g = 0, run = 0;
             bool ok = true;
             const int64_t nblocks_b = (p.n + 127) / 128;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
                 const int64_t m0 = static_cast<int64_t>(mb) * BM, n0 = static_cast<int64_t>(nb) * BN;
-                for (int kb = 0; kb < num_kb; ++kb, ++g) {
-                    if ((g & 1u) != mine) continue;
-                    const uint32_t slot = g % kScaleSlots, ph = (g / kScaleSlots) & 1u;
-                    if (!warp_wait(&sempty[slot], ph ^ 1u, ctl)) { ok = false; break; }
-                    float* dst = sScale + slot * C::kSlotFloats;
-                    float va[4];
+                for (int kb0 = 0; kb0 < num_kb; kb0 += kRun, ++run) {
+                    const int cnt = num_kb - kb0 < kRun ? num_kb - kb0 : kRun;
+                    if ((run & 1u) != mine) { g += cnt; continue; }
+                    float va[kRun][4], vb[kRun][kSbLoads];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int64_t row = m0 + lane + 32 * i;
-                        va[i] = row < p.m ? decode_scale(p.sfa, p.fmt, row * p.sam, kb, p.sak) : 0.0f;
-                    }
-                    if constexpr (PER_ROW_B) {
-                        float vb[BN / 32];
+                    for (int j = 0; j < kRun; ++j) {
 #pragma unroll
-                        for (int i = 0; i < BN / 32; ++i) {
-                            const int64_t col = n0 + lane + 32 * i;
-                            vb[i] = col < p.n ? decode_scale(p.sfb, p.fmt, col * p.sbn, kb, p.sbk) : 0.0f;
+                        for (int i = 0; i < 4; ++i) {
+                            const int64_t row = m0 + lane + 32 * i;
+                            va[j][i] = (j < cnt && row < p.m) ? decode_scale(p.sfa, p.fmt, row * p.sam, kb0 + j, p.sak) : 0.0f;
                         }
 #pragma unroll
-                        for (int i = 0; i < BN / 32; ++i) dst[BM + lane + 32 * i] = vb[i];
-                    } else {
-                        if (lane < (BN + 127) / 128) {
-                            const int64_t r = n0 / 128 + lane;
-                            dst[BM + lane] = r < nblocks_b ? decode_scale(p.sfb, p.fmt, r * p.sbn, kb, p.sbk) : 0.0f;
+                        for (int i = 0; i < kSbLoads; ++i) {
+                            float v = 0.0f;
+                            if (j < cnt) {
+                                if constexpr (PER_ROW_B) {
+                                    const int64_t col = n0 + lane + 32 * i;
+                                    if (col < p.n) v = decode_scale(p.sfb, p.fmt, col * p.sbn, kb0 + j, p.sbk);
+                                } else {
+                                    const int64_t r = n0 / 128 + lane;
+                                    if (lane < (BN + 127) / 128 && r < nblocks_b)
+                                        v = decode_scale(p.sfb, p.fmt, r * p.sbn, kb0 + j, p.sbk);
+                                }
+                            }
+                            vb[j][i] = v;
                         }
                     }
+                    for (int j = 0; j < cnt; ++j) {
+                        const uint32_t gj = g + j;
+                        const uint32_t slot = gj % kScaleSlots, ph = (gj / kScaleSlots) & 1u;
+                        if (!warp_wait(&sempty[slot], ph ^ 1u, ctl)) { ok = false; break; }
+                        float* dst = sScale + slot * C::kSlotFloats;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = va[i];
-                    mbar_arrive(&sfull[slot]);
+                        for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = va[j][i];
+                        if constexpr (PER_ROW_B) {
+#pragma unroll
+                            for (int i = 0; i < kSbLoads; ++i) dst[BM + lane + 32 * i] = vb[j][i];
+                        } else {
+                            if (lane < (BN + 127) / 128) dst[BM + lane] = vb[j][0];
+                        }
+                        mbar_arrive(&sfull[slot]);
+                    }
+                    if (!ok) break;
+                    g += cnt;
                 }
             }
         }
     } else {
-        regs_alloc<224>();
+        regs_alloc<208>();
         // ---------------- math warpgroups: promotion + epilogue ----------------
         constexpr int CPT = C::kColsPerThread;
         const int wg = (warp - 4) >> 2;          // column half

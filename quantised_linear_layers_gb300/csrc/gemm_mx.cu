@@ -20,8 +20,9 @@
 //               from shared to tensor memory, then issues 4 x 4 block-scaled
 //               MMAs selecting byte kb % 4 through the scale IDs.
 //   warps 2-3   scale loaders: per K group, one packed word per row of A and
-//               per row of B (B's 128x128 block exponent repeated over its 128
-//               rows; wgrad: B's own per-row exponents), stored in the order
+//               per row of B (B's 128x128 block exponent, loaded once and
+//               repeated over its 128 rows; wgrad: B's own per-row exponents),
+//               several groups per memory round trip, stored in the order
 //               tcgen05.cp's four-quarter layout expects: row 32q + r of a
 //               128-row chunk goes to 16-byte line r, word q.
 //   warps 4-11  epilogue: after a tile's last MMA, read the fp32 accumulator
@@ -42,7 +43,7 @@ constexpr int kThreads = 384;
 constexpr int kMathThreads = 256;
 constexpr int BM = 128;
 constexpr int BK = 128;
-constexpr int kSfSlots = 4;          // shared-memory scale ring (K groups)
+constexpr int kSfSlots = 8;          // shared-memory scale ring (K groups)
 
 template <int BN>
 struct MxCfg {
@@ -84,22 +85,34 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl)) != 0;
 }
 
-// Packed exponent word of K group g for the scale row at `row_off`: fmt 2
-// reads the int32 word directly; fmt 1 (fp32 powers of two) gathers the four
-// K blocks' exponent fields. K blocks past num_kb contribute byte 0.
-__device__ __forceinline__ uint32_t exp_word(const void* base, int fmt, int64_t row_off, int g, int64_t sk,
-                                             int num_kb) {
-    if (fmt == 2) return __ldg(static_cast<const uint32_t*>(base) + row_off + g * sk);
-    uint32_t w = 0;
+// Exponent words of K group g for R scale rows at once (row r at element
+// offset row_off[r]): fmt 2 reads the packed int32 word; fmt 1 (fp32 powers
+// of two) gathers the exponent fields of the group's four K blocks. Every
+// global load is issued before any is used, so a call costs one memory round
+// trip. K blocks past num_kb contribute byte 0.
+template <int R>
+__device__ __forceinline__ void exp_words(const void* base, int fmt, const int64_t (&row_off)[R],
+                                          const bool (&valid)[R], int g, int64_t sk, int num_kb, uint32_t (&w)[R]) {
+    if (fmt == 2) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int kb = 4 * g + j;
-        if (kb < num_kb) {
-            const uint32_t bits = __float_as_uint(__ldg(static_cast<const float*>(base) + row_off + kb * sk));
-            w |= ((bits >> 23) & 0xFFu) << (8 * j);
-        }
+        for (int r = 0; r < R; ++r)
+            w[r] = valid[r] ? __ldg(static_cast<const uint32_t*>(base) + row_off[r] + g * sk) : 0u;
+        return;
     }
-    return w;
+    uint32_t bits[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            bits[r][j] = (valid[r] && 4 * g + j < num_kb)
+                             ? __float_as_uint(__ldg(static_cast<const float*>(base) + row_off[r] + (4 * g + j) * sk))
+                             : 0u;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        w[r] = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[r] |= ((bits[r][j] >> 23) & 0xFFu) << (8 * j);
+    }
 }
 
 template <int BN, bool PER_ROW_B, bool OUT_F32>
@@ -223,50 +236,85 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         } else {
-            // scale loaders: warps 2 and 3 take alternate K groups
+            // scale loaders: warps 2 and 3 take alternate runs of K groups. A run
+            // is four groups when the exponents are packed (two when B has a
+            // word per row), else one group (four loads per word); all loads of
+            // a run are issued before any is stored, so a run costs one memory
+            // round trip. Line r of a 128-row chunk holds the words of rows
+            // r, 32+r, 64+r, 96+r.
+            constexpr int R = PER_ROW_B ? 2 : 4;
+            constexpr int NB = PER_ROW_B ? 4 * C::kSfbChunks : 1;
             const uint32_t mine = static_cast<uint32_t>(warp - 2);
-            uint32_t g = 0;
+            const int run_len = (p.fmt == 2) ? R : 1;
+            uint32_t g = 0, run = 0;
             bool ok = true;
             const int64_t nblocks_b = (p.n + 127) / 128;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
                 const int64_t m0 = static_cast<int64_t>(mb) * BM, n0 = static_cast<int64_t>(nb) * BN;
-                for (int kg = 0; kg < num_groups; ++kg, ++g) {
-                    if ((g & 1u) != mine) continue;
-                    const uint32_t slot = g % kSfSlots, ph = (g / kSfSlots) & 1u;
-                    if (!warp_wait(&sempty[slot], ph ^ 1u, ctl)) { ok = false; break; }
-                    uint32_t* dst = sSf + slot * C::kSlotWords;
-                    // line r of a 128-row chunk holds the words of rows r, 32+r, 64+r, 96+r
-                    {
-                        uint32_t w[4];
+                for (int kg0 = 0; kg0 < num_groups; kg0 += run_len, ++run) {
+                    const int cnt = num_groups - kg0 < run_len ? num_groups - kg0 : run_len;
+                    if ((run & 1u) != mine) { g += cnt; continue; }
+                    uint32_t wa[R][4], wb[R][NB];
+                    int64_t offa[4], offb[NB];
+                    bool vala[4], valb[NB];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int64_t row = m0 + 32 * q + lane;
-                            w[q] = row < p.m ? exp_word(p.sfa, p.fmt, row * p.sam, kg, p.sak, num_kb) : 0u;
-                        }
-                        *reinterpret_cast<uint4*>(dst + lane * 4) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int q = 0; q < 4; ++q) {
+                        const int64_t row = m0 + 32 * q + lane;
+                        vala[q] = row < p.m;
+                        offa[q] = row * p.sam;
                     }
-#pragma unroll 1
-                    for (int c = 0; c < C::kSfbChunks; ++c) {
-                        uint32_t w[4];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int64_t row = n0 + 128 * c + 32 * q + lane;
-                            w[q] = 0;
-                            if (row < p.n && row < n0 + BN) {
-                                if constexpr (PER_ROW_B) {
-                                    w[q] = exp_word(p.sfb, p.fmt, row * p.sbn, kg, p.sbk, num_kb);
-                                } else {
-                                    const int64_t r = row / 128;
-                                    if (r < nblocks_b) w[q] = exp_word(p.sfb, p.fmt, r * p.sbn, kg, p.sbk, num_kb);
-                                }
+                    for (int i = 0; i < NB; ++i) {
+                        if constexpr (PER_ROW_B) {
+                            const int64_t row = n0 + 32 * i + lane;        // chunk i/4, quarter i%4
+                            valb[i] = row < p.n;
+                            offb[i] = row * p.sbn;
+                        } else {
+                            const int64_t r = n0 / 128 + lane;             // one block word per chunk
+                            valb[i] = lane < C::kSfbChunks && r < nblocks_b;
+                            offb[i] = r * p.sbn;
+                        }
+                    }
+                    if (p.fmt == 2) {
+#pragma unroll
+                        for (int j = 0; j < R; ++j) {
+                            const bool in = j < cnt;
+                            bool va[4], vb[NB];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) va[q] = vala[q] && in;
+#pragma unroll
+                            for (int i = 0; i < NB; ++i) vb[i] = valb[i] && in;
+                            exp_words<4>(p.sfa, 2, offa, va, kg0 + j, p.sak, num_kb, wa[j]);
+                            exp_words<NB>(p.sfb, 2, offb, vb, kg0 + j, p.sbk, num_kb, wb[j]);
+                        }
+                    } else {
+                        exp_words<4>(p.sfa, p.fmt, offa, vala, kg0, p.sak, num_kb, wa[0]);
+                        exp_words<NB>(p.sfb, p.fmt, offb, valb, kg0, p.sbk, num_kb, wb[0]);
+                    }
+                    for (int j = 0; j < cnt; ++j) {
+                        const uint32_t gj = g + j;
+                        const uint32_t slot = gj % kSfSlots, ph = (gj / kSfSlots) & 1u;
+                        if (!warp_wait(&sempty[slot], ph ^ 1u, ctl)) { ok = false; break; }
+                        uint32_t* dst = sSf + slot * C::kSlotWords;
+                        *reinterpret_cast<uint4*>(dst + lane * 4) = make_uint4(wa[j][0], wa[j][1], wa[j][2], wa[j][3]);
+#pragma unroll
+                        for (int c = 0; c < C::kSfbChunks; ++c) {
+                            uint4 v;
+                            if constexpr (PER_ROW_B) {
+                                v = make_uint4(wb[j][4 * c], wb[j][4 * c + 1], wb[j][4 * c + 2], wb[j][4 * c + 3]);
+                            } else {
+                                const uint32_t wbc = __shfl_sync(0xffffffffu, wb[j][0], c);
+                                v = make_uint4(wbc, wbc, wbc, wbc);
                             }
+                            *reinterpret_cast<uint4*>(dst + BM + 128 * c + lane * 4) = v;
                         }
-                        *reinterpret_cast<uint4*>(dst + BM + 128 * c + lane * 4) = make_uint4(w[0], w[1], w[2], w[3]);
+                        fence_proxy_async_smem();   // visible to tcgen05.cp (async proxy)
+                        mbar_arrive(&sfull[slot]);
                     }
-                    fence_proxy_async_smem();   // visible to tcgen05.cp (async proxy)
-                    mbar_arrive(&sfull[slot]);
+                    if (!ok) break;
+                    g += cnt;
                 }
             }
         }
