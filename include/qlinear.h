@@ -106,18 +106,23 @@ ql_status fp8_cast_per_token(const void* x, ql_dtype x_dtype, int64_t m, int64_t
  * 128x128 block cast of "DeepGEMM Essentials" Part 4 (the RHS / weight cast).
  * Same arithmetic as fp8_cast_per_token with the group being a 128x128 block
  * (edge blocks partial). Scales fp32 [ceil(m/128), ceil(n/128)] at
- * out_sf[r*sf_stride_r + c*sf_stride_c]; fmt is QL_SF_FP32 or QL_SF_UE8M0
- * (optionally | QL_CAST_RECIP_OF_SCALE with QL_SF_FP32).
+ * out_sf[r*sf_stride_r + c*sf_stride_c] for QL_SF_FP32 / QL_SF_UE8M0
+ * (optionally | QL_CAST_RECIP_OF_SCALE with QL_SF_FP32); for
+ * QL_SF_PACKED_UE8M0 int32 words [ceil(m/128), ceil(ceil(n/128)/4)] packed
+ * along the column-block axis (block c is byte c % 4 of word c / 4, pad bytes
+ * 0) at out_sf[r*sf_stride_r + w*sf_stride_c]: the GEMM's B-scale layout.
  * Either view may be transposed: x_stride_m == 1 reads x column-wise, and
- * out_stride_m == 1 writes the data transposed; since a block's amax does not
- * depend on orientation, passing out = W^T's storage with transposed strides
- * and out_sf with swapped strides yields cast_per_block(W^T) in the same pass
- * (the dgrad operand of "[Help] Starter script for nn.Linear for fwd,bwd").
+ * out_stride_m == 1 writes the data transposed. Since a block's amax does not
+ * depend on orientation, cast_per_block(W^T) (the dgrad operand of "[Help]
+ * Starter script for nn.Linear for fwd,bwd") is obtained either by passing
+ * x = W^T as a transposed view of W, or (fp32 / UE8M0 scales) by writing W's
+ * cast through transposed out / out_sf views; for packed scales use the first
+ * form, so that the words pack along W^T's column blocks.
  * ------------------------------------------------------------------------- */
 ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t n,
                              int64_t x_stride_m, int64_t x_stride_n, int fmt,
                              uint8_t* out, int64_t out_stride_m, int64_t out_stride_n,
-                             float* out_sf, int64_t sf_stride_r, int64_t sf_stride_c,
+                             void* out_sf, int64_t sf_stride_r, int64_t sf_stride_c,
                              ql_stream_t stream);
 
 /* ---------------------------------------------------------------------------

@@ -170,12 +170,15 @@ def cast_per_token(x: np.ndarray, gran: int, fmt: int, recip: bool = False,
 
 def cast_per_block(x: np.ndarray, fmt: int, recip: bool = False,
                    out: np.ndarray | None = None, out_sf: np.ndarray | None = None):
-    """128x128 block cast. Returns (data uint8 [m,n], scales float32 [ceil(m/128), ceil(n/128)])."""
+    """128x128 block cast. Returns (data uint8 [m,n], scales float32 [ceil(m/128), ceil(n/128)],
+    or int32 words [ceil(m/128), ceil(ceil(n/128)/4)] packed along column blocks for fmt 2)."""
     m, n = x.shape
     if out is None:
         out = np.empty((m, n), dtype=np.uint8)
     if out_sf is None:
-        out_sf = np.empty((-(-m // 128), -(-n // 128)), dtype=np.float32)
+        C = -(-n // 128)
+        out_sf = (np.empty((-(-m // 128), C), dtype=np.float32) if fmt != SF_PACKED_UE8M0
+                  else np.empty((-(-m // 128), -(-C // 4)), dtype=np.int32))
     sx, so, ss = _elem_strides(x), _elem_strides(out), _elem_strides(out_sf)
     rc = _load().oracle_cast_per_block(_ptr(x), _dtype_code(x), m, n, sx[0], sx[1], fmt,
                                        int(bool(recip)), _ptr(out), so[0], so[1],

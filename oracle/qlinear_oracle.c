@@ -255,15 +255,19 @@ int oracle_cast_per_token(const void* x, int dtype, int64_t m, int64_t n,
 
 /* ------------------------------------------------------------------------
  * Per-block (128x128) cast (Part 4). Scales fp32 [ceil(m/128), ceil(n/128)]
- * at sf[r*ssr + c*ssc] (fp32 or UE8M0-as-fp32; no packed form).
+ * at sf[r*ssr + c*ssc] (fp32 or UE8M0-as-fp32), or packed UE8M0 int32 words
+ * along the column-block axis: block c is byte c % 4 of word c / 4.
  * ---------------------------------------------------------------------- */
 int oracle_cast_per_block(const void* x, int dtype, int64_t m, int64_t n,
                           int64_t sxm, int64_t sxn, int fmt, int recip,
                           uint8_t* out, int64_t som, int64_t son,
-                          float* sf, int64_t ssr, int64_t ssc) {
+                          void* sf, int64_t ssr, int64_t ssc) {
     const int64_t B = 128;
-    if (m < 0 || n < 0 || fmt == OR_SF_PACKED_UE8M0) return -1;
+    if (m < 0 || n < 0) return -1;
     int64_t R = (m + B - 1) / B, C = (n + B - 1) / B;
+    if (fmt == OR_SF_PACKED_UE8M0)          /* words along the column-block axis start at 0 */
+        for (int64_t r = 0; r < R; ++r)
+            for (int64_t w = 0; w < (C + 3) / 4; ++w) ((int32_t*)sf)[r * ssr + w * ssc] = 0;
     #pragma omp parallel for collapse(2) schedule(static)
     for (int64_t r = 0; r < R; ++r) {
         for (int64_t c = 0; c < C; ++c) {
@@ -280,7 +284,13 @@ int oracle_cast_per_block(const void* x, int dtype, int64_t m, int64_t n,
             for (int64_t i = r * B; i < i1; ++i)
                 for (int64_t j = c * B; j < j1; ++j)
                     out[i * som + j * son] = quantise(load_elem(x, dtype, i * sxm + j * sxn), f);
-            sf[r * ssr + c * ssc] = (float)s;
+            if (fmt == OR_SF_PACKED_UE8M0) {
+                uint32_t* word = (uint32_t*)sf + (r * ssr + (c / 4) * ssc);
+                #pragma omp atomic
+                *word |= ((uint32_t)ue8m0_byte(s)) << (8 * (c % 4));
+            } else {
+                ((float*)sf)[r * ssr + c * ssc] = (float)s;
+            }
         }
     }
     return 0;

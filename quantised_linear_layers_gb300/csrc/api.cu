@@ -162,12 +162,12 @@ ql_status fp8_cast_per_token(const void* x, ql_dtype x_dtype, int64_t m, int64_t
 
 ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t n, int64_t x_stride_m,
                              int64_t x_stride_n, int fmt, uint8_t* out, int64_t out_stride_m, int64_t out_stride_n,
-                             float* out_sf, int64_t sf_stride_r, int64_t sf_stride_c, ql_stream_t stream) {
+                             void* out_sf, int64_t sf_stride_r, int64_t sf_stride_c, ql_stream_t stream) {
     if (m < 0 || n < 0) return QL_ERR_INVALID_ARG;
     if (x_dtype != QL_BF16 && x_dtype != QL_F32) return QL_ERR_INVALID_ARG;
     const bool recip = (fmt & QL_CAST_RECIP_OF_SCALE) != 0;
     const int base = fmt & ~QL_CAST_RECIP_OF_SCALE;
-    if (base != QL_SF_FP32 && base != QL_SF_UE8M0) return QL_ERR_INVALID_ARG;
+    if (base < QL_SF_FP32 || base > QL_SF_PACKED_UE8M0) return QL_ERR_INVALID_ARG;
     if (recip && base != QL_SF_FP32) return QL_ERR_INVALID_ARG;
     if (m == 0 || n == 0) return QL_OK;
     if (x == nullptr || out == nullptr || out_sf == nullptr) return QL_ERR_INVALID_ARG;

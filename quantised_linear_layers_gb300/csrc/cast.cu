@@ -295,7 +295,7 @@ template <typename T, int FMT, bool RECIP>
 __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x, int64_t m, int64_t n,
                                                          int64_t sxm, int64_t sxn, int in_mode,
                                                          uint8_t* __restrict__ out, int64_t som, int64_t son,
-                                                         int out_mode, float* __restrict__ sf, int64_t ssr,
+                                                         int out_mode, void* __restrict__ sf, int64_t ssr,
                                                          int64_t ssc) {
     constexpr int B = 128, kPad = 16;
     __shared__ __align__(16) uint8_t q[B][B + kPad];
@@ -369,7 +369,19 @@ __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x
     float s, f;
     uint32_t ebyte;
     group_scale<FMT, RECIP>(amax, s, f, ebyte);
-    if (tid == 0) sf[static_cast<int64_t>(blockIdx.y) * ssr + static_cast<int64_t>(blockIdx.x) * ssc] = s;
+    if (tid == 0) {
+        const int64_t br = blockIdx.y, bc = blockIdx.x;
+        if constexpr (FMT != kSfPacked) {
+            static_cast<float*>(sf)[br * ssr + bc * ssc] = s;
+        } else {
+            // packed along the column-block axis: block bc is byte bc % 4 of
+            // word bc / 4; the last column block also zeroes the pad bytes
+            uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + br * ssr + (bc / 4) * ssc);
+            word[bc % 4] = static_cast<uint8_t>(ebyte);
+            if (bc == static_cast<int64_t>(gridDim.x) - 1)
+                for (int64_t z = bc % 4 + 1; z < 4; ++z) word[z] = 0;
+        }
+    }
 
     // quantise into shared memory, block-relative [row][col]
 #pragma unroll
@@ -500,6 +512,7 @@ cudaError_t launch_block_t(const CastBlockArgs& a, cudaStream_t st) {
 template <typename T>
 cudaError_t launch_block_fmt(const CastBlockArgs& a, cudaStream_t st) {
     if (a.fmt == kSfUe8m0) return launch_block_t<T, kSfUe8m0, false>(a, st);
+    if (a.fmt == kSfPacked) return launch_block_t<T, kSfPacked, false>(a, st);
     return a.recip ? launch_block_t<T, kSfFp32, true>(a, st) : launch_block_t<T, kSfFp32, false>(a, st);
 }
 

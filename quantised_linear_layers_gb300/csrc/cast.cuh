@@ -22,11 +22,11 @@ struct CastBlockArgs {
     const void* x;
     bool is_bf16;
     int64_t m, n, sxm, sxn;
-    int fmt;       // 0 fp32, 1 UE8M0 (fp32 storage)
+    int fmt;       // 0 fp32, 1 UE8M0 (fp32 storage), 2 packed UE8M0 (along column blocks)
     bool recip;
     uint8_t* out;
     int64_t som, son;
-    float* sf;
+    void* sf;
     int64_t ssr, ssc;
 };
 

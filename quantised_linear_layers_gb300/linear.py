@@ -1,0 +1,114 @@
+"""FP8 linear layer: forward, dgrad and wgrad over the library's cast and GEMM.
+
+Follows the three functions of "[Help] Starter script for nn.Linear for
+fwd,bwd" (maintainer's pseudo-code) and the integration of "DeepGEMM
+Essentials: High-Performance FP8 Matrix Multiplication" Part 18:
+
+  fwd    Y  = X  W^T  : cast X per token; GEMM against W's 128x128 block cast
+  dgrad  dX = dY W    : cast dY per token; GEMM against W^T's block cast
+  wgrad  dW = dY^T X  : cast dY^T and X^T per token along the token axis (the
+                        transposed views are read in place); wgrad GEMM with
+                        fp32 output, optionally accumulated into a main grad
+
+W and W^T are cast once per weight update (``FP8Weight``), not every forward.
+Every step runs in the CUDA library; torch only allocates outputs.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import ops
+
+
+class FP8Weight:
+    """A weight W [out, in] and its two E4M3 casts with 128x128 block scales:
+    W (the forward operand) and W^T (the dgrad operand, read from W column-wise,
+    so no transposed copy of W is made)."""
+
+    def __init__(self, w: torch.Tensor, fmt: int = ops.SF_PACKED_UE8M0):
+        self.fmt = fmt
+        self.update(w)
+
+    def update(self, w: torch.Tensor) -> None:
+        if w.dim() != 2:
+            raise ValueError("weight must be 2-D [out_features, in_features]")
+        self.shape = tuple(w.shape)
+        self.wq, self.ws = ops.fp8_cast_per_block(w, self.fmt)
+        self.wtq, self.wts = ops.fp8_cast_per_block(w.t(), self.fmt)
+
+
+def _cast_rows(x: torch.Tensor, fmt: int, mn_major: bool = True):
+    return ops.fp8_cast_per_token(x, 128, fmt, sf_mn_major=mn_major)
+
+
+def forward(x: torch.Tensor, w: FP8Weight, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y [T, out] = X [T, in] W^T (bf16)."""
+    xq, xs = _cast_rows(x, w.fmt)
+    return ops.gemm_fp8_nt_bf16(xq, xs, w.wq, w.ws, w.fmt, out=out)
+
+
+def dgrad(dy: torch.Tensor, w: FP8Weight, out: torch.Tensor | None = None) -> torch.Tensor:
+    """dX [T, in] = dY [T, out] W (bf16)."""
+    dq, ds = _cast_rows(dy, w.fmt)
+    return ops.gemm_fp8_nt_bf16(dq, ds, w.wtq, w.wts, w.fmt, out=out)
+
+
+def wgrad(dy: torch.Tensor, x: torch.Tensor, fmt: int = ops.SF_PACKED_UE8M0,
+          out: torch.Tensor | None = None, accumulate: bool = False) -> torch.Tensor:
+    """dW [out, in] (+)= dY^T X (fp32); K is the token axis, both operands with
+    1x128 scales along it."""
+    aq, sa = _cast_rows(dy.t(), fmt)
+    bq, sb = _cast_rows(x.t(), fmt, mn_major=False)
+    return ops.gemm_fp8_wgrad_fp32(aq, sa, bq, sb, out=out, accumulate=accumulate, fmt=fmt)
+
+
+class _FP8LinearFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, weight, w8, module):
+        ctx.save_for_backward(x)
+        ctx.w8 = w8
+        ctx.module = module
+        return forward(x, w8)
+
+    @staticmethod
+    def backward(ctx, dy):
+        (x,) = ctx.saved_tensors
+        dy = dy.contiguous()
+        dx = dgrad(dy, ctx.w8) if ctx.needs_input_grad[0] else None
+        module = ctx.module
+        if module is not None and module.main_grad is not None:
+            wgrad(dy, x, ctx.w8.fmt, out=module.main_grad, accumulate=True)
+            dw = None
+        else:
+            dw = wgrad(dy, x, ctx.w8.fmt).to(x.dtype) if ctx.needs_input_grad[1] else None
+        return dx, dw, None, None
+
+
+class FP8Linear(torch.nn.Module):
+    """nn.Linear (no bias) whose fwd / dgrad / wgrad run through the FP8 cast and
+    GEMM. With ``accumulate_main_grad`` the weight gradient accumulates into the
+    fp32 buffer ``main_grad`` (as the wgrad GEMM's accumulate form) instead of
+    being returned to autograd."""
+
+    def __init__(self, in_features: int, out_features: int, fmt: int = ops.SF_PACKED_UE8M0,
+                 device=None, dtype=torch.bfloat16, accumulate_main_grad: bool = False):
+        super().__init__()
+        self.weight = torch.nn.Parameter(torch.empty((out_features, in_features), device=device, dtype=dtype))
+        torch.nn.init.normal_(self.weight, std=0.02)
+        self.fmt = fmt
+        self.main_grad = (torch.zeros((out_features, in_features), device=device, dtype=torch.float32)
+                          if accumulate_main_grad else None)
+        self._w8 = None
+        self._w8_version = None
+
+    def fp8_weight(self) -> FP8Weight:
+        """The cached casts of the weight, refreshed when the weight changed."""
+        v = self.weight._version
+        if self._w8 is None or self._w8_version != v:
+            with torch.no_grad():
+                self._w8 = FP8Weight(self.weight.detach(), self.fmt)
+            self._w8_version = v
+        return self._w8
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return _FP8LinearFn.apply(x, self.weight, self.fp8_weight(), self)

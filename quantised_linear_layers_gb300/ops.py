@@ -137,15 +137,21 @@ def fp8_cast_per_token(x: torch.Tensor, gran_k: int = 128, fmt: int = SF_FP32, r
 
 def fp8_cast_per_block(x: torch.Tensor, fmt: int = SF_FP32, recip: bool = False,
                        out: torch.Tensor | None = None, out_sf: torch.Tensor | None = None):
-    """128x128 block FP8 cast. Returns (data [m, n], scales fp32 [ceil(m/128), ceil(n/128)]).
-    ``out`` / ``out_sf`` may be transposed views (e.g. ``wt.t()``) to write W^T's cast."""
+    """128x128 block FP8 cast. Returns (data [m, n], scales fp32 [ceil(m/128), ceil(n/128)],
+    or int32 words [ceil(m/128), ceil(ceil(n/128)/4)] packed along the column blocks
+    for SF_PACKED_UE8M0). ``out`` / ``out_sf`` may be transposed views (e.g.
+    ``wt.t()``) to write W^T's cast."""
     if x.dim() != 2:
         raise ValueError("x must be 2-D")
     m, n = x.shape
     if out is None:
         out = torch.empty((m, n), dtype=torch.float8_e4m3fn, device=x.device)
     if out_sf is None:
-        out_sf = torch.empty((_ceil(m, 128), _ceil(n, 128)), dtype=torch.float32, device=x.device)
+        cols = _ceil(n, 128)
+        if fmt == SF_PACKED_UE8M0:
+            out_sf = torch.empty((_ceil(m, 128), _ceil(cols, 4)), dtype=torch.int32, device=x.device)
+        else:
+            out_sf = torch.empty((_ceil(m, 128), cols), dtype=torch.float32, device=x.device)
     _bytes8(out)
     code = fmt | (CAST_RECIP_OF_SCALE if recip else 0)
     st = load_library().fp8_cast_per_block(

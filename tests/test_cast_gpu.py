@@ -203,3 +203,19 @@ def test_block_cast_large_weight_ue8m0(orc, ops):
     oq, os_ = orc.cast_per_block(np_input(w), 1)
     assert np.array_equal(np_bytes(q), oq)
     assert np.array_equal(np_sf(s), os_)
+
+
+@pytest.mark.parametrize("transposed_input", [False, True])
+@pytest.mark.parametrize("shape", [(300, 5 * 128 + 7), (4096, 7168)])
+def test_block_cast_packed(orc, ops, shape, transposed_input):
+    """Packed UE8M0 block scales (four column blocks per word, pad bytes 0),
+    from a row-major or a transposed input view."""
+    w = syn.randn(shape, seed=syn.SEED_W, mul=0.02)
+    if transposed_input:
+        q, s = ops.fp8_cast_per_block(w.cuda().t(), 2)
+        oq, os_ = orc.cast_per_block(np_input(w).T, 2)
+    else:
+        q, s = ops.fp8_cast_per_block(w.cuda(), 2)
+        oq, os_ = orc.cast_per_block(np_input(w), 2)
+    assert np.array_equal(np_bytes(q), oq)
+    assert np.array_equal(np_sf(s).view(np.uint32), os_.view(np.uint32))

@@ -1,0 +1,114 @@
+"""The Linear layer's fwd / dgrad / wgrad on the GPU against the CPU oracle.
+
+"[Help] Starter script for nn.Linear for fwd,bwd" (maintainer's pseudo-code):
+fwd casts X per token and multiplies by W's block cast; dgrad casts dY and
+multiplies by W^T's block cast (W transposed and requantised in 128x128
+blocks); wgrad casts dY^T and X^T per token along the token axis and writes
+fp32. Every cast is compared bit for bit with the oracle, every GEMM within
+the GEMM tolerance, at the full nn.Linear workload (X [4096, 7168],
+dY [4096, 4096], W [4096, 7168] * 0.02) on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import check_gemm, np_bytes, np_input, np_sf
+from quantised_linear_layers_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lin():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from quantised_linear_layers_gb300 import build, ops
+    build.build()
+    ops.load_library()
+    from quantised_linear_layers_gb300 import linear
+    return linear
+
+
+def oracle_fmt(fmt):
+    return fmt
+
+
+@pytest.mark.parametrize("fmt", [0, 2], ids=["fp32", "packed"])
+@pytest.mark.parametrize("shape", [(4096, 7168, 4096), (300, 640, 384)], ids=["full", "ragged"])
+def test_linear_fwd_dgrad_wgrad(orc, lin, fmt, shape):
+    T, IN, OUT = shape
+    x = syn.randn((T, IN), seed=syn.SEED_X)
+    dy = syn.randn((T, OUT), seed=syn.SEED_DY)
+    w = syn.randn((OUT, IN), seed=syn.SEED_W, mul=0.02)
+    xg, dyg, wg = x.cuda(), dy.cuda(), w.cuda()
+    w8 = lin.FP8Weight(wg, fmt)
+    # weight casts: W and W^T, bit-exact
+    bfmt = fmt
+    oq, os_ = orc.cast_per_block(np_input(w), bfmt)
+    assert np.array_equal(np_bytes(w8.wq), oq) and np.array_equal(np_sf(w8.ws).view(np.uint32), os_.view(np.uint32))
+    otq, ots = orc.cast_per_block(np_input(w).T, bfmt)
+    assert np.array_equal(np_bytes(w8.wtq), otq)
+    assert np.array_equal(np_sf(w8.wts).view(np.uint32), ots.view(np.uint32))
+
+    rng = np.random.default_rng(11)
+    rows_t = np.sort(rng.choice(T, min(T, 24), replace=False))
+    rows_o = np.sort(rng.choice(OUT, min(OUT, 16), replace=False))
+
+    # fwd
+    y = lin.forward(xg, w8)
+    xq, xs = orc.cast_per_token(np_input(x), 128, fmt)
+    ref = orc.gemm(xq, xs, oq, os_, fmt, rows=rows_t, out="bf16")
+    check_gemm(y[torch.from_numpy(rows_t).cuda()].float().cpu().numpy(), ref, "fwd")
+    # dgrad
+    dx = lin.dgrad(dyg, w8)
+    dq, ds = orc.cast_per_token(np_input(dy), 128, fmt)
+    ref = orc.gemm(dq, ds, otq, ots, fmt, rows=rows_t, out="bf16")
+    check_gemm(dx[torch.from_numpy(rows_t).cuda()].float().cpu().numpy(), ref, "dgrad")
+    # wgrad, fresh and accumulated into an fp32 main grad
+    dw = lin.wgrad(dyg, xg, fmt)
+    aq, sa = orc.cast_per_token(np_input(dy).T, 128, fmt)
+    bq, sb = orc.cast_per_token(np_input(x).T, 128, fmt)
+    ref = orc.gemm(aq, sa, bq, sb, fmt, b_per_row=True, rows=rows_o, out="f32")
+    check_gemm(dw[torch.from_numpy(rows_o).cuda()].double().cpu().numpy(), ref, "wgrad")
+    main = syn.randn((OUT, IN), seed=5, dtype=torch.float32, mul=0.1).cuda()
+    main0 = main.clone()
+    lin.wgrad(dyg, xg, fmt, out=main, accumulate=True)
+    ref_acc = orc.gemm(aq, sa, bq, sb, fmt, b_per_row=True, rows=rows_o,
+                       d_in=main0.double().cpu().numpy(), out="f32")
+    check_gemm(main[torch.from_numpy(rows_o).cuda()].double().cpu().numpy(), ref_acc, "wgrad accumulate")
+    # informational: the quantised layer stays close to the bf16 product
+    full = (xg.float() @ wg.float().t())
+    rel = (torch.linalg.norm(y.float() - full) / torch.linalg.norm(full)).item()
+    assert rel < 0.05
+
+
+def test_fp8_linear_module_autograd(orc, lin):
+    torch.manual_seed(0)
+    T, IN, OUT = 512, 1024, 768
+    m = lin.FP8Linear(IN, OUT, device="cuda")
+    x = syn.randn((T, IN), seed=syn.SEED_X).cuda().requires_grad_(True)
+    y = m(x)
+    dy = syn.randn((T, OUT), seed=syn.SEED_DY).cuda()
+    y.backward(dy)
+    w8 = m.fp8_weight()
+    ref_y = lin.forward(x.detach(), w8)
+    assert torch.equal(y, ref_y)
+    assert torch.equal(x.grad, lin.dgrad(dy, w8))
+    dw = lin.wgrad(dy, x.detach(), m.fmt)
+    assert torch.equal(m.weight.grad, dw.to(torch.bfloat16))
+    # a weight update refreshes the cached casts
+    with torch.no_grad():
+        m.weight.mul_(2.0)
+    assert m.fp8_weight() is not w8
+
+
+def test_fp8_linear_main_grad_accumulates(lin):
+    T, IN, OUT = 256, 512, 384
+    m = lin.FP8Linear(IN, OUT, device="cuda", accumulate_main_grad=True)
+    x = syn.randn((T, IN), seed=syn.SEED_X).cuda().requires_grad_(True)
+    dy = syn.randn((T, OUT), seed=syn.SEED_DY).cuda()
+    m(x).backward(dy)
+    g1 = m.main_grad.clone()
+    m(x).backward(dy)
+    assert m.weight.grad is None
+    assert torch.allclose(m.main_grad, 2 * g1, rtol=1e-5, atol=1e-5)

@@ -473,3 +473,18 @@ def test_gemm_output_rounding_option(orc):
     rounded = orc.gemm(qa, sa, qb, sb, orc.SF_FP32, out="bf16")
     assert np.array_equal(rounded, orc.round_output(exact, "bf16"))
     assert np.max(np.abs(rounded - exact) / np.maximum(np.abs(exact), 1e-30)) <= 2.0 ** -8
+
+
+def test_block_cast_packed_words(orc):
+    """Packed block scales hold the biased exponents of the UE8M0 block scales,
+    four column blocks per word, pad bytes zero (odd column-block count)."""
+    w = syn.randn((300, 5 * 128 + 7), seed=syn.SEED_W, mul=0.02)
+    wb = bf16_bits(w)
+    q1, s1 = orc.cast_per_block(wb, orc.SF_UE8M0)
+    q2, s2 = orc.cast_per_block(wb, orc.SF_PACKED_UE8M0)
+    assert np.array_equal(q1, q2)
+    assert s2.shape == (3, 2) and s1.shape == (3, 6)
+    e = ((s1.view(np.uint32) >> 23) & 0xFF).astype(np.uint8)
+    padded = np.zeros((3, 8), dtype=np.uint8)
+    padded[:, :6] = e
+    assert np.array_equal(s2.view(np.uint8).reshape(3, 8), padded)
