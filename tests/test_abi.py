@@ -75,8 +75,9 @@ def test_host_validation_rejects_before_cuda(lib):
     # bad dtype; null pointers
     assert L.fp8_cast_per_token(p, 9, 4, 256, 256, 1, 128, 0, p, 256, 1, p, 2, 1, None) == 1
     assert L.fp8_cast_per_token(None, 0, 4, 256, 256, 1, 128, 0, p, 256, 1, p, 2, 1, None) == 1
-    # block cast: packed format is not a block format
-    assert L.fp8_cast_per_block(p, 0, 4, 256, 256, 1, 2, p, 256, 1, p, 2, 1, None) == 1
+    # block cast: unknown format; recip with a UE8M0 format
+    assert L.fp8_cast_per_block(p, 0, 4, 256, 256, 1, 3, p, 256, 1, p, 2, 1, None) == 1
+    assert L.fp8_cast_per_block(p, 0, 4, 256, 256, 1, 0x102, p, 256, 1, p, 2, 1, None) == 1
     # empty problems are no-ops (no CUDA call)
     assert L.fp8_cast_per_token(None, 0, 0, 256, 256, 1, 128, 0, None, 256, 1, None, 2, 1, None) == 0
     assert L.gemm_fp8_nt_bf16(None, 16, None, 1, 1, None, 16, None, 1, 1, 0, None, 16, 0, 16, 16, None, 0,

@@ -160,7 +160,7 @@ def test_cast_invalid_arguments(ops):
     with pytest.raises(ops.QLError):
         ops.fp8_cast_per_token(x, 128, 1, recip=True)
     with pytest.raises(ops.QLError):
-        ops.fp8_cast_per_block(x, 2)
+        ops.fp8_cast_per_block(x, 3)
 
 
 # ---------------------------------------------------------------- block cast
