@@ -517,6 +517,13 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     // UE8M0 scales (fp32 powers of two or packed exponents): promotion by the
     // tensor core's block-scaled MMA unless the CUDA-core path is requested.
     const bool ue8m0 = L.fmt == 1 || L.fmt == 2;
+    if (ue8m0 && L.path == 3) return launch_gemm_mx2(L, p, st, num_sms);
+    if (ue8m0 && L.path == 0) {
+        // CTA pairs on 256 x 256 tiles when there are enough tiles to give
+        // every pair of SMs one; else single-SM tiles of the chosen width.
+        const int64_t pair_tiles = ((L.m + 255) / 256) * ((L.n + 255) / 256);
+        if (L.block_n == 0 && pair_tiles >= num_sms / 2) return launch_gemm_mx2(L, p, st, num_sms);
+    }
     if (ue8m0 && L.path != 1) return launch_gemm_mx(L, p, bn, st, num_sms);
     if (L.out_f32) return dispatch_bn<true, true>(bn, L, p, st, num_sms);
     return dispatch_bn<false, false>(bn, L, p, st, num_sms);

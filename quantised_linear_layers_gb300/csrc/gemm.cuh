@@ -42,7 +42,8 @@ struct GemmLaunch {
     int64_t ldd;
     int accumulate;
     int block_n;              // 0 = heuristic, else 32/64/128/256
-    int path;                 // 0 = auto, 1 = CUDA-core promotion, 2 = block-scaled MMA (UE8M0 only)
+    int path;                 // 0 = auto, 1 = CUDA-core promotion, 2 = block-scaled MMA on one SM,
+                              // 3 = block-scaled MMA on CTA pairs (UE8M0 formats only)
     uint32_t* dev_status;
     uint64_t wait_limit_ns;
 };
@@ -50,6 +51,7 @@ struct GemmLaunch {
 int choose_block_n(int64_t m, int64_t n, int num_sms);
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms);
 cudaError_t launch_gemm_mx(const GemmLaunch& L, const GemmParams& p, int bn, cudaStream_t st, int num_sms);
+cudaError_t launch_gemm_mx2(const GemmLaunch& L, const GemmParams& p, cudaStream_t st, int num_sms);
 
 // 2-D uint8 tensor map [rows, cols] (cols contiguous, row stride ld bytes),
 // box [box_rows x 128 bytes], 128-byte swizzle, zero fill out of bounds.

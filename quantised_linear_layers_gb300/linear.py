@@ -38,7 +38,12 @@ class FP8Weight:
 
 
 def _cast_rows(x: torch.Tensor, fmt: int, mn_major: bool = True):
-    return ops.fp8_cast_per_token(x, 128, fmt, sf_mn_major=mn_major)
+    """Per-token cast into a buffer whose rows start on 16-byte boundaries (the
+    GEMM's operand loads need it; the rows' padding is never read)."""
+    m, n = x.shape
+    ld = -(-max(n, 1) // 16) * 16
+    out = torch.empty((m, ld), dtype=torch.float8_e4m3fn, device=x.device)[:, :n]
+    return ops.fp8_cast_per_token(x, 128, fmt, out=out, sf_mn_major=mn_major)
 
 
 def forward(x: torch.Tensor, w: FP8Weight, out: torch.Tensor | None = None) -> torch.Tensor:

@@ -209,7 +209,7 @@ def _pow2_grid(rows, cols, seed, lo=-2, hi=2):
     return torch.pow(2.0, torch.randint(lo, hi + 1, (rows, cols), generator=g).float())
 
 
-@pytest.mark.parametrize("path", [1, 2], ids=["promotion", "block_scaled"])
+@pytest.mark.parametrize("path", [1, 2, 3], ids=["promotion", "block_scaled", "pair"])
 @pytest.mark.parametrize("bn", [32, 64, 128, 256])
 @pytest.mark.parametrize("k", [1024, 1152, 256])
 @pytest.mark.parametrize("packed", [False, True])
@@ -245,7 +245,7 @@ def test_wgrad_exact_pow2_scales(orc, ops, path, bn, k, packed):
     assert bad.size == 0, f"{len(bad)} mismatches; first {bad[0]} got {got[tuple(bad[0])]} ref {ref[tuple(bad[0])]}"
 
 
-@pytest.mark.parametrize("path", [1, 2], ids=["promotion", "block_scaled"])
+@pytest.mark.parametrize("path", [1, 2, 3], ids=["promotion", "block_scaled", "pair"])
 @pytest.mark.parametrize("bn", [32, 64, 128, 256])
 def test_fwd_exact_pow2_block_scales(orc, ops, path, bn):
     """fwd form: 1x128 A scales and 128x128 B block scales, all powers of two,
@@ -276,6 +276,30 @@ def test_block_scaled_matches_promotion_random(orc, ops, fmt):
     finally:
         ops.set_gemm_path(0)
     d2 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    ops.set_gemm_path(3)
+    try:
+        d3 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    finally:
+        ops.set_gemm_path(0)
     ref = oracle_fwd(orc, xq, xs, wq, ws, fmt)
     check_gemm(d1.float().cpu().numpy(), ref, "promotion")
     check_gemm(d2.float().cpu().numpy(), ref, "block-scaled")
+    check_gemm(d3.float().cpu().numpy(), ref, "pair")
+
+
+@pytest.mark.parametrize("path", [2, 3], ids=["block_scaled", "pair"])
+def test_large_packed_sampled_rows(orc, ops, path):
+    """The large cast+GEMM workload with packed UE8M0 scales on the 1-SM and
+    CTA-pair block-scaled kernels, sampled rows and the ragged last rows."""
+    m, n, k = 16384, 18432, 7168
+    x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, 2, w_mul=0.02)
+    ops.set_gemm_path(path)
+    try:
+        d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 2)
+    finally:
+        ops.set_gemm_path(0)
+    assert ops.device_status() == 0
+    rows = np.sort(np.random.default_rng(5).choice(m, 10, replace=False))
+    rows[0], rows[-1] = 0, m - 1
+    ref = oracle_fwd(orc, xq, xs, wq, ws, 2, rows=rows)
+    check_gemm(d[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref)
