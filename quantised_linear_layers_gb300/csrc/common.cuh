@@ -211,6 +211,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_
         : "memory");
 }
 
+// Brings a tile into L2 ahead of its load (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* desc, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(desc), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Tiled load into this CTA's shared memory whose completion is signalled on
 // the barrier at `bar_cluster_addr`, which may be in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* desc, uint32_t bar_cluster_addr, int32_t x,

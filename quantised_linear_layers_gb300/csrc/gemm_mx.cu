@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int num_groups = (num_kb + 3) / 4;
 
     if (warp < 4) {
-        regs_dealloc<88>();   // 128 x 88 + 256 x 208 = 384 x 168 registers
+        regs_dealloc<104>();  // 128 x 104 + 256 x 200 = 384 x 168 registers
         if (warp == 0) {
             if (elect_one()) {
                 uint32_t it = 0;
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        regs_alloc<208>();
+        regs_alloc<200>();
         // ---------------- epilogue warpgroups ----------------
         constexpr int CPT = C::kColsPerThread;
         constexpr int U = CPT < 32 ? CPT : 32;
@@ -335,17 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t as = tc % C::kAccStages, aph = (tc / C::kAccStages) & 1u;
             if (!warp_wait(&tfull[as], aph, ctl)) break;
             tc_fence_after_sync();
-            float acc[CPT];
+            uint32_t accb[CPT];
             const uint32_t tcol = tmem_base + lane_base + as * BN + wg * CPT;
 #pragma unroll
             for (int c0 = 0; c0 < CPT; c0 += U) {
-                uint32_t v[U];
-                if constexpr (U == 16) tmem_ld_32x32b_x16(tcol + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
-                else tmem_ld_32x32b_x32(tcol + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
-                tmem_wait_ld(v);
-#pragma unroll
-                for (int j = 0; j < U; ++j) acc[c0 + j] = __uint_as_float(v[j]);
+                if constexpr (U == 16) tmem_ld_32x32b_x16(tcol + c0, *reinterpret_cast<uint32_t(*)[16]>(&accb[c0]));
+                else tmem_ld_32x32b_x32(tcol + c0, *reinterpret_cast<uint32_t(*)[32]>(&accb[c0]));
             }
+            tmem_wait_ld(accb);            // one wait for all loads
+            float* acc = reinterpret_cast<float*>(accb);
             tc_fence_before_sync();
             mbar_arrive(&tempty[as]);
             const int64_t row = static_cast<int64_t>(mb) * BM + r_local;

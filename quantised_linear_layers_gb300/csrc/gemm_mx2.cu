@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued = 0;                         // stages this CTA's producer issued
 
     if (warp < 4) {
-        regs_dealloc<88>();   // 128 x 88 + 256 x 208 = 384 x 168 registers
+        regs_dealloc<104>();  // 128 x 104 + 256 x 200 = 384 x 168 registers
         if (warp == 0) {
             // ---------------- TMA producer (both CTAs) ----------------
             if (elect_one()) {
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        regs_alloc<208>();
+        regs_alloc<200>();
         // ---------------- epilogue (both CTAs): 128 rows x 256 columns ----------------
         constexpr int CPT = BN / 2;
         const int wg = (warp - 4) >> 2;
@@ -339,16 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coords(t, p, mb, nb);
             if (!warp_wait(tfull, tc & 1u, ctl)) break;
             tc_fence_after_sync();
-            float acc[CPT];
+            uint32_t accb[CPT];
             const uint32_t tcol = tmem_base + lane_base + wg * CPT;
 #pragma unroll
-            for (int c0 = 0; c0 < CPT; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tcol + c0, v);
-                tmem_wait_ld(v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc[c0 + j] = __uint_as_float(v[j]);
-            }
+            for (int c0 = 0; c0 < CPT; c0 += 32)
+                tmem_ld_32x32b_x32(tcol + c0, *reinterpret_cast<uint32_t(*)[32]>(&accb[c0]));
+            tmem_wait_ld(accb);            // one wait for all four loads
+            float* acc = reinterpret_cast<float*>(accb);
             tc_fence_before_sync();
             if (leader) mbar_arrive(tempty);
             else mbar_arrive_remote(leader_tempty);
