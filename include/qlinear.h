@@ -208,6 +208,13 @@ ql_status ql_set_gemm_path(int path);
  * drains its own copies, frees its tensor memory and returns. Process-wide. */
 ql_status ql_set_wait_limit_ms(int ms);
 
+/* Test hook for the failure path (process-wide, default off): while enabled,
+ * the GEMM kernels' operand producer issues no copies, so the tensor-core
+ * issuer's bounded wait runs out; the kernel then records
+ * QL_ERR_DEVICE_TIMEOUT, frees its tensor memory and returns, leaving the
+ * context usable. The output is not written. */
+ql_status ql_test_stall_gemm_producer(int enable);
+
 /* Synchronises `stream`, then returns and clears the device status word:
  * QL_OK, or QL_ERR_DEVICE_TIMEOUT if any kernel's bounded wait ran out since
  * the last call; QL_ERR_CUDA if the synchronisation itself failed. */

@@ -22,6 +22,7 @@ __device__ uint32_t g_dev_status = 0;
 std::atomic<int> g_num_sms_override{0};
 std::atomic<int> g_block_n_override{0};
 std::atomic<int> g_gemm_path{0};
+std::atomic<int> g_stall_producer{0};
 std::atomic<int> g_wait_limit_ms{2000};
 
 struct DeviceInfo {
@@ -104,6 +105,7 @@ ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sa
     L.accumulate = accumulate ? 1 : 0;
     L.block_n = g_block_n_override.load();
     L.path = g_gemm_path.load();
+    L.stall_producer = g_stall_producer.load();
     L.dev_status = di.status;
     L.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ms.load()) * 1000000ull;
     return from_cuda(ql::launch_gemm(L, st, effective_sms(di)));
@@ -245,6 +247,11 @@ ql_status ql_set_gemm_block_n(int block_n) {
 ql_status ql_set_gemm_path(int path) {
     if (path < 0 || path > 3) return QL_ERR_INVALID_ARG;
     g_gemm_path.store(path);
+    return QL_OK;
+}
+
+ql_status ql_test_stall_gemm_producer(int enable) {
+    g_stall_producer.store(enable ? 1 : 0);
     return QL_OK;
 }
 

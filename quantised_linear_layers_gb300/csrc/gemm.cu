@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) {
                 uint32_t it = 0;
                 bool ok = true;
-                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int t = blockIdx.x; t < num_tiles && ok && !p.stall_producer; t += gridDim.x) {
                     int mb, nb;
                     tile_coords(t, p, mb, nb);
                     for (int kb = 0; kb < num_kb; ++kb, ++it) {
@@ -511,6 +511,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     p.group_m = 16;
     p.dev_status = L.dev_status;
     p.wait_limit_ns = L.wait_limit_ns;
+    p.stall_producer = L.stall_producer;
     const int64_t es = L.out_f32 ? 4 : 2;
     p.vec_store = ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && (L.ldd * es) % 16 == 0) ? 1 : 0;
     const int bn = L.block_n > 0 ? L.block_n : choose_block_n(L.m, L.n, num_sms);

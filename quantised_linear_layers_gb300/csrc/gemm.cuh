@@ -22,6 +22,7 @@ struct GemmParams {
     int vec_store;            // 16-byte output stores allowed
     uint32_t* dev_status;
     uint64_t wait_limit_ns;
+    int stall_producer;       // test hook: the producer issues no copies (waits time out)
 };
 
 // Host-side description of one GEMM call.
@@ -46,6 +47,7 @@ struct GemmLaunch {
                               // 3 = block-scaled MMA on CTA pairs (UE8M0 formats only)
     uint32_t* dev_status;
     uint64_t wait_limit_ns;
+    int stall_producer;
 };
 
 int choose_block_n(int64_t m, int64_t n, int num_sms);

@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) {
                 uint32_t it = 0;
                 bool ok = true;
-                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int t = blockIdx.x; t < num_tiles && ok && !p.stall_producer; t += gridDim.x) {
                     int mb, nb;
                     tile_coords(t, p, mb, nb);
                     for (int kb = 0; kb < num_kb; ++kb, ++it) {

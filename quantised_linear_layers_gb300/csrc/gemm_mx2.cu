@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t it = 0;
                 bool ok = true;
                 const uint32_t leader_full0 = mapa_shared(&full[0], 0);
-                for (int t = cid; t < num_tiles && ok; t += ncl) {
+                for (int t = cid; t < num_tiles && ok && !p.stall_producer; t += ncl) {
                     int mb, nb;
                     tile_coords(t, p, mb, nb);
                     const int a_row = mb * 2 * BM + static_cast<int>(rank) * BM;

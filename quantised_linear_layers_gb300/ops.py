@@ -38,6 +38,7 @@ _SIGS = {
     "ql_set_wait_limit_ms": [_int],
     "ql_set_gemm_block_n": [_int],
     "ql_set_gemm_path": [_int],
+    "ql_test_stall_gemm_producer": [_int],
     "ql_device_status": [_vp],
     "ql_status_string": [_int],
 }
@@ -224,6 +225,11 @@ def set_gemm_block_n(bn: int) -> None:
 def set_gemm_path(path: int) -> None:
     """0 auto, 1 CUDA-core promotion, 2 block-scaled MMA (UE8M0 formats)."""
     _check("ql_set_gemm_path", load_library().ql_set_gemm_path(int(path)))
+
+
+def test_stall_gemm_producer(enable: bool) -> None:
+    """Failure-path test hook: GEMM producers issue no copies while enabled."""
+    _check("ql_test_stall_gemm_producer", load_library().ql_test_stall_gemm_producer(int(bool(enable))))
 
 
 def set_wait_limit_ms(ms: int) -> None:
