@@ -61,21 +61,22 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
 
 // ---------------------------------------------------------------------------
 // Row-contiguous per-token cast (x_stride_n == 1, out_stride_n == 1).
-// One warp task = (row, chunk of 512 elements); each lane owns 16 consecutive
-// elements, so a group of G elements is G/16 consecutive lanes and its amax
-// is a shuffle reduction over them. 16 elements = 32 B (bf16) / 64 B (fp32)
-// of loads in flight per lane.
+// One warp task = (row, chunk of 32*E elements); each lane owns E consecutive
+// elements, E = 64 bytes of input (32 bf16 or 16 fp32: four 16-byte loads, all
+// issued before use), so a group of G elements is G/E consecutive lanes and its
+// amax is a shuffle reduction over them (none for bf16 with G = 32).
 // ---------------------------------------------------------------------------
 template <typename T, int GRAN, int FMT, bool RECIP>
 __global__ void __launch_bounds__(256) cast_rows_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx,
                                                         uint8_t* __restrict__ out, int64_t ldo,
                                                         void* __restrict__ sf, int64_t ssm, int64_t ssg,
                                                         int64_t chunks_per_row, int vec_in, int vec_out) {
-    constexpr int kElemsPerLane = 16;
-    constexpr int kChunk = 32 * kElemsPerLane;            // 512
-    constexpr int kLanesPerGroup = GRAN / kElemsPerLane;  // 2 or 8
-    constexpr int kVec = 16 / sizeof(T);                  // elements per 16-byte load
-    constexpr int kLoads = kElemsPerLane / kVec;          // 2 (bf16) or 4 (fp32)
+    constexpr int kElemsPerLane = 64 / sizeof(T);          // 32 (bf16) or 16 (fp32)
+    constexpr int kChunk = 32 * kElemsPerLane;
+    constexpr int kLanesPerGroup = GRAN / kElemsPerLane;   // 1, 2, 4 or 8
+    constexpr int kVec = 16 / sizeof(T);                   // elements per 16-byte load
+    constexpr int kLoads = kElemsPerLane / kVec;           // 4
+    static_assert(kLanesPerGroup >= 1, "a lane's elements lie in one group");
 
     const int lane = threadIdx.x & 31;
     const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -89,19 +90,25 @@ __global__ void __launch_bounds__(256) cast_rows_kernel(const T* __restrict__ x,
         const int64_t e0 = chunk * kChunk + static_cast<int64_t>(lane) * kElemsPerLane;
         const T* xr = x + row * ldx;
 
-        float v[kElemsPerLane];
+        uint4 raw[kLoads];
 #pragma unroll
         for (int l = 0; l < kLoads; ++l) {
             const int64_t e = e0 + l * kVec;
             if (vec_in && e + kVec <= n) {
-                const uint4 u = __ldg(reinterpret_cast<const uint4*>(xr + e));
-                const T* t = reinterpret_cast<const T*>(&u);
-#pragma unroll
-                for (int i = 0; i < kVec; ++i) v[l * kVec + i] = to_f32(t[i]);
+                raw[l] = __ldg(reinterpret_cast<const uint4*>(xr + e));
             } else {
+                T tmp[kVec];
 #pragma unroll
-                for (int i = 0; i < kVec; ++i) v[l * kVec + i] = (e + i < n) ? to_f32(xr[e + i]) : 0.0f;
+                for (int i = 0; i < kVec; ++i) tmp[i] = (e + i < n) ? xr[e + i] : T(0.0f);
+                raw[l] = *reinterpret_cast<const uint4*>(tmp);
             }
+        }
+        float v[kElemsPerLane];
+#pragma unroll
+        for (int l = 0; l < kLoads; ++l) {
+            const T* t = reinterpret_cast<const T*>(&raw[l]);
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) v[l * kVec + i] = to_f32(t[i]);
         }
         float amax = 0.0f;
 #pragma unroll
@@ -115,11 +122,13 @@ __global__ void __launch_bounds__(256) cast_rows_kernel(const T* __restrict__ x,
 
         if (e0 < n) {
             uint8_t* orow = out + row * ldo;
-            uint32_t w[4];
+            uint32_t w[kElemsPerLane / 4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) w[q] = quant4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], f);
+            for (int q = 0; q < kElemsPerLane / 4; ++q) w[q] = quant4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], f);
             if (vec_out && e0 + kElemsPerLane <= n) {
-                *reinterpret_cast<uint4*>(orow + e0) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+                for (int q = 0; q < kElemsPerLane / 16; ++q)
+                    *reinterpret_cast<uint4*>(orow + e0 + 16 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             } else {
 #pragma unroll
                 for (int i = 0; i < kElemsPerLane; ++i)
@@ -132,7 +141,7 @@ __global__ void __launch_bounds__(256) cast_rows_kernel(const T* __restrict__ x,
             if ((lane % kLanesPerGroup) == 0 && g < G) static_cast<float*>(sf)[row * ssm + g * ssg] = s;
         } else {
             // four consecutive groups per int32 word; groups past the last are 0
-            constexpr int kWordLanes = 4 * kLanesPerGroup;  // 8 or 32
+            constexpr int kWordLanes = 4 * kLanesPerGroup;  // 4 .. 32
             const uint32_t mine = (g < G) ? ebyte : 0u;
             const int base = (lane / kWordLanes) * kWordLanes;
             uint32_t word = 0;
@@ -451,7 +460,7 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
     if (a.sxn == 1 && a.son == 1) {
         const int vec_in = aligned16(x) && ((a.sxm * static_cast<int64_t>(sizeof(T))) % 16 == 0);
         const int vec_out = aligned16(a.out) && (a.som % 16 == 0);
-        const int64_t chunks = (a.n + 511) / 512;
+        const int64_t chunks = (a.n + 32 * (64 / sizeof(T)) - 1) / (32 * (64 / sizeof(T)));
         const int64_t warps = a.m * chunks;
         int64_t blocks = (warps + 7) / 8;
         const int64_t cap = static_cast<int64_t>(num_sms) * 8 * 4;   // enough warps for full-rate HBM
