@@ -159,6 +159,11 @@ ql_status fp8_cast_per_token(const void* x, ql_dtype x_dtype, int64_t m, int64_t
     a.sf = out_sf;
     a.ssm = sf_stride_m;
     a.ssg = sf_stride_g;
+    const int64_t es = x_dtype == QL_BF16 ? 2 : 4;
+    a.tma_ok = aligned16(x) && x_stride_n > 0 && (x_stride_n * es) % 16 == 0 && x_stride_n * es < (int64_t(1) << 40) &&
+               m < (int64_t(1) << 31) && n < (int64_t(1) << 31);
+    a.dev_status = di.status;
+    a.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ms.load()) * 1000000ull;
     return from_cuda(ql::launch_cast_per_token(a, reinterpret_cast<cudaStream_t>(stream), di.num_sms));
 }
 

@@ -19,6 +19,8 @@
 #include <stdint.h>
 
 #include "cast.cuh"
+#include "common.cuh"
+#include "gemm.cuh"
 
 namespace ql {
 namespace {
@@ -67,7 +69,7 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
 // amax is a shuffle reduction over them (none for bf16 with G = 32).
 // ---------------------------------------------------------------------------
 template <typename T, int GRAN, int FMT, bool RECIP>
-__global__ void __launch_bounds__(256) cast_rows_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx,
+__global__ void __launch_bounds__(256, 4) cast_rows_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx,
                                                         uint8_t* __restrict__ out, int64_t ldo,
                                                         void* __restrict__ sf, int64_t ssm, int64_t ssg,
                                                         int64_t chunks_per_row, int vec_in, int vec_out) {
@@ -97,22 +99,31 @@ __global__ void __launch_bounds__(256) cast_rows_kernel(const T* __restrict__ x,
             if (vec_in && e + kVec <= n) {
                 raw[l] = __ldg(reinterpret_cast<const uint4*>(xr + e));
             } else {
-                T tmp[kVec];
+                union { uint4 u; T t[kVec]; } tmp;
 #pragma unroll
-                for (int i = 0; i < kVec; ++i) tmp[i] = (e + i < n) ? xr[e + i] : T(0.0f);
-                raw[l] = *reinterpret_cast<const uint4*>(tmp);
+                for (int i = 0; i < kVec; ++i) tmp.t[i] = (e + i < n) ? xr[e + i] : T(0.0f);
+                raw[l] = tmp.u;
             }
         }
-        float v[kElemsPerLane];
-#pragma unroll
-        for (int l = 0; l < kLoads; ++l) {
-            const T* t = reinterpret_cast<const T*>(&raw[l]);
-#pragma unroll
-            for (int i = 0; i < kVec; ++i) v[l * kVec + i] = to_f32(t[i]);
-        }
+        // |x| max (exact in the input type): packed bf16x2 or scalar fp32
         float amax = 0.0f;
+        if constexpr (sizeof(T) == 2) {
+            __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
 #pragma unroll
-        for (int i = 0; i < kElemsPerLane; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            for (int l = 0; l < kLoads; ++l) {
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[l]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) m2 = __hmax2(m2, __habs2(h[i]));
+            }
+            amax = fmaxf(__bfloat162float(m2.x), __bfloat162float(m2.y));
+        } else {
+#pragma unroll
+            for (int l = 0; l < kLoads; ++l) {
+                const float* t = reinterpret_cast<const float*>(&raw[l]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(t[i]));
+            }
+        }
 #pragma unroll
         for (int off = 1; off < kLanesPerGroup; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
 
@@ -124,7 +135,10 @@ __global__ void __launch_bounds__(256) cast_rows_kernel(const T* __restrict__ x,
             uint8_t* orow = out + row * ldo;
             uint32_t w[kElemsPerLane / 4];
 #pragma unroll
-            for (int q = 0; q < kElemsPerLane / 4; ++q) w[q] = quant4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], f);
+            for (int q = 0; q < kElemsPerLane / 4; ++q) {
+                const T* t = reinterpret_cast<const T*>(&raw[0]) + 4 * q;
+                w[q] = quant4(to_f32(t[0]), to_f32(t[1]), to_f32(t[2]), to_f32(t[3]), f);
+            }
             if (vec_out && e0 + kElemsPerLane <= n) {
 #pragma unroll
                 for (int q = 0; q < kElemsPerLane / 16; ++q)
@@ -156,105 +170,285 @@ __global__ void __launch_bounds__(256) cast_rows_kernel(const T* __restrict__ x,
 
 // ---------------------------------------------------------------------------
 // Transposed per-token cast (x_stride_m == 1): logical row i is a column of the
-// physical array P[j][i] = x[i + j*ldx]. A CTA stages a TJ x 32 tile of P in
-// shared memory (coalesced 32-wide loads along i), reduces each logical row's
-// groups down the tile's columns, then writes each logical row's TJ bytes
-// contiguously (16 B per thread).
-// TJ = 128, or 4*GRAN for packed UE8M0 (so a CTA owns whole int32 words).
+// physical array P[j][i] = x[i + j*ldx], and its groups run along j.
+// A warp owns 4V consecutive i (V = elements per 16-byte load) and walks kSub
+// subtiles of 128 consecutive j. In a subtile, lane (jr = lane/4, ic = lane%4)
+// loads rows j + 16*jr + l, l < 16, at columns i0 .. i0+V: 16 independent
+// 16-byte loads per lane. For each of its V logical rows a lane then holds 16
+// consecutive j, so a group's amax is a shuffle over the lanes of the same ic
+// (three steps for 128-wide groups, one for 32), and the lane writes its 16
+// output bytes with one 16-byte store (eight lanes fill 128 contiguous bytes of
+// an output row). The 8 warps of a CTA sit side by side along i, so the CTA
+// reads 8 x 64 contiguous bytes of every physical row it touches. Packed
+// 128-wide groups take kSub = 4 subtiles per warp so that the warp itself owns
+// whole int32 words.
 // ---------------------------------------------------------------------------
-template <typename T, int GRAN, int FMT, bool RECIP, int TJ>
-__global__ void __launch_bounds__(256) cast_cols_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx,
-                                                        uint8_t* __restrict__ out, int64_t ldo,
-                                                        void* __restrict__ sf, int64_t ssm, int64_t ssg,
-                                                        int vec_out) {
-    constexpr int TI = 32;
-    constexpr int kGroups = TJ / GRAN;
-    constexpr int kParts = TJ / 16;          // 16-row partial reductions per column
-    extern __shared__ float smem_cast[];
-    float* tile = smem_cast;                 // [TJ][TI + 1]
-    float* part = tile + TJ * (TI + 1);      // [kParts][TI]
-    float* fac = part + kParts * TI;         // [kGroups][TI]
-    uint32_t* ebuf = reinterpret_cast<uint32_t*>(fac + kGroups * TI);  // [kGroups][TI]
+template <typename T, int GRAN, int FMT, bool RECIP>
+__global__ void __launch_bounds__(256, 1) cast_cols_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx,
+                                                           uint8_t* __restrict__ out, int64_t ldo,
+                                                           void* __restrict__ sf, int64_t ssm, int64_t ssg,
+                                                           int vec_in, int vec_out) {
+    constexpr int V = 16 / sizeof(T);          // 8 (bf16) or 4 (fp32)
+    constexpr int WI = 4 * V;                  // logical rows per warp
+    constexpr int WJ = 128;                    // group-axis extent of a subtile
+    constexpr int kSub = (FMT == kSfPacked && GRAN == 128) ? 4 : 1;
+    constexpr int kLaneSpan = GRAN / 16;       // lanes (along jr) per group: 2 or 8
 
-    const int tid = threadIdx.x;
-    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * TI;
-    const int64_t j0 = static_cast<int64_t>(blockIdx.y) * TJ;
-
-    // load: warp w reads physical rows w, w+8, ...; lane = column i
-    {
-        const int li = tid & 31;
-        const int64_t i = i0 + li;
-        for (int lj = tid >> 5; lj < TJ; lj += 8) {
-            const int64_t j = j0 + lj;
-            float val = 0.0f;
-            if (i < m && j < n) val = to_f32(x[j * ldx + i]);
-            tile[lj * (TI + 1) + li] = val;
-        }
-    }
-    __syncthreads();
-    // partial amax over 16 rows: thread (p, i)
-    for (int t = tid; t < kParts * TI; t += 256) {
-        const int p = t / TI, li = t % TI;
-        float a = 0.0f;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) a = fmaxf(a, fabsf(tile[(p * 16 + r) * (TI + 1) + li]));
-        part[p * TI + li] = a;
-    }
-    __syncthreads();
-    // per (group, i): scale, factor; scale store
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int jr = lane >> 2, ic = lane & 3;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * (8 * WI) + warp * WI + ic * V;   // lane's first column
+    const int64_t jw = static_cast<int64_t>(blockIdx.y) * (kSub * WJ);                     // warp's first row
     const int64_t Gtot = (n + GRAN - 1) / GRAN;
-    for (int t = tid; t < kGroups * TI; t += 256) {
-        const int gl = t / TI, li = t % TI;
-        float a = 0.0f;
+    const bool full_cols = vec_in && i0 + V <= m;
+    const bool leader = (jr % kLaneSpan) == 0;  // first lane of a group (per ic)
+
+    uint32_t ebytes[V];                         // packed 128-groups: byte k of each word
 #pragma unroll
-        for (int p = 0; p < GRAN / 16; ++p) a = fmaxf(a, part[(gl * (GRAN / 16) + p) * TI + li]);
-        float s, f;
-        uint32_t ebyte;
-        group_scale<FMT, RECIP>(a, s, f, ebyte);
-        fac[gl * TI + li] = f;
-        const int64_t i = i0 + li;
-        const int64_t g = j0 / GRAN + gl;
-        if constexpr (FMT != kSfPacked) {
-            if (i < m && g < Gtot) static_cast<float*>(sf)[i * ssm + g * ssg] = s;
-        } else {
-            ebuf[gl * TI + li] = (g < Gtot) ? ebyte : 0u;
+    for (int c = 0; c < V; ++c) ebytes[c] = 0;
+
+    for (int sub = 0; sub < kSub; ++sub) {
+        const int64_t j0 = jw + sub * WJ + jr * 16;                          // lane's first row
+        uint4 raw[16];
+#pragma unroll
+        for (int l = 0; l < 16; ++l) {
+            const int64_t j = j0 + l;
+            if (j < n && full_cols) {
+                raw[l] = __ldg(reinterpret_cast<const uint4*>(x + j * ldx + i0));
+            } else {
+                union { uint4 u; T t[V]; } tmp;
+#pragma unroll
+                for (int c = 0; c < V; ++c) tmp.t[c] = (j < n && i0 + c < m) ? x[j * ldx + i0 + c] : T(0.0f);
+                raw[l] = tmp.u;
+            }
+        }
+        float amax[V];
+#pragma unroll
+        for (int c = 0; c < V; ++c) amax[c] = 0.0f;
+#pragma unroll
+        for (int l = 0; l < 16; ++l) {
+            const T* t = reinterpret_cast<const T*>(&raw[l]);
+#pragma unroll
+            for (int c = 0; c < V; ++c) amax[c] = fmaxf(amax[c], fabsf(to_f32(t[c])));
+        }
+#pragma unroll
+        for (int c = 0; c < V; ++c)
+#pragma unroll
+            for (int off = 4; off < 4 * kLaneSpan; off <<= 1)
+                amax[c] = fmaxf(amax[c], __shfl_xor_sync(0xffffffffu, amax[c], off));
+
+        const int64_t g = j0 / GRAN;             // this lane's group along j
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+            float s, f;
+            uint32_t ebyte;
+            group_scale<FMT, RECIP>(amax[c], s, f, ebyte);
+            const int64_t i = i0 + c;
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const T* t0 = reinterpret_cast<const T*>(&raw[4 * q]);
+                const T* t1 = reinterpret_cast<const T*>(&raw[4 * q + 1]);
+                const T* t2 = reinterpret_cast<const T*>(&raw[4 * q + 2]);
+                const T* t3 = reinterpret_cast<const T*>(&raw[4 * q + 3]);
+                w[q] = quant4(to_f32(t0[c]), to_f32(t1[c]), to_f32(t2[c]), to_f32(t3[c]), f);
+            }
+            if (i < m && j0 < n) {
+                uint8_t* orow = out + i * ldo;
+                if (vec_out && j0 + 16 <= n) {
+                    *reinterpret_cast<uint4*>(orow + j0) = make_uint4(w[0], w[1], w[2], w[3]);
+                } else {
+                    for (int e = 0; e < 16; ++e)
+                        if (j0 + e < n) orow[j0 + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+                }
+            }
+            if constexpr (FMT != kSfPacked) {
+                if (leader && i < m && g < Gtot) static_cast<float*>(sf)[i * ssm + g * ssg] = s;
+            } else if constexpr (GRAN == 32) {
+                // the subtile's 128 rows are one word: groups of lanes jr = 0, 2, 4, 6
+                const uint32_t mine = (g < Gtot) ? ebyte : 0u;
+                uint32_t word = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) word |= __shfl_sync(0xffffffffu, mine, ic + 8 * k) << (8 * k);
+                const int64_t g0 = (jw + sub * WJ) / GRAN;
+                if (jr == 0 && i < m && g0 < Gtot)
+                    static_cast<int32_t*>(sf)[i * ssm + (g0 / 4) * ssg] = static_cast<int32_t>(word);
+            } else {
+                ebytes[c] |= ((g < Gtot) ? ebyte : 0u) << (8 * sub);
+            }
+        }
+    }
+    if constexpr (FMT == kSfPacked && GRAN == 128) {
+        const int64_t g0 = jw / GRAN;            // four groups: one word
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+            const int64_t i = i0 + c;
+            if (jr == 0 && i < m && g0 < Gtot)
+                static_cast<int32_t*>(sf)[i * ssm + (g0 / 4) * ssg] = static_cast<int32_t>(ebytes[c]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMA-staged transposed per-token cast (x_stride_m == 1, 16-byte-aligned
+// rows). The physical array P[j][i] is read in boxes of 128 rows (j) x 128
+// bytes (BI = 64 bf16 or 32 fp32 values of i) by one producer thread into a
+// 4-stage shared-memory ring; two consumer warps each take 4V of the box's
+// columns with the lane mapping of the register kernel below (lane jr, ic:
+// rows 16*jr .. +16, columns V*ic .. +V), quantise, and store 16 bytes per
+// logical row. A CTA walks a unit of four consecutive boxes along j of one
+// column strip, so for packed 128-wide groups each lane owns whole words.
+// Every wait is bounded; on a time-out the CTA records it and drains.
+// ---------------------------------------------------------------------------
+namespace cols_tma {
+constexpr int kStages = 4;
+constexpr int kRows = 128;                 // j per box
+constexpr int kBoxBytes = kRows * 128;     // 16 KB
+constexpr int kUnit = 4;                   // boxes per unit (512 rows)
+constexpr int kThreads = 96;               // producer warp + 2 consumer warps
+}  // namespace cols_tma
+
+template <typename T, int GRAN, int FMT, bool RECIP>
+__global__ void __launch_bounds__(96) cast_cols_tma_kernel(const __grid_constant__ CUtensorMap tmap, int64_t m,
+                                                          int64_t n, uint8_t* __restrict__ out, int64_t ldo,
+                                                          void* __restrict__ sf, int64_t ssm, int64_t ssg,
+                                                          int vec_out, uint32_t* dev_status, uint64_t limit_ns) {
+    using namespace cols_tma;
+    constexpr int V = 16 / sizeof(T);
+    constexpr int BI = 128 / sizeof(T);        // columns per box
+    constexpr int kLaneSpan = GRAN / 16;       // lanes (along jr) per group
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kStages * kBoxBytes);
+    uint64_t* empty = full + kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t strips = (m + BI - 1) / BI;
+    const int64_t jblocks = (n + kUnit * kRows - 1) / (kUnit * kRows);
+    const int64_t units = strips * jblocks;
+    const int64_t Gtot = (n + GRAN - 1) / GRAN;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 2); }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const WaitCtl ctl{abort_flag, dev_status, limit_ns};
+
+    if (warp == 0) {
+        // ---- producer ----
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const int64_t strip = u % strips, jb = u / strips;
+                for (int b = 0; b < kUnit; ++b, ++it) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                    if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[s], kBoxBytes);
+                    tma_load_2d(ring + s * kBoxBytes, &tmap, &full[s], static_cast<int32_t>(strip * BI),
+                                static_cast<int32_t>((jb * kUnit + b) * kRows));
+                }
+            }
+            if (!ok) {
+                const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+                for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % kStages], (j / kStages) & 1u, limit_ns);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- consumers: warp c takes columns [c*4V, c*4V + 4V) of each box ----
+        const int cw = warp - 1;
+        const int jr = lane >> 2, ic = lane & 3;
+        const bool leader = (jr % kLaneSpan) == 0;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int64_t strip = u % strips, jb = u / strips;
+            const int64_t i0 = strip * BI + cw * 4 * V + ic * V;
+            uint32_t words[V];
+#pragma unroll
+            for (int c = 0; c < V; ++c) words[c] = 0;
+            for (int b = 0; b < kUnit; ++b, ++it) {
+                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, ctl))) { ok = false; break; }
+                const uint8_t* box = ring + s * kBoxBytes;
+                uint4 raw[16];
+#pragma unroll
+                for (int l = 0; l < 16; ++l)
+                    raw[l] = *reinterpret_cast<const uint4*>(box + (jr * 16 + l) * 128 + (cw * 4 * V + ic * V) * sizeof(T));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                const int64_t j0 = (jb * kUnit + b) * kRows + jr * 16;
+                float amax[V];
+#pragma unroll
+                for (int c = 0; c < V; ++c) amax[c] = 0.0f;
+#pragma unroll
+                for (int l = 0; l < 16; ++l) {
+                    const T* t = reinterpret_cast<const T*>(&raw[l]);
+#pragma unroll
+                    for (int c = 0; c < V; ++c) amax[c] = fmaxf(amax[c], fabsf(to_f32(t[c])));
+                }
+#pragma unroll
+                for (int c = 0; c < V; ++c)
+#pragma unroll
+                    for (int off = 4; off < 4 * kLaneSpan; off <<= 1)
+                        amax[c] = fmaxf(amax[c], __shfl_xor_sync(0xffffffffu, amax[c], off));
+                const int64_t g = j0 / GRAN;
+#pragma unroll
+                for (int c = 0; c < V; ++c) {
+                    float sc, f;
+                    uint32_t ebyte;
+                    group_scale<FMT, RECIP>(amax[c], sc, f, ebyte);
+                    const int64_t i = i0 + c;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const T* t0 = reinterpret_cast<const T*>(&raw[4 * q]);
+                        const T* t1 = reinterpret_cast<const T*>(&raw[4 * q + 1]);
+                        const T* t2 = reinterpret_cast<const T*>(&raw[4 * q + 2]);
+                        const T* t3 = reinterpret_cast<const T*>(&raw[4 * q + 3]);
+                        w[q] = quant4(to_f32(t0[c]), to_f32(t1[c]), to_f32(t2[c]), to_f32(t3[c]), f);
+                    }
+                    if (i < m && j0 < n) {
+                        uint8_t* orow = out + i * ldo;
+                        if (vec_out && j0 + 16 <= n) {
+                            *reinterpret_cast<uint4*>(orow + j0) = make_uint4(w[0], w[1], w[2], w[3]);
+                        } else {
+                            for (int e = 0; e < 16; ++e)
+                                if (j0 + e < n) orow[j0 + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+                        }
+                    }
+                    if constexpr (FMT != kSfPacked) {
+                        if (leader && i < m && g < Gtot) static_cast<float*>(sf)[i * ssm + g * ssg] = sc;
+                    } else if constexpr (GRAN == 32) {
+                        const uint32_t mine = (g < Gtot) ? ebyte : 0u;
+                        uint32_t word = 0;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) word |= __shfl_sync(0xffffffffu, mine, ic + 8 * k) << (8 * k);
+                        const int64_t g0 = (jb * kUnit + b) * kRows / GRAN;
+                        if (jr == 0 && i < m && g0 < Gtot)
+                            static_cast<int32_t*>(sf)[i * ssm + (g0 / 4) * ssg] = static_cast<int32_t>(word);
+                    } else {
+                        words[c] |= ((g < Gtot) ? ebyte : 0u) << (8 * b);
+                    }
+                }
+            }
+            if constexpr (FMT == kSfPacked && GRAN == 128) {
+                if (ok) {
+                    const int64_t g0 = jb * kUnit;
+#pragma unroll
+                    for (int c = 0; c < V; ++c) {
+                        const int64_t i = i0 + c;
+                        if (jr == 0 && i < m && g0 < Gtot)
+                            static_cast<int32_t*>(sf)[i * ssm + (g0 / 4) * ssg] = static_cast<int32_t>(words[c]);
+                    }
+                }
+            }
         }
     }
     __syncthreads();
-    if constexpr (FMT == kSfPacked) {
-        // kGroups is a multiple of 4: one word per 4 groups per column
-        for (int t = tid; t < (kGroups / 4) * TI; t += 256) {
-            const int wl = t / TI, li = t % TI;
-            const int64_t i = i0 + li;
-            const int64_t g = j0 / GRAN + wl * 4;
-            uint32_t word = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) word |= ebuf[(wl * 4 + q) * TI + li] << (8 * q);
-            if (i < m && g < Gtot) static_cast<int32_t*>(sf)[i * ssm + (g / 4) * ssg] = static_cast<int32_t>(word);
-        }
-    }
-    // quantise + store: thread -> (i, 16-element segment of j)
-    constexpr int kSegs = TJ / 16;
-    for (int t = tid; t < TI * kSegs; t += 256) {
-        const int li = t / kSegs, seg = t % kSegs;
-        const int64_t i = i0 + li;
-        const int64_t jb = j0 + seg * 16;
-        if (i >= m || jb >= n) continue;
-        const float f = fac[(seg * 16 / GRAN) * TI + li];
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float* c = tile + (seg * 16 + 4 * q) * (TI + 1) + li;
-            w[q] = quant4(c[0], c[TI + 1], c[2 * (TI + 1)], c[3 * (TI + 1)], f);
-        }
-        uint8_t* orow = out + i * ldo;
-        if (vec_out && jb + 16 <= n) {
-            *reinterpret_cast<uint4*>(orow + jb) = make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-            for (int e = 0; e < 16; ++e)
-                if (jb + e < n) orow[jb + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -469,17 +663,38 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
             x, a.m, a.n, a.sxm, a.out, a.som, a.sf, a.ssm, a.ssg, chunks, vec_in, vec_out);
         return cudaGetLastError();
     }
-    if (a.sxm == 1 && a.son == 1) {
-        constexpr int TJ = (FMT == kSfPacked) ? ((4 * GRAN > 128) ? 4 * GRAN : 128) : 128;
-        const size_t smem = (static_cast<size_t>(TJ) * 33 + (TJ / 16) * 32 + 2 * (TJ / GRAN) * 32) * sizeof(float);
-        auto kern = cast_cols_kernel<T, GRAN, FMT, RECIP, TJ>;
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-            if (e != cudaSuccess) return e;
+    if (a.sxm == 1 && a.son == 1 && a.tma_ok) {
+        using namespace cols_tma;
+        constexpr int BI = 128 / sizeof(T);
+        CUtensorMap tmap;
+        if (encode_2d_map(&tmap, x, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          a.n, a.m, a.sxn * static_cast<int64_t>(sizeof(T)), kRows, BI)) {
+            const int vec_out = aligned16(a.out) && (a.som % 16 == 0);
+            const int smem = kStages * kBoxBytes + 2 * kStages * 8 + 16 + 1024;
+            auto kern = cast_cols_tma_kernel<T, GRAN, FMT, RECIP>;
+            static bool attr = false;
+            if (!attr) {
+                cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                if (e != cudaSuccess) return e;
+                attr = true;
+            }
+            const int64_t units = ((a.m + BI - 1) / BI) * ((a.n + kUnit * kRows - 1) / (kUnit * kRows));
+            int64_t grid = static_cast<int64_t>(num_sms) * 3;
+            if (grid > units) grid = units;
+            kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tmap, a.m, a.n, a.out, a.som, a.sf, a.ssm, a.ssg,
+                                                                    vec_out, a.dev_status, a.wait_limit_ns);
+            return cudaGetLastError();
         }
+    }
+    if (a.sxm == 1 && a.son == 1) {
+        constexpr int V = 16 / sizeof(T);
+        const int vec_in = aligned16(x) && ((a.sxn * static_cast<int64_t>(sizeof(T))) % 16 == 0);
         const int vec_out = aligned16(a.out) && (a.som % 16 == 0);
-        dim3 grid(static_cast<unsigned>((a.m + 31) / 32), static_cast<unsigned>((a.n + TJ - 1) / TJ));
-        kern<<<grid, 256, smem, st>>>(x, a.m, a.n, a.sxn, a.out, a.som, a.sf, a.ssm, a.ssg, vec_out);
+        constexpr int kRowsPerCta = (FMT == kSfPacked && GRAN == 128) ? 512 : 128;
+        dim3 grid(static_cast<unsigned>((a.m + 32 * V - 1) / (32 * V)),
+                  static_cast<unsigned>((a.n + kRowsPerCta - 1) / kRowsPerCta));
+        cast_cols_kernel<T, GRAN, FMT, RECIP><<<grid, 256, 0, st>>>(x, a.m, a.n, a.sxn, a.out, a.som, a.sf, a.ssm,
+                                                                     a.ssg, vec_in, vec_out);
         return cudaGetLastError();
     }
     const int64_t G = (a.n + GRAN - 1) / GRAN;

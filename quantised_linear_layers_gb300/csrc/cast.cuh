@@ -16,6 +16,9 @@ struct CastTokenArgs {
     int64_t som, son;
     void* sf;
     int64_t ssm, ssg;
+    bool tma_ok;            // the transposed view may be read with TMA
+    uint32_t* dev_status;   // time-out flags of the TMA-staged kernel
+    uint64_t wait_limit_ns;
 };
 
 struct CastBlockArgs {

@@ -59,4 +59,9 @@ cudaError_t launch_gemm_mx2(const GemmLaunch& L, const GemmParams& p, cudaStream
 // box [box_rows x 128 bytes], 128-byte swizzle, zero fill out of bounds.
 bool encode_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows);
 
+// 2-D tensor map of `rows` rows of `cols` elements (row stride in bytes), box
+// [box_rows x box_cols] elements, no swizzle, zero fill out of bounds.
+bool encode_2d_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int64_t rows, int64_t cols,
+                   int64_t row_stride_bytes, int box_rows, int box_cols);
+
 }  // namespace ql
