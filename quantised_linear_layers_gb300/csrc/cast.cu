@@ -500,8 +500,13 @@ __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x
                                                          uint8_t* __restrict__ out, int64_t som, int64_t son,
                                                          int out_mode, void* __restrict__ sf, int64_t ssr,
                                                          int64_t ssc) {
-    constexpr int B = 128, kPad = 16;
-    __shared__ __align__(16) uint8_t q[B][B + kPad];
+    constexpr int B = 128;
+    // E4M3 bytes of the block, [row][col] with a row pitch of 144 bytes (16-byte
+    // rows: 8-byte stores, 16-byte loads) for row-contiguous input, or 129 bytes
+    // for column-contiguous input, whose per-lane byte stores go down a column
+    // (an odd pitch puts rows 8 apart in distinct banks).
+    __shared__ __align__(16) uint8_t qbuf[B * 144];
+    const int pitch = (in_mode == 1) ? 129 : 144;
     __shared__ float red[8];
     const int tid = threadIdx.x;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * B;
@@ -591,16 +596,16 @@ __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x
     for (int it = 0; it < 8; ++it) {
         const int bb = it * 16 + tid / 16;
         const int a0 = (tid % 16) * 8;
+        const uint32_t lo = quant4(v[it * 8], v[it * 8 + 1], v[it * 8 + 2], v[it * 8 + 3], f);
+        const uint32_t hi = quant4(v[it * 8 + 4], v[it * 8 + 5], v[it * 8 + 6], v[it * 8 + 7], f);
+        if (in_mode == 1) {
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const uint32_t w2 = e4m3x2(__fmul_rn(v[it * 8 + e], f), __fmul_rn(v[it * 8 + e + 1], f));
-            if (in_mode == 1) {
-                q[a0 + e][bb] = static_cast<uint8_t>(w2);
-                q[a0 + e + 1][bb] = static_cast<uint8_t>(w2 >> 8);
-            } else {
-                q[bb][a0 + e] = static_cast<uint8_t>(w2);
-                q[bb][a0 + e + 1] = static_cast<uint8_t>(w2 >> 8);
+            for (int e = 0; e < 4; ++e) {
+                qbuf[(a0 + e) * pitch + bb] = static_cast<uint8_t>(lo >> (8 * e));
+                qbuf[(a0 + 4 + e) * pitch + bb] = static_cast<uint8_t>(hi >> (8 * e));
             }
+        } else {
+            *reinterpret_cast<uint2*>(&qbuf[bb * pitch + a0]) = make_uint2(lo, hi);
         }
     }
     __syncthreads();
@@ -613,11 +618,23 @@ __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x
             const int64_t gr = r0 + line, gc = c0 + off;
             if (gr >= m) continue;
             uint8_t* o = out + gr * som + gc;
-            if (gc + 16 <= n) {
-                *reinterpret_cast<uint4*>(o) = *reinterpret_cast<const uint4*>(&q[line][off]);
+            uint4 u;
+            if (pitch == 144) {
+                u = *reinterpret_cast<const uint4*>(&qbuf[line * pitch + off]);
             } else {
+                uint32_t* uw = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint8_t* b = &qbuf[line * pitch + off + 4 * e];
+                    uw[e] = b[0] | (b[1] << 8) | (b[2] << 16) | (static_cast<uint32_t>(b[3]) << 24);
+                }
+            }
+            if (gc + 16 <= n) {
+                *reinterpret_cast<uint4*>(o) = u;
+            } else {
+                const uint8_t* ub = reinterpret_cast<const uint8_t*>(&u);
                 for (int e = 0; e < 16; ++e)
-                    if (gc + e < n) o[e] = q[line][off + e];
+                    if (gc + e < n) o[e] = ub[e];
             }
         } else if (out_mode == 1) {
             const int64_t gc = c0 + line, gr = r0 + off;
@@ -625,7 +642,7 @@ __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x
             uint8_t* o = out + gr + gc * son;
             uint8_t b16[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) b16[e] = q[off + e][line];
+            for (int e = 0; e < 16; ++e) b16[e] = qbuf[(off + e) * pitch + line];
             if (gr + 16 <= m) {
                 uint4 u;
                 uint32_t* uw = reinterpret_cast<uint32_t*>(&u);
@@ -641,7 +658,7 @@ __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x
             const int64_t gr = r0 + line, gc = c0 + off;
             if (gr >= m) continue;
             for (int e = 0; e < 16; ++e)
-                if (gc + e < n) out[gr * som + (gc + e) * son] = q[line][off + e];
+                if (gc + e < n) out[gr * som + (gc + e) * son] = qbuf[line * pitch + off + e];
         }
     }
 }
