@@ -12,7 +12,10 @@ Prints one JSON line (rank 0). Keys: metric/value/unit (GEMM TFLOP/s of the
 whole step), ms_per_step, roofline (dominant kernel: the GEMM, against the
 dense FP8 peak = 2x the measured bf16 peak), cast (GB/s of the cast kernel
 against measured HBM bandwidth), cast_sweep (the pages' per-token cast
-point: 16384 tokens x 4096, group 32, packed UE8M0), e2e (host buffers,
+point: 16384 tokens x 4096, group 32, packed UE8M0), workloads (the smaller
+workloads, timed apart from the step: forward GEMMs at M = 64/128/4096, the
+Linear layer's fwd+dgrad+wgrad step, the low-latency cast at 1-512 tokens
+eager and inside a CUDA graph), e2e (host buffers,
 copies inside the timed region), cpu_baseline (the CPU oracle on a bounded
 sample), clocks (nvidia-smi during the timed region), gpu_launches.
 
@@ -52,6 +55,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads (small-M GEMMs, Linear step, low-latency cast)")
+    ap.add_argument("--only-workloads", action="store_true",
+                    help="run only the other workloads and print them as one JSON line")
+    ap.add_argument("--reps", type=int, default=20, help="timed repetitions per other workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-oracle sample time")
     return ap.parse_args()
 
@@ -230,6 +238,12 @@ def run_ours(args, world, rank, local):
     fp8_peak = 2.0 * pk["bf16"]
     fp8_peak_sus = 2.0 * pk["bf16_sus"] if pk["bf16_sus"] else None
 
+    if args.only_workloads:
+        wl, _ = run_workloads(dev, pk, args.reps)
+        if rank == 0:
+            print(json.dumps({"workloads": wl}), flush=True)
+        return
+
     x = syn.randn((m, k), seed=syn.SEED_X + 1000 * rank, device=str(dev))
     w = syn.randn((n, k), seed=syn.SEED_W, mul=0.02, device=str(dev))
     wq, ws = ops.fp8_cast_per_block(w, fmt)
@@ -340,6 +354,11 @@ def run_ours(args, world, rank, local):
         e2e = {"value": round(flops_step * world * ke / te / 1e12, 2), "unit": UNIT,
                "h2d_bytes_per_step": m * k * 2, "d2h_bytes_per_step": m * n * 2, "steps": ke}
 
+    workloads = None
+    if not args.no_workloads:
+        del x, xq, xs, d
+        workloads, _ = run_workloads(dev, pk, args.reps)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         sample = CpuOracleSample(n, k, fmt)
@@ -371,12 +390,132 @@ def run_ours(args, world, rank, local):
             "cast": {"ms": round(cast_ms, 4), "bytes": cast_bytes, "gbs": round(cast_gbs, 1),
                      "frac_hbm": round(cast_gbs / pk["hbm_gbs"], 4), "peak_gbs": pk["hbm_gbs"]},
             "cast_sweep": sweep,
+            "workloads": workloads,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": 2 * K,
         }
         print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ other workloads
+def _median_ms(fn, reps, flush=None, warm=3):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def run_workloads(dev, pk, reps):
+    """The smaller workloads of the method's pages, each timed with CUDA events
+    (median of `reps`):
+
+    - forward GEMM N=4096, K=7168 at M = 64, 128 (HBM-bound: W's bytes
+      dominate) and 4096 (tensor-bound), L2 flushed before each repetition;
+    - the Linear layer's step, X [4096, 7168], dY [4096, 4096], W [4096, 7168]:
+      weight casts (W and W^T, 128x128), forward (cast X + GEMM), dgrad (cast dY
+      + GEMM against W^T), wgrad (transposed casts of dY and X + fp32 GEMM),
+      L2 flushed before each step;
+    - the low-latency per-token cast (hidden 4096, group 32, packed UE8M0) at
+      1, 64 and 512 tokens: eager with a flushed L2, and the device time per
+      cast inside a captured CUDA graph of 50 casts.
+    Returns (dict, number of this library's kernel launches timed).
+    """
+    import torch
+
+    from quantised_linear_layers_gb300 import linear, ops
+    from quantised_linear_layers_gb300 import synthetic as syn
+
+    P = ops.SF_PACKED_UE8M0
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    out, launches = {}, 0
+
+    w = syn.randn((4096, 7168), seed=syn.SEED_W, mul=0.02, device=str(dev))
+    wq, ws = ops.fp8_cast_per_block(w, P)
+    rows = []
+    for m in (64, 128, 4096):
+        x = syn.randn((m, 7168), seed=syn.SEED_X, device=str(dev))
+        xq, xs = ops.fp8_cast_per_token(x, 128, P, sf_mn_major=True)
+        d = torch.empty((m, 4096), dtype=torch.bfloat16, device=dev)
+        ms = _median_ms(lambda: ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, P, out=d), reps, flush)
+        launches += reps
+        byts = m * 7168 + 4096 * 7168 + m * 4096 * 2 + 4 * (m + 4096 // 128) * (7168 // 512)
+        fl = 2 * m * 4096 * 7168
+        rows.append({"m": m, "n": 4096, "k": 7168, "us": round(ms * 1e3, 2),
+                     "tflops": round(fl / ms / 1e9, 1), "gbs": round(byts / ms / 1e6, 1),
+                     "frac_hbm": round(byts / ms / 1e6 / pk["hbm_gbs"], 3)})
+    out["gemm_fwd_n4096_k7168_cold_l2"] = rows
+
+    x = syn.randn((4096, 7168), seed=syn.SEED_X, device=str(dev))
+    dy = syn.randn((4096, 4096), seed=syn.SEED_DY, device=str(dev))
+    w8 = linear.FP8Weight(w, P)
+    torch.cuda.synchronize()
+    ev = []
+    for i in range(3 + reps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        e[0].record()
+        w8.update(w)
+        e[1].record()
+        linear.forward(x, w8)
+        e[2].record()
+        linear.dgrad(dy, w8)
+        e[3].record()
+        linear.wgrad(dy, x, P)
+        e[4].record()
+        if i >= 3:
+            ev.append(e)
+            launches += 8
+    torch.cuda.synchronize()
+    part = [statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(4)]
+    step = statistics.median(e[0].elapsed_time(e[4]) for e in ev)
+    fl = 2 * 4096 * 4096 * 7168
+    out["linear_step_4096x4096x7168_cold_l2"] = {
+        "us_weight_casts": round(part[0] * 1e3, 1), "us_fwd": round(part[1] * 1e3, 1),
+        "us_dgrad": round(part[2] * 1e3, 1), "us_wgrad": round(part[3] * 1e3, 1),
+        "us_step": round(step * 1e3, 1), "tflops_step": round(3 * fl / step / 1e9, 1),
+        "tflops_without_weight_casts": round(3 * fl / (step - part[0]) / 1e9, 1)}
+    del x, dy, w8, w, wq, ws
+
+    rows = []
+    G = 50
+    for t in (1, 64, 512):
+        xt = syn.randn_row_exp(t, 4096, device=str(dev))
+        q = torch.empty((t, 4096), dtype=torch.float8_e4m3fn, device=dev)
+        sf = ops.empty_sf(t, ops.sf_shape(4096, 32, P), P, dev)
+        f = lambda: ops.fp8_cast_per_token(xt, 32, P, out=q, out_sf=sf)
+        eager = _median_ms(f, reps, flush)
+        launches += reps
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            f()
+            s.synchronize()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(G):
+                    f()
+        torch.cuda.current_stream().wait_stream(s)
+        per = _median_ms(lambda: g.replay(), reps) / G
+        launches += reps * G
+        byts = t * 4096 * 3 + t * 32 * 4
+        rows.append({"tokens": t, "bytes": byts, "us_eager_cold_l2": round(eager * 1e3, 2),
+                     "us_per_cast_in_graph": round(per * 1e3, 2)})
+    out["cast_low_latency_h4096_g32_packed"] = rows
+    assert ops.device_status() == 0
+    return out, launches
 
 
 # ------------------------------------------------------------------ reference arm

@@ -10,5 +10,6 @@ it with gcc and exposes numpy-level wrappers.
 from .oracle import (  # noqa: F401
     SF_FP32, SF_UE8M0, SF_PACKED_UE8M0, BF16, F32,
     build, round_output, e4m3_encode, e4m3_decode, cast_per_token, cast_per_block, gemm,
+    gemm_m_grouped_contiguous,
     overflow_count, reset_overflow_count, num_threads, set_num_threads,
 )

@@ -14,6 +14,10 @@ Functions and the passages they follow:
   gemm            "DeepGEMM Essentials" Parts 6 and 12-13; RHS scales read
                   row-wise per "[Help] Starter script for nn.Linear for
                   fwd,bwd" (maintainer's reply on RHS scales)
+  gemm_m_grouped_contiguous
+                  "DeepGEMM Essentials" Parts 8-11: each row of the
+                  contiguous token matrix times its expert's B; rows marked
+                  -1 are padding and are not computed
 
 Parity unpinned: the byte order of packed UE8M0 words (the pages never print
 it; little-endian, group j in byte j % 4 of word j // 4, is the reading).
@@ -222,3 +226,28 @@ def gemm(a: np.ndarray, sfa: np.ndarray, b: np.ndarray, sfb: np.ndarray, fmt: in
     if rc != 0:
         raise ValueError("oracle_gemm: bad arguments")
     return round_output(d, out) if out != "f64" else d
+
+
+def gemm_m_grouped_contiguous(a: np.ndarray, sfa: np.ndarray, b: np.ndarray, sfb: np.ndarray, fmt: int,
+                              m_indices, out: str = "f64") -> np.ndarray:
+    """M-grouped GEMM over the contiguous layout of "DeepGEMM Essentials"
+    Parts 8-11 (m_grouped_gemm_fp8_fp8_bf16_nt_contiguous): row i of A is
+    multiplied by expert e = m_indices[i]'s weights, D[i] = A[i] B[e]^T with
+    A's 1x128 scales and expert e's own 128x128 block-scale grid (Part 10 casts
+    every expert separately). Rows whose index is -1 are padding (Part 9) and
+    stay NaN in the result; any other index outside [0, G) is an error.
+
+    a: uint8 [m, k]; b: uint8 [G, n, k]; sfb: [G, ceil(n/128), ceil(k/128)]
+    (float32, or int32 words when fmt == 2). Returns float64 [m, n]."""
+    idx = np.asarray(m_indices).astype(np.int64).reshape(-1)
+    m = a.shape[0]
+    G, n, _ = b.shape
+    assert idx.size == m and sfb.shape[0] == G
+    if np.any((idx < -1) | (idx >= G)):
+        raise ValueError("m_indices outside [-1, G)")
+    d = np.full((m, n), np.nan)
+    for e in range(G):
+        rows = np.nonzero(idx == e)[0]
+        if rows.size:
+            d[rows] = gemm(a, sfa, b[e], sfb[e], fmt, rows=rows, out=out)
+    return d

@@ -15,6 +15,9 @@ per-token FP8 cast in Triton (fused_per_token_cast_to_fp8), version 3"
   * ``randn_row_exp``   standard normal times 10**u per row, u ~ U(-3, 3)
   * edge planting       one all-zero group (row 0, first group) and one row
                         of +-3.0e38 entries (representable in bf16)
+  * ``contiguous_layout`` the expert-id vector of "DeepGEMM Essentials"
+                        Parts 8-9: each expert's tokens padded up to the
+                        alignment, padding rows marked -1
 """
 from __future__ import annotations
 
@@ -68,3 +71,23 @@ def random_bytes(nbytes: int, seed: int, device: str = "cpu") -> torch.Tensor:
     """Canary bytes for view-isolation checks."""
     return torch.randint(0, 256, (nbytes,), generator=_gen(seed, device), dtype=torch.int32,
                          device=device).to(torch.uint8)
+
+
+def contiguous_layout(tokens_per_expert, alignment: int = 128):
+    """Expert index per row of the contiguous grouped layout: expert e's
+    tokens, then -1 up to the next multiple of ``alignment``, expert after
+    expert. Returns (int32 tensor [sum of aligned counts], aligned counts)."""
+    aligned = [(t + alignment - 1) // alignment * alignment for t in tokens_per_expert]
+    idx = torch.full((sum(aligned),), -1, dtype=torch.int32)
+    start = 0
+    for e, (t, a) in enumerate(zip(tokens_per_expert, aligned)):
+        idx[start:start + t] = e
+        start += a
+    return idx, aligned
+
+
+def tokens_per_expert(num_experts: int, mean: int, seed: int, spread: float = 0.25) -> list:
+    """Uneven token counts per expert: mean * U(1 - spread, 1 + spread), rounded."""
+    g = _gen(seed)
+    u = torch.rand(num_experts, generator=g, dtype=torch.float64)
+    return [int(round(mean * (1 - spread + 2 * spread * float(v)))) for v in u]

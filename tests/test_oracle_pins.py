@@ -488,3 +488,93 @@ def test_block_cast_packed_words(orc):
     padded = np.zeros((3, 8), dtype=np.uint8)
     padded[:, :6] = e
     assert np.array_equal(s2.view(np.uint8).reshape(3, 8), padded)
+
+
+# ------------------------------------------- M-grouped contiguous GEMM (Parts 8-11)
+def test_contiguous_layout_worked_example():
+    shapes = json.load(open(os.path.join(GOLDEN, "worked_shapes.json")))
+    for key in ("grouped_worked", "grouped_challenge"):
+        w = shapes[key]
+        idx, aligned = syn.contiguous_layout(w["tokens_per_expert"], w["alignment"])
+        assert aligned == w["aligned"] and idx.numel() == w["total_aligned"]
+        start = 0
+        for e, (t, a) in enumerate(zip(w["tokens_per_expert"], aligned)):
+            assert start % w["alignment"] == 0
+            assert bool((idx[start:start + t] == e).all()) and bool((idx[start + t:start + a] == -1).all())
+            start += a
+    w = shapes["grouped_worked"]
+    idx, _ = syn.contiguous_layout(w["tokens_per_expert"], w["alignment"])
+    assert int((idx == -1).sum()) == w["padding_rows"]
+
+
+def _grouped_int_case(G_tokens, n, k, seed):
+    idx, aligned = syn.contiguous_layout(G_tokens, 128)
+    m, G = idx.numel(), len(G_tokens)
+    a = syn.e4m3_small_ints((m, k), seed=seed).numpy()
+    b = syn.e4m3_small_ints((G, n, k), seed=seed + 1).numpy()
+    return idx.numpy(), a, b
+
+
+def test_grouped_gemm_exact_small_integers(orc):
+    w = json.load(open(os.path.join(GOLDEN, "worked_shapes.json")))["grouped_worked"]
+    n, k = w["n"], w["k"]
+    idx, a, b = _grouped_int_case(w["tokens_per_expert"], n, k, 51)
+    G, KB = b.shape[0], k // 128
+    qa, qb = orc.e4m3_encode(a), orc.e4m3_encode(b)
+    sfa = np.ones((a.shape[0], KB), dtype=np.float32)
+    # each expert's own grid: expert e scales its whole B by 2^(e-1)
+    sfb = np.stack([np.full((n // 128, KB), 2.0 ** (e - 1), dtype=np.float32) for e in range(G)])
+    d = orc.gemm_m_grouped_contiguous(qa, sfa, qb, sfb, orc.SF_FP32, idx)
+    for i in range(a.shape[0]):
+        e = idx[i]
+        if e < 0:
+            assert np.all(np.isnan(d[i]))
+        else:
+            ref = (a[i].astype(np.int64) @ b[e].astype(np.int64).T).astype(np.float64) * 2.0 ** (e - 1)
+            assert np.array_equal(d[i], ref)
+    # taking expert 0's weights for every row would not match (the pin discriminates)
+    rows1 = np.nonzero(idx == 1)[0]
+    wrong = a[rows1].astype(np.int64) @ b[0].astype(np.int64).T
+    assert not np.array_equal(d[rows1], wrong.astype(np.float64))
+
+
+def test_grouped_gemm_expert_scale_grid_row_wise(orc):
+    n, k = 384, 640                                            # n/128 = 3 != k/128 = 5
+    idx, a, b = _grouped_int_case([100, 0, 200], n, k, 61)      # an expert with no tokens
+    G = b.shape[0]
+    qa, qb = orc.e4m3_encode(a), orc.e4m3_encode(b)
+    sfa = np.array([[2.0 ** ((i % 3) - j) for j in range(5)] for i in range(a.shape[0])], dtype=np.float32)
+    sfb = np.array([[[2.0 ** (e + i - 2 * j) for j in range(5)] for i in range(3)] for e in range(G)],
+                   dtype=np.float32)
+    d = orc.gemm_m_grouped_contiguous(qa, sfa, qb, sfb, orc.SF_FP32, idx)
+    adeq = a.astype(np.float64) * np.repeat(sfa.astype(np.float64), 128, 1)
+    for e in (0, 2):
+        rows = np.nonzero(idx == e)[0]
+        bdeq = b[e].astype(np.float64) * np.repeat(np.repeat(sfb[e].astype(np.float64), 128, 0), 128, 1)
+        assert np.array_equal(d[rows], adeq[rows] @ bdeq.T)
+    assert np.all(np.isnan(d[idx < 0]))
+
+
+def test_grouped_gemm_packed_equals_fp32_powers(orc):
+    idx, a, b = _grouped_int_case([130, 60], 256, 1024, 71)
+    qa, qb = orc.e4m3_encode(a), orc.e4m3_encode(b)
+    m, G = a.shape[0], b.shape[0]
+    rng = np.random.default_rng(9)
+    ea = rng.integers(120, 134, size=(m, 8)).astype(np.uint8)
+    eb = rng.integers(120, 134, size=(G, 2, 8)).astype(np.uint8)
+    fa = np.ldexp(1.0, ea.astype(np.int32) - 127).astype(np.float32)
+    fb = np.ldexp(1.0, eb.astype(np.int32) - 127).astype(np.float32)
+    d1 = orc.gemm_m_grouped_contiguous(qa, fa, qb, fb, orc.SF_UE8M0, idx)
+    d2 = orc.gemm_m_grouped_contiguous(qa, ea.view(np.int32).reshape(m, 2), qb,
+                                       eb.view(np.int32).reshape(G, 2, 2), orc.SF_PACKED_UE8M0, idx)
+    assert np.array_equal(d1, d2, equal_nan=True)
+
+
+def test_grouped_gemm_rejects_bad_index(orc):
+    idx, a, b = _grouped_int_case([128], 128, 128, 81)
+    qa, qb = orc.e4m3_encode(a), orc.e4m3_encode(b)
+    idx = idx.copy()
+    idx[5] = 1                                                  # only expert 0 exists
+    with pytest.raises(ValueError):
+        orc.gemm_m_grouped_contiguous(qa, np.ones((128, 1), np.float32), qb, np.ones((1, 1, 1), np.float32),
+                                      orc.SF_FP32, idx)
