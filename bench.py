@@ -430,7 +430,9 @@ def run_workloads(dev, pk, reps):
       L2 flushed before each step;
     - the low-latency per-token cast (hidden 4096, group 32, packed UE8M0) at
       1, 64 and 512 tokens: eager with a flushed L2, and the device time per
-      cast inside a captured CUDA graph of 50 casts.
+      cast inside a captured CUDA graph of 50 casts;
+    - the M-grouped contiguous GEMM of a mixture-of-experts layer: 8 experts
+      of about 2048 tokens each, N=4096, K=7168, L2 flushed.
     Returns (dict, number of this library's kernel launches timed).
     """
     import torch
@@ -457,6 +459,7 @@ def run_workloads(dev, pk, reps):
                      "tflops": round(fl / ms / 1e9, 1), "gbs": round(byts / ms / 1e6, 1),
                      "frac_hbm": round(byts / ms / 1e6 / pk["hbm_gbs"], 3)})
     out["gemm_fwd_n4096_k7168_cold_l2"] = rows
+
 
     x = syn.randn((4096, 7168), seed=syn.SEED_X, device=str(dev))
     dy = syn.randn((4096, 4096), seed=syn.SEED_DY, device=str(dev))
@@ -514,6 +517,31 @@ def run_workloads(dev, pk, reps):
         rows.append({"tokens": t, "bytes": byts, "us_eager_cold_l2": round(eager * 1e3, 2),
                      "us_per_cast_in_graph": round(per * 1e3, 2)})
     out["cast_low_latency_h4096_g32_packed"] = rows
+
+    # M-grouped contiguous GEMM (mixture of experts): 8 experts of about 2048
+    # tokens each (uneven), N = 4096, K = 7168, packed UE8M0 scales
+    tokens = syn.tokens_per_expert(8, 2048, seed=17)
+    idx, _ = syn.contiguous_layout(tokens, 128)
+    mg = idx.numel()
+    xg = syn.randn((mg, 7168), seed=syn.SEED_X, device=str(dev))
+    xgq, xgs = ops.fp8_cast_per_token(xg, 128, P, sf_mn_major=True)
+    del xg
+    wg = torch.empty((8, 4096, 7168), dtype=torch.float8_e4m3fn, device=dev)
+    wgs = torch.empty((8, 32, 14), dtype=torch.int32, device=dev)
+    for e in range(8):
+        we = syn.randn((4096, 7168), seed=100 + e, mul=0.02, device=str(dev))
+        ops.fp8_cast_per_block(we, P, out=wg[e], out_sf=wgs[e])
+    del we
+    idx = idx.to(dev)
+    dg = torch.empty((mg, 4096), dtype=torch.bfloat16, device=dev)
+    ms = _median_ms(lambda: ops.m_grouped_gemm_fp8_nt_bf16_contiguous(xgq, xgs, wg, wgs, idx, P, out=dg),
+                    reps, flush)
+    launches += reps
+    fl = 2 * sum(tokens) * 4096 * 7168
+    out["grouped_gemm_8experts_n4096_k7168_cold_l2"] = {
+        "tokens": tokens, "m_aligned": mg, "us": round(ms * 1e3, 1), "tflops_valid_rows": round(fl / ms / 1e9, 1),
+        "tflops_incl_padding": round(2 * mg * 4096 * 7168 / ms / 1e9, 1)}
+    del xgq, xgs, wg, wgs, dg
     assert ops.device_status() == 0
     return out, launches
 

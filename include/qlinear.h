@@ -144,8 +144,9 @@ ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t
  *   d    [m, n] bf16 at d[i*ldd + j].
  *   workspace / ws_bytes: reserved, may be NULL / 0 (ql_gemm_workspace_size returns 0).
  * Requirements (QL_ERR_ALIGNMENT otherwise): a, b 16-byte aligned; lda, ldb
- * multiples of 16; k a multiple of 16 (the tensor-memory-access unit moves
- * 16-byte rows). m == 0 or n == 0 is a no-op; k == 0 writes D = 0.
+ * multiples of 16 (the tensor-memory-access unit moves 16-byte rows). Any k:
+ * the operand tiles are zero-filled past column k. m == 0 or n == 0 is a
+ * no-op; k == 0 writes D = 0.
  * ------------------------------------------------------------------------- */
 ql_status gemm_fp8_nt_bf16(const uint8_t* a, int64_t lda, const void* sfa,
                            int64_t sfa_stride_m, int64_t sfa_stride_k,
@@ -174,6 +175,45 @@ ql_status gemm_fp8_wgrad_fp32(const uint8_t* a, int64_t lda, const void* sfa,
                               int fmt, float* d, int64_t ldd,
                               int64_t m, int64_t n, int64_t k, int accumulate,
                               void* workspace, size_t ws_bytes, ql_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * m_grouped_gemm_fp8_nt_bf16_contiguous
+ * The M-grouped GEMM over the contiguous layout of "DeepGEMM Essentials"
+ * Parts 8-11 (m_grouped_gemm_fp8_fp8_bf16_nt_contiguous), as used for the
+ * experts of a mixture-of-experts layer: the tokens of all experts are stacked
+ * in one matrix A, each expert's rows padded up to a multiple of
+ * ql_get_m_alignment_for_contiguous_layout() (128), and m_indices gives the
+ * expert of every row (-1 for padding rows). For every row i with
+ * e = m_indices[i] >= 0:
+ *
+ *   D[i,j] = bf16_rn( sum_kb sa[i,kb] * sfb_e[j/128,kb] * sum_{k in kb} A[i,k] B_e[j,k] )
+ *
+ *   a, sfa     as gemm_fp8_nt_bf16 ([m, k] with 1x128 scales).
+ *   b          [num_groups, n, k] E4M3: expert e's row j at b + (e*n + j)*ldb.
+ *   sfb        expert e's 128x128 block grid [ceil(n/128), ceil(k/128)] at
+ *              sfb[e*sfb_stride_g + r*sfb_stride_n + kb*sfb_stride_k] (Part 10
+ *              casts each expert separately), same format rules as sfa.
+ *   m_indices  device int32 [m]: expert per row, -1 for padding.
+ *   d          [m, n] bf16 at d[i*ldd + j]. Rows with index -1 are not written.
+ * Requirements: m a multiple of 128 (QL_ERR_INVALID_ARG otherwise), every
+ * expert's segment starting on a multiple of 128, num_groups*n < 2^31,
+ * k > 0 (QL_ERR_UNSUPPORTED for k == 0), alignment rules of gemm_fp8_nt_bf16.
+ * The indices are read on the device: a 128-row tile whose first index is -1
+ * is skipped; an index outside [-1, num_groups), or a row whose expert differs
+ * from its tile's first row, is not computed and makes the next
+ * ql_device_status() return QL_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------- */
+ql_status m_grouped_gemm_fp8_nt_bf16_contiguous(const uint8_t* a, int64_t lda, const void* sfa,
+                                                int64_t sfa_stride_m, int64_t sfa_stride_k,
+                                                const uint8_t* b, int64_t ldb, const void* sfb,
+                                                int64_t sfb_stride_g, int64_t sfb_stride_n,
+                                                int64_t sfb_stride_k, int fmt, uint16_t* d,
+                                                int64_t ldd, const int32_t* m_indices, int num_groups,
+                                                int64_t m, int64_t n, int64_t k, ql_stream_t stream);
+
+/* Row alignment of every expert segment in the contiguous grouped layout
+ * ("DeepGEMM Essentials" Part 8: get_m_alignment_for_contiguous_layout): 128. */
+int ql_get_m_alignment_for_contiguous_layout(void);
 
 /* Workspace bytes a GEMM of this shape needs (0 in this build). */
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k);
@@ -216,8 +256,9 @@ ql_status ql_set_wait_limit_ms(int ms);
 ql_status ql_test_stall_gemm_producer(int enable);
 
 /* Synchronises `stream`, then returns and clears the device status word:
- * QL_OK, or QL_ERR_DEVICE_TIMEOUT if any kernel's bounded wait ran out since
- * the last call; QL_ERR_CUDA if the synchronisation itself failed. */
+ * QL_OK; QL_ERR_DEVICE_TIMEOUT if any kernel's bounded wait ran out since the
+ * last call; else QL_ERR_INVALID_ARG if a grouped GEMM met an invalid expert
+ * index; QL_ERR_CUDA if the synchronisation itself failed. */
 ql_status ql_device_status(ql_stream_t stream);
 
 #ifdef __cplusplus

@@ -65,7 +65,8 @@ ql_status from_cuda(cudaError_t e) {
 
 ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sam, int64_t sak, const uint8_t* b,
                       int64_t ldb, const void* sfb, int64_t sbn, int64_t sbk, int fmt, void* d, int64_t ldd,
-                      int64_t m, int64_t n, int64_t k, bool wgrad, int accumulate, cudaStream_t st) {
+                      int64_t m, int64_t n, int64_t k, bool wgrad, int accumulate, cudaStream_t st,
+                      const int32_t* m_indices = nullptr, int num_groups = 1, int64_t sbg = 0) {
     if (m < 0 || n < 0 || k < 0) return QL_ERR_INVALID_ARG;
     if (fmt < QL_SF_FP32 || fmt > QL_SF_PACKED_UE8M0) return QL_ERR_INVALID_ARG;
     if (m >= (int64_t(1) << 31) || n >= (int64_t(1) << 31) || k >= (int64_t(1) << 31)) return QL_ERR_UNSUPPORTED;
@@ -108,6 +109,9 @@ ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sa
     L.stall_producer = g_stall_producer.load();
     L.dev_status = di.status;
     L.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ms.load()) * 1000000ull;
+    L.m_indices = m_indices;
+    L.num_groups = num_groups;
+    L.sbg = sbg;
     return from_cuda(ql::launch_gemm(L, st, effective_sms(di)));
 }
 
@@ -218,6 +222,27 @@ ql_status gemm_fp8_wgrad_fp32(const uint8_t* a, int64_t lda, const void* sfa, in
                        m, n, k, true, accumulate, reinterpret_cast<cudaStream_t>(stream));
 }
 
+ql_status m_grouped_gemm_fp8_nt_bf16_contiguous(const uint8_t* a, int64_t lda, const void* sfa,
+                                                int64_t sfa_stride_m, int64_t sfa_stride_k, const uint8_t* b,
+                                                int64_t ldb, const void* sfb, int64_t sfb_stride_g,
+                                                int64_t sfb_stride_n, int64_t sfb_stride_k, int fmt, uint16_t* d,
+                                                int64_t ldd, const int32_t* m_indices, int num_groups, int64_t m,
+                                                int64_t n, int64_t k, ql_stream_t stream) {
+    if (m < 0 || n < 0 || k < 0 || num_groups < 1) return QL_ERR_INVALID_ARG;
+    if (m % ql::kGroupAlignM != 0) return QL_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_groups) * n >= (int64_t(1) << 31)) return QL_ERR_UNSUPPORTED;
+    if (m == 0 || n == 0) return QL_OK;
+    if (m_indices == nullptr) return QL_ERR_INVALID_ARG;
+    // k == 0 would make every expert row zero while leaving padding rows
+    // untouched; that needs the indices on the host, so it is refused.
+    if (k == 0) return QL_ERR_UNSUPPORTED;
+    return gemm_common(a, lda, sfa, sfa_stride_m, sfa_stride_k, b, ldb, sfb, sfb_stride_n, sfb_stride_k, fmt, d, ldd,
+                       m, n, k, false, 0, reinterpret_cast<cudaStream_t>(stream), m_indices, num_groups,
+                       sfb_stride_g);
+}
+
+int ql_get_m_alignment_for_contiguous_layout(void) { return ql::kGroupAlignM; }
+
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k) {
     (void)m;
     (void)n;
@@ -270,7 +295,7 @@ ql_status ql_device_status(ql_stream_t stream) {
     if (v != 0) {
         const uint32_t zero = 0;
         if (cudaMemcpy(di.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return QL_ERR_CUDA;
-        return QL_ERR_DEVICE_TIMEOUT;
+        return (v & ql::kDevErrTimeout) ? QL_ERR_DEVICE_TIMEOUT : QL_ERR_INVALID_ARG;
     }
     return QL_OK;
 }

@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(128) cast_generic_kernel(const T* __restrict__
 // out_mode: 0 rows contiguous, 1 columns contiguous, 2 generic
 // ---------------------------------------------------------------------------
 template <typename T, int FMT, bool RECIP>
-__global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x, int64_t m, int64_t n,
+__global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel(const T* __restrict__ x, int64_t m, int64_t n,
                                                          int64_t sxm, int64_t sxn, int in_mode,
                                                          uint8_t* __restrict__ out, int64_t som, int64_t son,
                                                          int out_mode, void* __restrict__ sf, int64_t ssr,
@@ -513,8 +513,23 @@ __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * B;
 
     // element e (0..63) of this thread: (a, b) in block coordinates along the
-    // (contiguous, strided) input axes: b = v*16 + tid/16, a = (tid%16)*8 + e%8
-    float v[64];
+    // (contiguous, strided) input axes: b = v*16 + tid/16, a = (tid%16)*8 + e%8.
+    // The elements are kept as the raw input words (bf16 pairs, or fp32), so
+    // the block costs 32 registers of data per thread for bf16 input.
+    constexpr int WPG = (8 * static_cast<int>(sizeof(T))) / 4;      // words per 8 elements
+    uint32_t raw[8 * WPG];
+    auto elem_bits = [&](const T* q) -> uint32_t {
+        if constexpr (sizeof(T) == 2) return __bfloat16_as_ushort(*q);
+        else return __float_as_uint(*q);
+    };
+    auto put = [&](int it, int e, uint32_t bits) {
+        if constexpr (sizeof(T) == 2) {
+            uint32_t& w = raw[it * WPG + e / 2];
+            w = (e & 1) ? ((w & 0xFFFFu) | (bits << 16)) : ((w & 0xFFFF0000u) | bits);
+        } else {
+            raw[it * WPG + e] = bits;
+        }
+    };
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int bb = it * 16 + tid / 16;
@@ -522,51 +537,43 @@ __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x
         int64_t r, c;  // block-relative row/col of element a0
         if (in_mode == 1) { r = a0; c = bb; } else { r = bb; c = a0; }
         const int64_t gr = r0 + r, gc = c0 + c;
-        if (in_mode == 0) {
-            const T* p = x + gr * sxm + gc;
-            if (gr < m && gc + 8 <= n) {
-                const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-                const T* t = reinterpret_cast<const T*>(&u);
-                if constexpr (sizeof(T) == 2) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[it * 8 + e] = to_f32(t[e]);
-                } else {
-                    const uint4 u2 = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-                    const T* t2 = reinterpret_cast<const T*>(&u2);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) { v[it * 8 + e] = to_f32(t[e]); v[it * 8 + 4 + e] = to_f32(t2[e]); }
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[it * 8 + e] = (gr < m && gc + e < n) ? to_f32(p[e]) : 0.0f;
-            }
-        } else if (in_mode == 1) {
-            const T* p = x + gr + gc * sxn;
-            if (gc < n && gr + 8 <= m) {
-                const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-                const T* t = reinterpret_cast<const T*>(&u);
-                if constexpr (sizeof(T) == 2) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[it * 8 + e] = to_f32(t[e]);
-                } else {
-                    const uint4 u2 = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-                    const T* t2 = reinterpret_cast<const T*>(&u2);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) { v[it * 8 + e] = to_f32(t[e]); v[it * 8 + 4 + e] = to_f32(t2[e]); }
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[it * 8 + e] = (gc < n && gr + e < m) ? to_f32(p[e]) : 0.0f;
+        const T* p;
+        bool full;
+        int64_t step;                                   // element stride along a
+        if (in_mode == 0) { p = x + gr * sxm + gc; full = gr < m && gc + 8 <= n; step = 1; }
+        else if (in_mode == 1) { p = x + gr + gc * sxn; full = gc < n && gr + 8 <= m; step = 1; }
+        else { p = x + gr * sxm + gc * sxn; full = false; step = sxn; }
+        if (full) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+            raw[it * WPG + 0] = u.x; raw[it * WPG + 1] = u.y; raw[it * WPG + 2] = u.z; raw[it * WPG + 3] = u.w;
+            if constexpr (sizeof(T) == 4) {
+                const uint4 u2 = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+                raw[it * WPG + 4] = u2.x; raw[it * WPG + 5] = u2.y; raw[it * WPG + 6] = u2.z; raw[it * WPG + 7] = u2.w;
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                v[it * 8 + e] = (gr < m && gc + e < n) ? to_f32(x[gr * sxm + (gc + e) * sxn]) : 0.0f;
+            for (int w = 0; w < WPG; ++w) raw[it * WPG + w] = 0u;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const bool in = (in_mode == 1) ? (gc < n && gr + e < m) : (gr < m && gc + e < n);
+                if (in) put(it, e, elem_bits(p + e * step));
+            }
         }
     }
-    float amax = 0.0f;
+    float amax;
+    if constexpr (sizeof(T) == 2) {
+        __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
 #pragma unroll
-    for (int e = 0; e < 64; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        for (int w = 0; w < 8 * WPG; ++w) {
+            const uint32_t u = raw[w];
+            m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&u)));
+        }
+        amax = fmaxf(__low2float(m2), __high2float(m2));
+    } else {
+        amax = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8 * WPG; ++w) amax = fmaxf(amax, fabsf(__uint_as_float(raw[w])));
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     if ((tid & 31) == 0) red[tid >> 5] = amax;
@@ -592,12 +599,20 @@ __global__ void __launch_bounds__(256) cast_block_kernel(const T* __restrict__ x
     }
 
     // quantise into shared memory, block-relative [row][col]
+    auto val = [&](int it, int e) -> float {
+        if constexpr (sizeof(T) == 2) {
+            const uint32_t w = raw[it * WPG + e / 2];
+            return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+        } else {
+            return __uint_as_float(raw[it * WPG + e]);
+        }
+    };
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int bb = it * 16 + tid / 16;
         const int a0 = (tid % 16) * 8;
-        const uint32_t lo = quant4(v[it * 8], v[it * 8 + 1], v[it * 8 + 2], v[it * 8 + 3], f);
-        const uint32_t hi = quant4(v[it * 8 + 4], v[it * 8 + 5], v[it * 8 + 6], v[it * 8 + 7], f);
+        const uint32_t lo = quant4(val(it, 0), val(it, 1), val(it, 2), val(it, 3), f);
+        const uint32_t hi = quant4(val(it, 4), val(it, 5), val(it, 6), val(it, 7), f);
         if (in_mode == 1) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {

@@ -11,7 +11,8 @@
 namespace ql {
 
 // Device status word bits (read by ql_device_status()).
-constexpr uint32_t kDevErrTimeout = 1u;
+constexpr uint32_t kDevErrTimeout = 1u;     // a bounded wait ran out
+constexpr uint32_t kDevErrBadIndex = 2u;    // a grouped GEMM's expert index was invalid
 
 // ---------------------------------------------------------------------------
 // Small helpers

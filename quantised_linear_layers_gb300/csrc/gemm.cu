@@ -228,12 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = blockIdx.x; t < num_tiles && ok && !p.stall_producer; t += gridDim.x) {
                     int mb, nb;
                     tile_coords(t, p, mb, nb);
+                    const int e = tile_expert(p, mb, false);
+                    if (e < 0) continue;
+                    const int brow = static_cast<int>(e * p.b_group_rows) + nb * BN;
                     for (int kb = 0; kb < num_kb; ++kb, ++it) {
                         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                         if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
                         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                         tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], kb * BK, mb * BM);
-                        tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, nb * BN);
+                        tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, brow);
                     }
                 }
                 if (!ok) {
@@ -251,6 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t it = 0, tc = 0;
                 bool ok = true;
                 for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    int mb, nb;
+                    tile_coords(t, p, mb, nb);
+                    if (tile_expert(p, mb, false) < 0) continue;
                     for (int kb = 0; kb < num_kb; ++kb, ++it, ++tc) {
                         const uint32_t ts = tc % C::kTmemStages, tph = (tc / C::kTmemStages) & 1u;
                         if (!mbar_wait(&tempty[ts], tph ^ 1u, ctl)) { ok = false; break; }
@@ -287,7 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
+                const int e = tile_expert(p, mb, false);
+                if (e < 0) continue;
                 const int64_t m0 = static_cast<int64_t>(mb) * BM, n0 = static_cast<int64_t>(nb) * BN;
+                const int64_t sb_off = e * p.sbg;
                 for (int kb0 = 0; kb0 < num_kb; kb0 += kRun, ++run) {
                     const int cnt = num_kb - kb0 < kRun ? num_kb - kb0 : kRun;
                     if ((run & 1u) != mine) { g += cnt; continue; }
@@ -305,11 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (j < cnt) {
                                 if constexpr (PER_ROW_B) {
                                     const int64_t col = n0 + lane + 32 * i;
-                                    if (col < p.n) v = decode_scale(p.sfb, p.fmt, col * p.sbn, kb0 + j, p.sbk);
+                                    if (col < p.n) v = decode_scale(p.sfb, p.fmt, sb_off + col * p.sbn, kb0 + j, p.sbk);
                                 } else {
                                     const int64_t r = n0 / 128 + lane;
                                     if (lane < (BN + 127) / 128 && r < nblocks_b)
-                                        v = decode_scale(p.sfb, p.fmt, r * p.sbn, kb0 + j, p.sbk);
+                                        v = decode_scale(p.sfb, p.fmt, sb_off + r * p.sbn, kb0 + j, p.sbk);
                                 }
                             }
                             vb[j][i] = v;
@@ -350,6 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             int mb, nb;
             tile_coords(t, p, mb, nb);
+            const int e = tile_expert(p, mb, threadIdx.x == kThreads - kMathThreads);
+            if (e < 0) continue;
+            const int64_t row = static_cast<int64_t>(mb) * BM + r_local;
+            const bool store_row = row < p.m && (wg != 0 ? row_in_expert_quiet(p, row, e) : row_in_expert(p, row, e));
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
             for (int kb = 0; kb < num_kb; ++kb, ++g) {
@@ -407,9 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---------------- epilogue ----------------
-            const int64_t row = static_cast<int64_t>(mb) * BM + r_local;
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
-            if (row < p.m) {
+            if (store_row) {
                 if constexpr (!OUT_F32) {
                     __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
 #pragma unroll
@@ -468,7 +480,8 @@ cudaError_t launch_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num
     using Cf = Cfg<BN, PER_ROW_B>;
     CUtensorMap ta, tb;
     if (!encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)) return cudaErrorInvalidValue;
-    if (!encode_kmajor_map(&tb, L.b, L.n, L.k, L.ldb, BN)) return cudaErrorInvalidValue;
+    if (!encode_kmajor_map(&tb, L.b, L.n * (L.m_indices ? L.num_groups : 1), L.k, L.ldb, BN))
+        return cudaErrorInvalidValue;
     p.tiles_m = static_cast<int>((L.m + BM - 1) / BM);
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
     const int tiles = p.tiles_m * p.tiles_n;
@@ -525,14 +538,19 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     p.dev_status = L.dev_status;
     p.wait_limit_ns = L.wait_limit_ns;
     p.stall_producer = L.stall_producer;
+    p.m_indices = L.m_indices;
+    p.num_groups = L.m_indices ? L.num_groups : 1;
+    p.b_group_rows = L.n;
+    p.sbg = L.sbg;
     const int64_t es = L.out_f32 ? 4 : 2;
     p.vec_store = ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && (L.ldd * es) % 16 == 0) ? 1 : 0;
     const int bn = L.block_n > 0 ? L.block_n : choose_block_n(L.m, L.n, num_sms);
     // UE8M0 scales (fp32 powers of two or packed exponents): promotion by the
     // tensor core's block-scaled MMA unless the CUDA-core path is requested.
     const bool ue8m0 = L.fmt == 1 || L.fmt == 2;
-    if (ue8m0 && L.path == 3) return launch_gemm_mx2(L, p, st, num_sms);
-    if (ue8m0 && L.path == 0) {
+    const bool grouped = L.m_indices != nullptr;   // the pair kernel's two M halves share one B
+    if (ue8m0 && L.path == 3 && !grouped) return launch_gemm_mx2(L, p, st, num_sms);
+    if (ue8m0 && L.path == 0 && !grouped) {
         // CTA pairs on 256 x 256 tiles when there are enough tiles to give
         // every pair of SMs one; else single-SM tiles of the chosen width.
         const int64_t pair_tiles = ((L.m + 255) / 256) * ((L.n + 255) / 256);

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace ql {
 
 // Kernel parameters (passed by value).
@@ -23,6 +25,11 @@ struct GemmParams {
     uint32_t* dev_status;
     uint64_t wait_limit_ns;
     int stall_producer;       // test hook: the producer issues no copies (waits time out)
+    // M-grouped contiguous layout: expert index per row of A (nullptr: one B)
+    const int* m_indices;
+    int num_groups;
+    int64_t b_group_rows;     // rows of B per expert (n) in B's tensor map
+    int64_t sbg;              // sfb elements (or packed words) between experts
 };
 
 // Host-side description of one GEMM call.
@@ -48,7 +55,47 @@ struct GemmLaunch {
     uint32_t* dev_status;
     uint64_t wait_limit_ns;
     int stall_producer;
+    const int* m_indices;     // M-grouped contiguous layout (nullptr: plain GEMM)
+    int num_groups;
+    int64_t sbg;
 };
+
+// Rows of A per M tile; in the M-grouped contiguous layout every expert's
+// segment starts on a multiple of it.
+constexpr int kGroupAlignM = 128;
+
+#ifdef __CUDACC__
+// Expert of M tile `mb` in the M-grouped contiguous layout (0 for a plain
+// GEMM), read from the tile's first row. Returns -1 when the tile is padding
+// (index -1) and when the index lies outside [-1, num_groups): such a tile is
+// skipped by every role of the CTA; the caller passing report = true records a
+// bad index in the device status word.
+__device__ __forceinline__ int tile_expert(const GemmParams& p, int mb, bool report) {
+    if (p.m_indices == nullptr) return 0;
+    const int e = __ldg(p.m_indices + static_cast<int64_t>(mb) * kGroupAlignM);
+    if (e < -1 || e >= p.num_groups) {
+        if (report) atomicOr(p.dev_status, kDevErrBadIndex);
+        return -1;
+    }
+    return e;
+}
+
+// Whether the epilogue thread owning `row` of a tile of expert `e` stores it:
+// padding rows (-1) are left untouched; a row of another expert (a segment
+// not starting on the alignment) is not stored and is recorded as a bad index.
+__device__ __forceinline__ bool row_in_expert(const GemmParams& p, int64_t row, int e) {
+    if (p.m_indices == nullptr) return true;
+    const int r = __ldg(p.m_indices + row);
+    if (r == e) return true;
+    if (r != -1) atomicOr(p.dev_status, kDevErrBadIndex);
+    return false;
+}
+
+// The same decision without recording (for the other threads of the row).
+__device__ __forceinline__ bool row_in_expert_quiet(const GemmParams& p, int64_t row, int e) {
+    return p.m_indices == nullptr || __ldg(p.m_indices + row) == e;
+}
+#endif
 
 int choose_block_n(int64_t m, int64_t n, int num_sms);
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms);

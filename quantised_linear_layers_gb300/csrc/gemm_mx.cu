@@ -171,12 +171,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = blockIdx.x; t < num_tiles && ok && !p.stall_producer; t += gridDim.x) {
                     int mb, nb;
                     tile_coords(t, p, mb, nb);
+                    const int e = tile_expert(p, mb, false);
+                    if (e < 0) continue;
+                    const int brow = static_cast<int>(e * p.b_group_rows) + nb * BN;
                     for (int kb = 0; kb < num_kb; ++kb, ++it) {
                         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                         if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
                         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                         tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], kb * BK, mb * BM);
-                        tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, nb * BN);
+                        tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, brow);
                     }
                 }
                 if (!ok) {
@@ -190,8 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) {
                 uint32_t it = 0, g = 0, tc = 0;
                 bool ok = true;
-                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tc) {
+                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    int mb, nb;
+                    tile_coords(t, p, mb, nb);
+                    if (tile_expert(p, mb, false) < 0) continue;
                     const uint32_t as = tc % C::kAccStages, aph = (tc / C::kAccStages) & 1u;
+                    ++tc;
                     if (!mbar_wait(&tempty[as], aph ^ 1u, ctl)) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + as * BN;
@@ -252,7 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
+                const int e = tile_expert(p, mb, false);
+                if (e < 0) continue;
                 const int64_t m0 = static_cast<int64_t>(mb) * BM, n0 = static_cast<int64_t>(nb) * BN;
+                const int64_t sb_off = e * p.sbg;
                 for (int kg0 = 0; kg0 < num_groups; kg0 += run_len, ++run) {
                     const int cnt = num_groups - kg0 < run_len ? num_groups - kg0 : run_len;
                     if ((run & 1u) != mine) { g += cnt; continue; }
@@ -270,11 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (PER_ROW_B) {
                             const int64_t row = n0 + 32 * i + lane;        // chunk i/4, quarter i%4
                             valb[i] = row < p.n;
-                            offb[i] = row * p.sbn;
+                            offb[i] = sb_off + row * p.sbn;
                         } else {
                             const int64_t r = n0 / 128 + lane;             // one block word per chunk
                             valb[i] = lane < C::kSfbChunks && r < nblocks_b;
-                            offb[i] = r * p.sbn;
+                            offb[i] = sb_off + r * p.sbn;
                         }
                     }
                     if (p.fmt == 2) {
@@ -329,10 +339,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const bool vec_store = p.vec_store != 0;
         uint32_t tc = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             int mb, nb;
             tile_coords(t, p, mb, nb);
+            const int e = tile_expert(p, mb, threadIdx.x == kThreads - kMathThreads);
+            if (e < 0) continue;
+            const int64_t row = static_cast<int64_t>(mb) * BM + r_local;
+            const bool store_row = row < p.m && (wg != 0 ? row_in_expert_quiet(p, row, e) : row_in_expert(p, row, e));
             const uint32_t as = tc % C::kAccStages, aph = (tc / C::kAccStages) & 1u;
+            ++tc;
             if (!warp_wait(&tfull[as], aph, ctl)) break;
             tc_fence_after_sync();
             uint32_t accb[CPT];
@@ -346,9 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* acc = reinterpret_cast<float*>(accb);
             tc_fence_before_sync();
             mbar_arrive(&tempty[as]);
-            const int64_t row = static_cast<int64_t>(mb) * BM + r_local;
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
-            if (row < p.m) {
+            if (store_row) {
                 if constexpr (!OUT_F32) {
                     __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
 #pragma unroll
@@ -407,7 +421,8 @@ cudaError_t launch_mx_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int 
     using Cf = MxCfg<BN>;
     CUtensorMap ta, tb;
     if (!encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)) return cudaErrorInvalidValue;
-    if (!encode_kmajor_map(&tb, L.b, L.n, L.k, L.ldb, BN)) return cudaErrorInvalidValue;
+    if (!encode_kmajor_map(&tb, L.b, L.n * (L.m_indices ? L.num_groups : 1), L.k, L.ldb, BN))
+        return cudaErrorInvalidValue;
     p.tiles_m = static_cast<int>((L.m + BM - 1) / BM);
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
     const int tiles = p.tiles_m * p.tiles_n;

@@ -32,6 +32,9 @@ _SIGS = {
                          _i64, _i64, _i64, _vp, _sz, _vp],
     "gemm_fp8_wgrad_fp32": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
                             _i64, _i64, _i64, _int, _vp, _sz, _vp],
+    "m_grouped_gemm_fp8_nt_bf16_contiguous": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _i64,
+                                              _int, _vp, _i64, _vp, _int, _i64, _i64, _i64, _vp],
+    "ql_get_m_alignment_for_contiguous_layout": [],
     "ql_gemm_workspace_size": [_i64, _i64, _i64],
     "ql_set_num_sms": [_int],
     "ql_get_num_sms": [],
@@ -208,6 +211,42 @@ def gemm_fp8_wgrad_fp32(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb
         fmt, out.data_ptr(), out.stride(0), m, n, k, int(bool(accumulate)), None, 0, _stream(a))
     _check("gemm_fp8_wgrad_fp32", st)
     return out
+
+
+def m_grouped_gemm_fp8_nt_bf16_contiguous(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor,
+                                          sfb: torch.Tensor, m_indices: torch.Tensor, fmt: int = SF_FP32,
+                                          out: torch.Tensor | None = None) -> torch.Tensor:
+    """Grouped D = A B_e^T over the contiguous layout: A [m, k] (m a multiple of
+    128) with 1x128 scales, B [G, n, k] with scales sfb [G, ceil(n/128),
+    ceil(k/128)], m_indices int32 [m] (expert per row, -1 for padding rows,
+    which are left unwritten in ``out``)."""
+    _bytes8(a)
+    _bytes8(b)
+    if a.dim() != 2 or b.dim() != 3 or a.stride(1) != 1 or b.stride(2) != 1:
+        raise ValueError("a must be [m, k] and b [G, n, k], both with contiguous K")
+    if b.stride(0) != b.shape[1] * b.stride(1):
+        raise ValueError("b's experts must be stacked without gaps (stride(0) == n * stride(1))")
+    if a.shape[1] != b.shape[2] or sfb.dim() != 3 or sfb.shape[0] != b.shape[0]:
+        raise ValueError("shapes of a, b and sfb do not agree")
+    if m_indices.dtype != torch.int32 or m_indices.dim() != 1 or m_indices.shape[0] != a.shape[0] \
+            or not m_indices.is_contiguous() or m_indices.device != a.device:
+        raise ValueError("m_indices must be a contiguous int32 [m] tensor on a's device")
+    m, k = a.shape
+    G, n = b.shape[0], b.shape[1]
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    if out.dtype != torch.bfloat16 or out.stride(1) != 1:
+        raise ValueError("out must be bf16 with contiguous rows")
+    st = load_library().m_grouped_gemm_fp8_nt_bf16_contiguous(
+        a.data_ptr(), a.stride(0), sfa.data_ptr(), sfa.stride(0), sfa.stride(1),
+        b.data_ptr(), b.stride(1), sfb.data_ptr(), sfb.stride(0), sfb.stride(1), sfb.stride(2),
+        fmt, out.data_ptr(), out.stride(0), m_indices.data_ptr(), G, m, n, k, _stream(a))
+    _check("m_grouped_gemm_fp8_nt_bf16_contiguous", st)
+    return out
+
+
+def get_m_alignment_for_contiguous_layout() -> int:
+    return int(load_library().ql_get_m_alignment_for_contiguous_layout())
 
 
 def set_num_sms(n: int) -> None:

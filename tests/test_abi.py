@@ -29,7 +29,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("fp8_cast_per_token", "fp8_cast_per_block", "gemm_fp8_nt_bf16", "gemm_fp8_wgrad_fp32",
-                     "ql_status_string", "ql_set_num_sms", "ql_get_num_sms", "ql_device_status"):
+                     "m_grouped_gemm_fp8_nt_bf16_contiguous", "ql_status_string", "ql_set_num_sms", "ql_get_num_sms", "ql_device_status"):
         assert required in names
 
 
@@ -90,6 +90,14 @@ def test_host_validation_rejects_before_cuda(lib):
     q = ctypes.c_void_p(24)
     assert L.gemm_fp8_nt_bf16(q, 32, p, 1, 1, p, 32, p, 1, 1, 0, p, 8, 4, 8, 32, None, 0, None) == 3
     assert L.gemm_fp8_nt_bf16(p, 40, p, 1, 1, p, 32, p, 1, 1, 0, p, 8, 4, 8, 32, None, 0, None) == 3
+    # grouped GEMM: m not a multiple of the 128-row alignment, no experts, no index vector, k == 0
+    G = L.m_grouped_gemm_fp8_nt_bf16_contiguous
+    assert G(p, 32, p, 1, 1, p, 32, p, 1, 1, 1, 0, p, 8, p, 2, 100, 8, 32, None) == 1
+    assert G(p, 32, p, 1, 1, p, 32, p, 1, 1, 1, 0, p, 8, p, 0, 128, 8, 32, None) == 1
+    assert G(p, 32, p, 1, 1, p, 32, p, 1, 1, 1, 0, p, 8, None, 2, 128, 8, 32, None) == 1
+    assert G(p, 32, p, 1, 1, p, 32, p, 1, 1, 1, 0, p, 8, p, 2, 128, 8, 0, None) == 2
+    assert G(None, 32, None, 1, 1, None, 32, None, 1, 1, 1, 0, None, 8, None, 2, 0, 8, 32, None) == 0
+    assert L.ql_get_m_alignment_for_contiguous_layout() == 128
     assert L.ql_set_gemm_block_n(48) == 1
     assert L.ql_set_wait_limit_ms(0) == 1
 
