@@ -185,6 +185,33 @@ __device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) 
 __device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
+// 16-byte store into the shared memory of a CTA of the cluster (16-byte aligned address).
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c,
+                                                     uint32_t d) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// the shared memory of a CTA of the cluster (both addresses 16-byte aligned);
+// completion is signalled as transaction bytes on the destination CTA's
+// mbarrier (`bar_cluster_addr`). Tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster_addr, const void* src, uint32_t bytes,
+                                                     uint32_t bar_cluster_addr) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster_addr),
+        "r"(smem_addr(src)), "r"(bytes), "r"(bar_cluster_addr)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk copy of this thread has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
 
 // Waits with only a time limit (no abort check): used when draining copies
 // that are already in flight after an abort.

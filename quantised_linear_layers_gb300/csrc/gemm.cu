@@ -550,11 +550,15 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     const bool ue8m0 = L.fmt == 1 || L.fmt == 2;
     const bool grouped = L.m_indices != nullptr;   // the pair kernel's two M halves share one B
     if (ue8m0 && L.path == 3 && !grouped) return launch_gemm_mx2(L, p, st, num_sms);
-    if (ue8m0 && L.path == 0 && !grouped) {
+    const int split = (ue8m0 && !grouped && !L.out_f32) ? choose_split_k(L.m, L.n, L.k, num_sms) : 1;
+    if (L.path == 4 && split >= 2) return launch_gemm_mx_sk(L, p, split, st);
+    if (ue8m0 && L.path == 0 && !grouped && L.block_n == 0) {
         // CTA pairs on 256 x 256 tiles when there are enough tiles to give
-        // every pair of SMs one; else single-SM tiles of the chosen width.
+        // every pair of SMs one; split-K over a cluster when the 128 x 256
+        // tiles are too few to occupy the SMs; else single-SM tiles.
         const int64_t pair_tiles = ((L.m + 255) / 256) * ((L.n + 255) / 256);
-        if (L.block_n == 0 && pair_tiles >= num_sms / 2) return launch_gemm_mx2(L, p, st, num_sms);
+        if (pair_tiles >= num_sms / 2) return launch_gemm_mx2(L, p, st, num_sms);
+        if (split >= 2) return launch_gemm_mx_sk(L, p, split, st);
     }
     if (ue8m0 && L.path != 1) return launch_gemm_mx(L, p, bn, st, num_sms);
     if (L.out_f32) return dispatch_bn<true, true>(bn, L, p, st, num_sms);

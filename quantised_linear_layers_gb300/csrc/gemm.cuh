@@ -51,7 +51,8 @@ struct GemmLaunch {
     int accumulate;
     int block_n;              // 0 = heuristic, else 32/64/128/256
     int path;                 // 0 = auto, 1 = CUDA-core promotion, 2 = block-scaled MMA on one SM,
-                              // 3 = block-scaled MMA on CTA pairs (UE8M0 formats only)
+                              // 3 = block-scaled MMA on CTA pairs, 4 = split-K over a cluster
+                              // (3 and 4: UE8M0 formats only)
     uint32_t* dev_status;
     uint64_t wait_limit_ns;
     int stall_producer;
@@ -101,6 +102,10 @@ int choose_block_n(int64_t m, int64_t n, int num_sms);
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms);
 cudaError_t launch_gemm_mx(const GemmLaunch& L, const GemmParams& p, int bn, cudaStream_t st, int num_sms);
 cudaError_t launch_gemm_mx2(const GemmLaunch& L, const GemmParams& p, cudaStream_t st, int num_sms);
+// Split-K over a thread-block cluster (bf16 output, UE8M0 formats): cluster
+// size for the shape (1 = no split applies) and the launch.
+int choose_split_k(int64_t m, int64_t n, int64_t k, int num_sms);
+cudaError_t launch_gemm_mx_sk(const GemmLaunch& L, GemmParams p, int split, cudaStream_t st);
 
 // 2-D uint8 tensor map [rows, cols] (cols contiguous, row stride ld bytes),
 // box [box_rows x 128 bytes], 128-byte swizzle, zero fill out of bounds.

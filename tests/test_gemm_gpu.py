@@ -245,7 +245,7 @@ def test_wgrad_exact_pow2_scales(orc, ops, path, bn, k, packed):
     assert bad.size == 0, f"{len(bad)} mismatches; first {bad[0]} got {got[tuple(bad[0])]} ref {ref[tuple(bad[0])]}"
 
 
-@pytest.mark.parametrize("path", [1, 2, 3], ids=["promotion", "block_scaled", "pair"])
+@pytest.mark.parametrize("path", [1, 2, 3, 4], ids=["promotion", "block_scaled", "pair", "split_k"])
 @pytest.mark.parametrize("bn", [32, 64, 128, 256])
 def test_fwd_exact_pow2_block_scales(orc, ops, path, bn):
     """fwd form: 1x128 A scales and 128x128 B block scales, all powers of two,
@@ -303,3 +303,33 @@ def test_large_packed_sampled_rows(orc, ops, path):
     rows[0], rows[-1] = 0, m - 1
     ref = oracle_fwd(orc, xq, xs, wq, ws, 2, rows=rows)
     check_gemm(d[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref)
+
+
+# (m, n, k, SM budget): cluster sizes 4 and 2, ragged M/N/K, one row, K
+# ranges that start and end inside a four-K-block scale group
+SPLIT_CASES = [(64, 4096, 7168, 0), (128, 2048, 7168, 40), (200, 300, 592, 0), (1, 512, 4096, 0),
+               (64, 4096, 1024, 0), (256, 4096, 7168, 0), (96, 1000, 1920, 24), (96, 1000, 1920, 0)]
+
+
+@pytest.mark.parametrize("fmt", [1, 2], ids=["ue8m0", "packed"])
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: "x".join(map(str, c[:3])) + f"_sms{c[3]}")
+def test_split_k_cluster(orc, ops, case, fmt):
+    """Split-K over a thread-block cluster (small M): the partial tiles of S
+    CTAs summed through distributed shared memory equal the block-scaled
+    product within the GEMM tolerance, for every cluster size."""
+    m, n, k, sms = case
+    x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, fmt, w_mul=0.02, seed_x=7, seed_w=8)
+    ops.set_num_sms(sms)
+    ops.set_gemm_path(4)
+    try:
+        d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    finally:
+        ops.set_gemm_path(0)
+        ops.set_num_sms(0)
+    assert ops.device_status() == 0
+    rows = np.arange(m) if m <= 256 else np.sort(np.random.default_rng(1).choice(m, 64, replace=False))
+    ref = oracle_fwd(orc, xq, xs, wq, ws, fmt, rows=rows)
+    check_gemm(d[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref, "split-k")
+    # the default path picks the same kernel for these shapes and agrees
+    d2 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt) if sms == 0 else d
+    assert torch.equal(d, d2)
