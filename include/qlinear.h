@@ -215,6 +215,31 @@ ql_status m_grouped_gemm_fp8_nt_bf16_contiguous(const uint8_t* a, int64_t lda, c
  * ("DeepGEMM Essentials" Part 8: get_m_alignment_for_contiguous_layout): 128. */
 int ql_get_m_alignment_for_contiguous_layout(void);
 
+/* ---------------------------------------------------------------------------
+ * gemm_fp8_nt_fp8out
+ * gemm_fp8_nt_bf16 with the per-token cast of its output fused into the
+ * epilogue, so the next layer's E4M3 operand is written directly (the
+ * maintainer's advice in "[Help] Starter script for nn.Linear for fwd,bwd":
+ * fuse cast and scaling into the previous kernel's output). The result is
+ * exactly fp8_cast_per_token(Y, d_gran_k, d_fmt) of Y = the bf16 D that
+ * gemm_fp8_nt_bf16 computes with the same tiles:
+ *   d      [m, n] E4M3 at d[i*ldd + j] (ldd bytes).
+ *   d_sf   [m, ceil(n/d_gran_k)] scales, as fp8_cast_per_token's out_sf
+ *          (fp32 at d_sf[i*d_sf_stride_m + g*d_sf_stride_g]; packed UE8M0:
+ *          byte g%4 of int32 word d_sf[i*d_sf_stride_m + (g/4)*d_sf_stride_g]).
+ *   d_gran_k 32 or 128; d_fmt a ql_sf_format, optionally | QL_CAST_RECIP_OF_SCALE
+ *          with QL_SF_FP32.
+ * The other arguments and requirements are gemm_fp8_nt_bf16's; k == 0 returns
+ * QL_ERR_UNSUPPORTED. The kernels use 256-column tiles for this form.
+ * ------------------------------------------------------------------------- */
+ql_status gemm_fp8_nt_fp8out(const uint8_t* a, int64_t lda, const void* sfa,
+                             int64_t sfa_stride_m, int64_t sfa_stride_k,
+                             const uint8_t* b, int64_t ldb, const void* sfb,
+                             int64_t sfb_stride_n, int64_t sfb_stride_k, int fmt,
+                             uint8_t* d, int64_t ldd, void* d_sf, int64_t d_sf_stride_m,
+                             int64_t d_sf_stride_g, int d_gran_k, int d_fmt,
+                             int64_t m, int64_t n, int64_t k, ql_stream_t stream);
+
 /* Workspace bytes a GEMM of this shape needs (0 in this build). */
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k);
 

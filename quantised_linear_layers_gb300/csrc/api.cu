@@ -66,13 +66,15 @@ ql_status from_cuda(cudaError_t e) {
 ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sam, int64_t sak, const uint8_t* b,
                       int64_t ldb, const void* sfb, int64_t sbn, int64_t sbk, int fmt, void* d, int64_t ldd,
                       int64_t m, int64_t n, int64_t k, bool wgrad, int accumulate, cudaStream_t st,
-                      const int32_t* m_indices = nullptr, int num_groups = 1, int64_t sbg = 0) {
+                      const int32_t* m_indices = nullptr, int num_groups = 1, int64_t sbg = 0,
+                      const ql::GemmLaunch* fp8out = nullptr) {
     if (m < 0 || n < 0 || k < 0) return QL_ERR_INVALID_ARG;
     if (fmt < QL_SF_FP32 || fmt > QL_SF_PACKED_UE8M0) return QL_ERR_INVALID_ARG;
     if (m >= (int64_t(1) << 31) || n >= (int64_t(1) << 31) || k >= (int64_t(1) << 31)) return QL_ERR_UNSUPPORTED;
     if (m == 0 || n == 0) return QL_OK;
     if (d == nullptr || ldd < n) return QL_ERR_INVALID_ARG;
     const size_t es = wgrad ? 4 : 2;
+    if (k == 0 && fp8out != nullptr) return QL_ERR_UNSUPPORTED;
     if (k == 0) {
         if (wgrad && accumulate) return QL_OK;
         return from_cuda(cudaMemset2DAsync(d, static_cast<size_t>(ldd) * es, 0, static_cast<size_t>(n) * es,
@@ -112,6 +114,15 @@ ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sa
     L.m_indices = m_indices;
     L.num_groups = num_groups;
     L.sbg = sbg;
+    if (fp8out != nullptr) {
+        L.out_fp8 = true;
+        L.dsf = fp8out->dsf;
+        L.dsm = fp8out->dsm;
+        L.dsg = fp8out->dsg;
+        L.dgran = fp8out->dgran;
+        L.dfmt = fp8out->dfmt;
+        L.drecip = fp8out->drecip;
+    }
     return from_cuda(ql::launch_gemm(L, st, effective_sms(di)));
 }
 
@@ -242,6 +253,28 @@ ql_status m_grouped_gemm_fp8_nt_bf16_contiguous(const uint8_t* a, int64_t lda, c
 }
 
 int ql_get_m_alignment_for_contiguous_layout(void) { return ql::kGroupAlignM; }
+
+ql_status gemm_fp8_nt_fp8out(const uint8_t* a, int64_t lda, const void* sfa, int64_t sfa_stride_m,
+                             int64_t sfa_stride_k, const uint8_t* b, int64_t ldb, const void* sfb,
+                             int64_t sfb_stride_n, int64_t sfb_stride_k, int fmt, uint8_t* d, int64_t ldd,
+                             void* d_sf, int64_t d_sf_stride_m, int64_t d_sf_stride_g, int d_gran_k, int d_fmt,
+                             int64_t m, int64_t n, int64_t k, ql_stream_t stream) {
+    if (d_gran_k != 32 && d_gran_k != 128) return QL_ERR_INVALID_ARG;
+    const bool recip = (d_fmt & QL_CAST_RECIP_OF_SCALE) != 0;
+    const int base = d_fmt & ~QL_CAST_RECIP_OF_SCALE;
+    if (base < QL_SF_FP32 || base > QL_SF_PACKED_UE8M0) return QL_ERR_INVALID_ARG;
+    if (recip && base != QL_SF_FP32) return QL_ERR_INVALID_ARG;
+    if (m > 0 && n > 0 && d_sf == nullptr) return QL_ERR_INVALID_ARG;
+    ql::GemmLaunch o{};
+    o.dsf = d_sf;
+    o.dsm = d_sf_stride_m;
+    o.dsg = d_sf_stride_g;
+    o.dgran = d_gran_k;
+    o.dfmt = base;
+    o.drecip = recip ? 1 : 0;
+    return gemm_common(a, lda, sfa, sfa_stride_m, sfa_stride_k, b, ldb, sfb, sfb_stride_n, sfb_stride_k, fmt, d, ldd,
+                       m, n, k, false, 0, reinterpret_cast<cudaStream_t>(stream), nullptr, 1, 0, &o);
+}
 
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k) {
     (void)m;

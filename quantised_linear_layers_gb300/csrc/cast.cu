@@ -6,13 +6,8 @@
 // (Part 4). Each kernel reads its input once from HBM and writes E4M3 data and
 // scales straight into the caller's (possibly strided) views.
 //
-// Arithmetic per group (bit-exact):
-//   amax = max(|x|) in fp32 (exact), clamped below at the float nearest 1e-4
-//   fp32 scales : s = amax / 448 and f = 448 / amax, both correctly rounded
-//                 (or f = 1 / s with the recip-of-scale option)
-//   UE8M0       : s rounded up to a power of two: E = biased exponent of s,
-//                 plus one if s has any mantissa bit; f = 2^(127 - E) exactly
-//   data        : E4M3 round-to-nearest-even of fl32(x * f), sign kept
+// Arithmetic per group (bit-exact; quant.cuh): amax = max(|x|) in fp32
+// (exact), then the scale, factor and E4M3 rounding of quant.cuh.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -21,11 +16,10 @@
 #include "cast.cuh"
 #include "common.cuh"
 #include "gemm.cuh"
+#include "quant.cuh"
 
 namespace ql {
 namespace {
-
-constexpr int kSfFp32 = 0, kSfUe8m0 = 1, kSfPacked = 2;
 
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);
@@ -33,33 +27,6 @@ template <>
 __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
-
-// Scale, factor and UE8M0 exponent byte of one group from its amax.
-template <int FMT, bool RECIP>
-__device__ __forceinline__ void group_scale(float amax, float& s_store, float& f, uint32_t& ebyte) {
-    const float a = fmaxf(amax, 1e-4f);          // 1e-4f is the float nearest 1e-4
-    const float s = __fdiv_rn(a, 448.0f);
-    if constexpr (FMT == kSfFp32) {
-        s_store = s;
-        f = RECIP ? __fdiv_rn(1.0f, s) : __fdiv_rn(448.0f, a);
-        ebyte = 0;
-    } else {
-        const uint32_t b = __float_as_uint(s);   // s is a positive normal float
-        const uint32_t E = ((b >> 23) & 0xFFu) + ((b & 0x7FFFFFu) != 0u ? 1u : 0u);
-        s_store = __uint_as_float(E << 23);
-        f = __uint_as_float((254u - E) << 23);   // 2^(127 - E)
-        ebyte = E;
-    }
-}
-
-// Two fp32 values to two E4M3 bytes (lo -> low byte), round to nearest even.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
-}
-
-__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float f) {
-    return e4m3x2(__fmul_rn(a, f), __fmul_rn(b, f)) | (e4m3x2(__fmul_rn(c, f), __fmul_rn(d, f)) << 16);
-}
 
 // ---------------------------------------------------------------------------
 // Row-contiguous per-token cast (x_stride_n == 1, out_stride_n == 1).

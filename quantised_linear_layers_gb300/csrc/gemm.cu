@@ -35,6 +35,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "epilogue_fp8.cuh"
 #include "gemm.cuh"
 
 namespace ql {
@@ -175,7 +176,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl)) != 0;
 }
 
-template <int BN, bool PER_ROW_B, bool OUT_F32>
+template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmParams p) {
@@ -422,7 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- epilogue ----------------
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
             if (store_row) {
-                if constexpr (!OUT_F32) {
+                if constexpr (OUT_FP8) {
+                    static_assert(CPT == 128, "E4M3 output needs 128 columns per thread");
+                    store_row_e4m3_any(acc, row, col0, p);
+                } else if constexpr (!OUT_F32) {
                     __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
 #pragma unroll
                     for (int j = 0; j < CPT; j += 8) {
@@ -475,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, bool PER_ROW_B, bool OUT_F32>
+template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
     using Cf = Cfg<BN, PER_ROW_B>;
     CUtensorMap ta, tb;
@@ -486,7 +490,7 @@ cudaError_t launch_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
     const int tiles = p.tiles_m * p.tiles_n;
     int grid = tiles < num_sms ? tiles : num_sms;
-    auto kern = gemm_fp8_kernel<BN, PER_ROW_B, OUT_F32>;
+    auto kern = gemm_fp8_kernel<BN, PER_ROW_B, OUT_F32, OUT_FP8>;
     static bool attr_done = false;   // per instantiation
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
@@ -542,13 +546,29 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     p.num_groups = L.m_indices ? L.num_groups : 1;
     p.b_group_rows = L.n;
     p.sbg = L.sbg;
-    const int64_t es = L.out_f32 ? 4 : 2;
+    p.dsf = L.dsf;
+    p.dsm = L.dsm;
+    p.dsg = L.dsg;
+    p.dgran = L.dgran;
+    p.dfmt = L.dfmt;
+    p.drecip = L.drecip;
+    const int64_t es = L.out_fp8 ? 1 : (L.out_f32 ? 4 : 2);
     p.vec_store = ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && (L.ldd * es) % 16 == 0) ? 1 : 0;
     const int bn = L.block_n > 0 ? L.block_n : choose_block_n(L.m, L.n, num_sms);
     // UE8M0 scales (fp32 powers of two or packed exponents): promotion by the
     // tensor core's block-scaled MMA unless the CUDA-core path is requested.
     const bool ue8m0 = L.fmt == 1 || L.fmt == 2;
     const bool grouped = L.m_indices != nullptr;   // the pair kernel's two M halves share one B
+    if (L.out_fp8) {
+        // E4M3 output: 256-wide tiles, so every epilogue thread owns whole
+        // 128-column groups of its row (pair, single-SM or promotion kernel)
+        if (ue8m0 && L.path != 1) {
+            const int64_t pair_tiles = ((L.m + 255) / 256) * ((L.n + 255) / 256);
+            if (L.path == 3 || (L.path == 0 && pair_tiles >= num_sms / 2)) return launch_gemm_mx2(L, p, st, num_sms);
+            return launch_gemm_mx(L, p, 256, st, num_sms);
+        }
+        return launch_t<256, false, false, true>(L, p, st, num_sms);
+    }
     if (ue8m0 && L.path == 3 && !grouped) return launch_gemm_mx2(L, p, st, num_sms);
     const int split = (ue8m0 && !grouped && !L.out_f32) ? choose_split_k(L.m, L.n, L.k, num_sms) : 1;
     if (L.path == 4 && split >= 2) return launch_gemm_mx_sk(L, p, split, st);

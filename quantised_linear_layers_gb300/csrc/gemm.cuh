@@ -30,6 +30,12 @@ struct GemmParams {
     int num_groups;
     int64_t b_group_rows;     // rows of B per expert (n) in B's tensor map
     int64_t sbg;              // sfb elements (or packed words) between experts
+    // E4M3 output with per-token scales (the GEMM kernels' OUT_FP8 form)
+    void* dsf;
+    int64_t dsm, dsg;
+    int dgran;                // 32 or 128
+    int dfmt;                 // 0 fp32, 1 UE8M0 (fp32 powers of two), 2 packed UE8M0
+    int drecip;               // fp32 scales: factor 1 / s
 };
 
 // Host-side description of one GEMM call.
@@ -59,6 +65,10 @@ struct GemmLaunch {
     const int* m_indices;     // M-grouped contiguous layout (nullptr: plain GEMM)
     int num_groups;
     int64_t sbg;
+    bool out_fp8;             // E4M3 output + per-token scales (fwd form only)
+    void* dsf;
+    int64_t dsm, dsg;
+    int dgran, dfmt, drecip;
 };
 
 // Rows of A per M tile; in the M-grouped contiguous layout every expert's

@@ -34,6 +34,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "epilogue_fp8.cuh"
 #include "gemm.cuh"
 
 namespace ql {
@@ -115,7 +116,7 @@ __device__ __forceinline__ void exp_words(const void* base, int fmt, const int64
     }
 }
 
-template <int BN, bool PER_ROW_B, bool OUT_F32>
+template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const GemmParams p) {
@@ -363,7 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&tempty[as]);
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
             if (store_row) {
-                if constexpr (!OUT_F32) {
+                if constexpr (OUT_FP8) {
+                    static_assert(CPT == 128, "E4M3 output needs 128 columns per thread");
+                    store_row_e4m3_any(acc, row, col0, p);
+                } else if constexpr (!OUT_F32) {
                     __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
 #pragma unroll
                     for (int j = 0; j < CPT; j += 8) {
@@ -416,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, bool PER_ROW_B, bool OUT_F32>
+template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_mx_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
     using Cf = MxCfg<BN>;
     CUtensorMap ta, tb;
@@ -427,7 +431,7 @@ cudaError_t launch_mx_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int 
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    auto kern = gemm_mx_kernel<BN, PER_ROW_B, OUT_F32>;
+    auto kern = gemm_mx_kernel<BN, PER_ROW_B, OUT_F32, OUT_FP8>;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
@@ -451,6 +455,7 @@ cudaError_t dispatch_mx(int bn, const GemmLaunch& L, const GemmParams& p, cudaSt
 }  // namespace
 
 cudaError_t launch_gemm_mx(const GemmLaunch& L, const GemmParams& p, int bn, cudaStream_t st, int num_sms) {
+    if (L.out_fp8) return launch_mx_t<256, false, false, true>(L, p, st, num_sms);
     if (L.out_f32) return dispatch_mx<true, true>(bn, L, p, st, num_sms);
     return dispatch_mx<false, false>(bn, L, p, st, num_sms);
 }

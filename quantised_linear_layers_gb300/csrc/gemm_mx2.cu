@@ -30,6 +30,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "epilogue_fp8.cuh"
 #include "gemm.cuh"
 
 namespace ql {
@@ -105,7 +106,7 @@ __device__ __forceinline__ void exp_words(const void* base, int fmt, const int64
     }
 }
 
-template <bool PER_ROW_B, bool OUT_F32>
+template <bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmParams p) {
@@ -352,7 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + r_local;
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
             if (row < p.m) {
-                if constexpr (!OUT_F32) {
+                if constexpr (OUT_FP8) {
+                    store_row_e4m3_any(acc, row, col0, p);
+                } else if constexpr (!OUT_F32) {
                     __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
 #pragma unroll
                     for (int j = 0; j < CPT; j += 8) {
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool PER_ROW_B, bool OUT_F32>
+template <bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
     using Cf = Mx2Cfg;
     CUtensorMap ta, tb;
@@ -434,7 +437,7 @@ cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int
     int pairs = num_sms / 2;
     if (pairs < 1) pairs = 1;
     if (tiles < pairs) pairs = tiles;
-    auto kern = gemm_mx2_kernel<PER_ROW_B, OUT_F32>;
+    auto kern = gemm_mx2_kernel<PER_ROW_B, OUT_F32, OUT_FP8>;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
@@ -470,6 +473,7 @@ cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int
 }  // namespace
 
 cudaError_t launch_gemm_mx2(const GemmLaunch& L, const GemmParams& p, cudaStream_t st, int num_sms) {
+    if (L.out_fp8) return launch_mx2_t<false, false, true>(L, p, st, num_sms);
     if (L.out_f32) return launch_mx2_t<true, true>(L, p, st, num_sms);
     return launch_mx2_t<false, false>(L, p, st, num_sms);
 }

@@ -35,6 +35,8 @@ _SIGS = {
     "m_grouped_gemm_fp8_nt_bf16_contiguous": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _i64,
                                               _int, _vp, _i64, _vp, _int, _i64, _i64, _i64, _vp],
     "ql_get_m_alignment_for_contiguous_layout": [],
+    "gemm_fp8_nt_fp8out": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64, _vp, _i64,
+                           _i64, _int, _int, _i64, _i64, _i64, _vp],
     "ql_gemm_workspace_size": [_i64, _i64, _i64],
     "ql_set_num_sms": [_int],
     "ql_get_num_sms": [],
@@ -192,6 +194,30 @@ def gemm_fp8_nt_bf16(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: t
         fmt, out.data_ptr(), out.stride(0), m, n, k, None, 0, _stream(a))
     _check("gemm_fp8_nt_bf16", st)
     return out
+
+
+def gemm_fp8_nt_fp8out(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor,
+                       fmt: int = SF_FP32, gran_k: int = 128, out_fmt: int = SF_FP32, recip: bool = False,
+                       out: torch.Tensor | None = None, out_sf: torch.Tensor | None = None,
+                       sf_mn_major: bool = False):
+    """D = A B^T cast per token inside the GEMM: returns (E4M3 [m, n], scales),
+    equal to fp8_cast_per_token(gemm_fp8_nt_bf16(...), gran_k, out_fmt)."""
+    m, n, k = _gemm_args(a, sfa, b, sfb)
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float8_e4m3fn, device=a.device)
+    _bytes8(out)
+    if out.stride(1) != 1:
+        raise ValueError("out must have contiguous rows")
+    if out_sf is None:
+        out_sf = empty_sf(m, sf_shape(n, gran_k, out_fmt), out_fmt, a.device, mn_major=sf_mn_major)
+    code = out_fmt | (CAST_RECIP_OF_SCALE if recip else 0)
+    st = load_library().gemm_fp8_nt_fp8out(
+        a.data_ptr(), a.stride(0), sfa.data_ptr(), sfa.stride(0), sfa.stride(1),
+        b.data_ptr(), b.stride(0), sfb.data_ptr(), sfb.stride(0), sfb.stride(1),
+        fmt, out.data_ptr(), out.stride(0), out_sf.data_ptr(), out_sf.stride(0), out_sf.stride(1),
+        gran_k, code, m, n, k, _stream(a))
+    _check("gemm_fp8_nt_fp8out", st)
+    return out, out_sf
 
 
 def gemm_fp8_wgrad_fp32(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor,

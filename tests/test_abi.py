@@ -98,6 +98,13 @@ def test_host_validation_rejects_before_cuda(lib):
     assert G(p, 32, p, 1, 1, p, 32, p, 1, 1, 1, 0, p, 8, p, 2, 128, 8, 0, None) == 2
     assert G(None, 32, None, 1, 1, None, 32, None, 1, 1, 1, 0, None, 8, None, 2, 0, 8, 32, None) == 0
     assert L.ql_get_m_alignment_for_contiguous_layout() == 128
+    # GEMM with E4M3 output: group 64, unknown format, recip with UE8M0, no scale buffer, k == 0
+    F = L.gemm_fp8_nt_fp8out
+    assert F(p, 32, p, 1, 1, p, 32, p, 1, 1, 0, p, 32, p, 1, 1, 64, 0, 4, 8, 32, None) == 1
+    assert F(p, 32, p, 1, 1, p, 32, p, 1, 1, 0, p, 32, p, 1, 1, 128, 5, 4, 8, 32, None) == 1
+    assert F(p, 32, p, 1, 1, p, 32, p, 1, 1, 0, p, 32, p, 1, 1, 128, 0x101, 4, 8, 32, None) == 1
+    assert F(p, 32, p, 1, 1, p, 32, p, 1, 1, 0, p, 32, None, 1, 1, 128, 0, 4, 8, 32, None) == 1
+    assert F(p, 32, p, 1, 1, p, 32, p, 1, 1, 0, p, 32, p, 1, 1, 128, 0, 4, 8, 0, None) == 2
     assert L.ql_set_gemm_block_n(48) == 1
     assert L.ql_set_wait_limit_ms(0) == 1
 
