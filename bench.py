@@ -423,7 +423,8 @@ def run_workloads(dev, pk, reps):
     (median of `reps`):
 
     - forward GEMM N=4096, K=7168 at M = 64, 128 (HBM-bound: W's bytes
-      dominate) and 4096 (tensor-bound), L2 flushed before each repetition;
+      dominate) and 4096 (tensor-bound), L2 flushed before each repetition,
+      and at M = 64, 128 as 32 GEMMs back to back over 8 distinct weights;
     - the Linear layer's step, X [4096, 7168], dY [4096, 4096], W [4096, 7168]:
       weight casts (W and W^T, 128x128), forward (cast X + GEMM), dgrad (cast dY
       + GEMM against W^T), wgrad (transposed casts of dY and X + fp32 GEMM),
@@ -431,6 +432,8 @@ def run_workloads(dev, pk, reps):
     - the low-latency per-token cast (hidden 4096, group 32, packed UE8M0) at
       1, 64 and 512 tokens: eager with a flushed L2, and the device time per
       cast inside a captured CUDA graph of 50 casts;
+    - a GEMM whose output feeds the next FP8 layer: bf16 output plus the
+      per-token cast, against the cast fused into the GEMM's epilogue;
     - the M-grouped contiguous GEMM of a mixture-of-experts layer: 8 experts
       of about 2048 tokens each, N=4096, K=7168, L2 flushed.
     Returns (dict, number of this library's kernel launches timed).
@@ -459,6 +462,7 @@ def run_workloads(dev, pk, reps):
                      "tflops": round(fl / ms / 1e9, 1), "gbs": round(byts / ms / 1e6, 1),
                      "frac_hbm": round(byts / ms / 1e6 / pk["hbm_gbs"], 3)})
     out["gemm_fwd_n4096_k7168_cold_l2"] = rows
+
 
 
     x = syn.randn((4096, 7168), seed=syn.SEED_X, device=str(dev))
@@ -491,6 +495,35 @@ def run_workloads(dev, pk, reps):
         "us_step": round(step * 1e3, 1), "tflops_step": round(3 * fl / step / 1e9, 1),
         "tflops_without_weight_casts": round(3 * fl / (step - part[0]) / 1e9, 1)}
     del x, dy, w8, w, wq, ws
+
+    # GEMM whose output feeds the next FP8 layer: bf16 output then the
+    # per-token cast, against the cast fused into the GEMM's epilogue
+    # (Y = X W^T with X [4096, 4096], W [7168, 4096]; 1x128 packed output)
+    xa = syn.randn((4096, 4096), seed=syn.SEED_X, device=str(dev))
+    xaq, xas = ops.fp8_cast_per_token(xa, 128, P, sf_mn_major=True)
+    wb = syn.randn((7168, 4096), seed=syn.SEED_W, mul=0.02, device=str(dev))
+    wbq, wbs = ops.fp8_cast_per_block(wb, P)
+    del xa, wb
+    y = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
+    yq = torch.empty((4096, 7168), dtype=torch.float8_e4m3fn, device=dev)
+    ys = ops.empty_sf(4096, ops.sf_shape(7168, 128, P), P, dev, mn_major=True)
+
+    def unfused():
+        ops.gemm_fp8_nt_bf16(xaq, xas, wbq, wbs, P, out=y)
+        ops.fp8_cast_per_token(y, 128, P, out=yq, out_sf=ys)
+
+    def fused():
+        ops.gemm_fp8_nt_fp8out(xaq, xas, wbq, wbs, P, 128, P, out=yq, out_sf=ys)
+
+    t_un = _median_ms(unfused, reps, flush)
+    t_fu = _median_ms(fused, reps, flush)
+    launches += 3 * reps
+    fl = 2 * 4096 * 7168 * 4096
+    out["gemm_cast_fused_4096x7168x4096_cold_l2"] = {
+        "us_gemm_bf16_then_cast": round(t_un * 1e3, 1), "us_fused": round(t_fu * 1e3, 1),
+        "tflops_unfused": round(fl / t_un / 1e9, 1), "tflops_fused": round(fl / t_fu / 1e9, 1),
+        "hbm_bytes_saved": 4096 * 7168 * 2 * 2}
+    del xaq, xas, wbq, wbs, y, yq, ys
 
     rows = []
     G = 50
@@ -542,6 +575,29 @@ def run_workloads(dev, pk, reps):
         "tokens": tokens, "m_aligned": mg, "us": round(ms * 1e3, 1), "tflops_valid_rows": round(fl / ms / 1e9, 1),
         "tflops_incl_padding": round(2 * mg * 4096 * 7168 / ms / 1e9, 1)}
     del xgq, xgs, wg, wgs, dg
+
+    # small M back to back, as in decoding: 32 GEMMs in a row over 8 distinct
+    # weights (8 x 29.4 MB > L2), one event pair around the sequence
+    wcopies = [ops.fp8_cast_per_block(syn.randn((4096, 7168), seed=200 + i, mul=0.02, device=str(dev)), P)
+               for i in range(8)]
+    rows = []
+    for m in (64, 128):
+        x = syn.randn((m, 7168), seed=syn.SEED_X, device=str(dev))
+        xq, xs = ops.fp8_cast_per_token(x, 128, P, sf_mn_major=True)
+        d = torch.empty((m, 4096), dtype=torch.bfloat16, device=dev)
+
+        def seq():
+            for _ in range(4):
+                for wq_i, ws_i in wcopies:
+                    ops.gemm_fp8_nt_bf16(xq, xs, wq_i, ws_i, P, out=d)
+
+        ms = _median_ms(seq, max(3, reps // 4)) / 32
+        launches += 32 * max(3, reps // 4)
+        byts = m * 7168 + 4096 * 7168 + m * 4096 * 2 + 4 * (m + 4096 // 128) * (7168 // 512)
+        rows.append({"m": m, "us_per_gemm": round(ms * 1e3, 2), "gbs": round(byts / ms / 1e6, 1),
+                     "frac_hbm": round(byts / ms / 1e6 / pk["hbm_gbs"], 3)})
+    out["gemm_fwd_small_m_back_to_back_8_weights"] = rows
+    del wcopies
     assert ops.device_status() == 0
     return out, launches
 
