@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(256, 4) cast_rows_kernel(const T* __restrict__
                                                         uint8_t* __restrict__ out, int64_t ldo,
                                                         void* __restrict__ sf, int64_t ssm, int64_t ssg,
                                                         int64_t chunks_per_row, int vec_in, int vec_out) {
+    pdl_launch_dependents();    // a dependent GEMM may start its prologue
     constexpr int kElemsPerLane = 64 / sizeof(T);          // 32 (bf16) or 16 (fp32)
     constexpr int kChunk = 32 * kElemsPerLane;
     constexpr int kLanesPerGroup = GRAN / kElemsPerLane;   // 1, 2, 4 or 8
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(256, 1) cast_cols_kernel(const T* __restrict__
                                                            uint8_t* __restrict__ out, int64_t ldo,
                                                            void* __restrict__ sf, int64_t ssm, int64_t ssg,
                                                            int vec_in, int vec_out) {
+    pdl_launch_dependents();    // a dependent GEMM may start its prologue
     constexpr int V = 16 / sizeof(T);          // 8 (bf16) or 4 (fp32)
     constexpr int WI = 4 * V;                  // logical rows per warp
     constexpr int WJ = 128;                    // group-axis extent of a subtile
@@ -279,6 +281,7 @@ __global__ void __launch_bounds__(96) cast_cols_tma_kernel(const __grid_constant
                                                           int64_t n, uint8_t* __restrict__ out, int64_t ldo,
                                                           void* __restrict__ sf, int64_t ssm, int64_t ssg,
                                                           int vec_out, uint32_t* dev_status, uint64_t limit_ns) {
+    pdl_launch_dependents();    // a dependent GEMM may start its prologue
     using namespace cols_tma;
     constexpr int V = 16 / sizeof(T);
     constexpr int BI = 128 / sizeof(T);        // columns per box
@@ -427,6 +430,7 @@ __global__ void __launch_bounds__(128) cast_generic_kernel(const T* __restrict__
                                                            int64_t sxm, int64_t sxn, uint8_t* __restrict__ out,
                                                            int64_t som, int64_t son, void* __restrict__ sf,
                                                            int64_t ssm, int64_t ssg) {
+    pdl_launch_dependents();    // a dependent GEMM may start its prologue
     const int64_t G = (n + GRAN - 1) / GRAN;
     const int64_t W = (G + 3) / 4;
     const int64_t total = m * W;
@@ -467,6 +471,7 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
                                                          uint8_t* __restrict__ out, int64_t som, int64_t son,
                                                          int out_mode, void* __restrict__ sf, int64_t ssr,
                                                          int64_t ssc) {
+    pdl_launch_dependents();    // a dependent GEMM may start its prologue
     constexpr int B = 128;
     // E4M3 bytes of the block, [row][col] with a row pitch of 144 bytes (16-byte
     // rows: 8-byte stores, 16-byte loads) for row-contiguous input, or 129 bytes

@@ -452,6 +452,16 @@ __device__ __forceinline__ void regs_alloc() {
 }
 
 // Named barrier among `nthreads` threads (a multiple of 32).
+// Programmatic dependent launch. launch_dependents lets the next kernel of the
+// stream (launched with programmatic stream serialization) be scheduled once
+// every CTA of this grid has issued it or exited; wait_prior blocks until the
+// previous kernel of the stream has completed and its memory is visible. Both
+// are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -208,12 +208,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmap_a); tma_prefetch_desc(&tmap_b); }
+    pdl_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+        // the first tile's first weight tiles into L2 while the previous kernel finishes
+        if (p.m_indices == nullptr && static_cast<int>(blockIdx.x) < p.tiles_m * p.tiles_n) {
+            int mb0, nb0;
+            tile_coords(blockIdx.x, p, mb0, nb0);
+            for (int kb = 0; kb < p.num_kb && kb < C::kStages; ++kb) tma_prefetch_l2_2d(&tmap_b, kb * BK, nb0 * BN);
+        }
+    }
     if (warp == 1) { tmem_alloc(tmem_base_sm, C::kTmemCols); tmem_relinquish(); }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_base_sm;
+    pdl_wait_prior();            // inputs of the previous kernel are complete from here on
 
     const WaitCtl ctl{abort_flag, p.dev_status, p.wait_limit_ns};
     const int num_tiles = p.tiles_m * p.tiles_n;
@@ -497,8 +508,7 @@ cudaError_t launch_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    kern<<<grid, kThreads, Cf::kSmemBytes, st>>>(ta, tb, p);
-    return cudaGetLastError();
+    return launch_gemm_kernel(kern, static_cast<unsigned>(grid), 1, Cf::kSmemBytes, st, ta, tb, p);
 }
 
 template <bool PER_ROW_B, bool OUT_F32>

@@ -108,6 +108,36 @@ __device__ __forceinline__ bool row_in_expert_quiet(const GemmParams& p, int64_t
 }
 #endif
 
+// Launch of a GEMM kernel (384 threads, two tensor maps and the parameters)
+// with programmatic stream serialization, so its prologue and the L2
+// prefetch of its first weight tiles overlap the previous kernel's tail; the
+// kernel waits for the previous kernel before it reads any input. `cluster`
+// > 1 adds a cluster dimension.
+template <typename Kern>
+inline cudaError_t launch_gemm_kernel(Kern kern, unsigned grid, unsigned cluster, size_t smem, cudaStream_t st,
+                                      const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(384, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+}
+
 int choose_block_n(int64_t m, int64_t n, int num_sms);
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms);
 cudaError_t launch_gemm_mx(const GemmLaunch& L, const GemmParams& p, int bn, cudaStream_t st, int num_sms);

@@ -151,12 +151,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmap_a); tma_prefetch_desc(&tmap_b); }
+    pdl_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+        // the first tile's first weight tiles (this CTA's half) into L2 while the
+        // previous kernel finishes
+        if (cid < p.tiles_m * p.tiles_n) {
+            int mb0, nb0;
+            tile_coords(cid, p, mb0, nb0);
+            for (int kb = 0; kb < p.num_kb && kb < C::kStages; ++kb)
+                tma_prefetch_l2_2d(&tmap_b, kb * BK, nb0 * BN + static_cast<int>(rank) * BNH);
+        }
+    }
     if (warp == 1) { tmem_alloc_pair(tmem_base_sm, C::kTmemCols); tmem_relinquish_pair(); }
     tc_fence_before_sync();
     cluster_sync_all();          // barriers of both CTAs initialised before any remote arrive
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_base_sm;
+    pdl_wait_prior();            // inputs of the previous kernel are complete from here on
 
     const WaitCtl ctl{abort_flag, p.dev_status, p.wait_limit_ns};
     const int num_tiles = p.tiles_m * p.tiles_n;     // pair tiles of 256 x 256
@@ -467,7 +480,7 @@ cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int
         pairs = max_pairs;
         cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     }
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+    return launch_gemm_kernel(kern, cfg.gridDim.x, 2, Cf::kSmemBytes, st, ta, tb, p);
 }
 
 }  // namespace

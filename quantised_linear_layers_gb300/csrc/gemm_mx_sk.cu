@@ -159,12 +159,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // armed before the cluster barrier that precedes any copy into this CTA
         mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(split - 1) * slice_bytes);
     }
-    if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmap_a); tma_prefetch_desc(&tmap_b); }
+    pdl_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+        // this CTA's first weight tiles into L2 while the previous kernel finishes
+        for (int kb = kb0; kb < kb1 && kb < kb0 + C::kStages; ++kb) tma_prefetch_l2_2d(&tmap_b, kb * BK, nb * BN);
+    }
     if (warp == 1) { tmem_alloc(tmem_base_sm, C::kTmemCols); tmem_relinquish(); }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_base_sm;
+    pdl_wait_prior();            // inputs of the previous kernel are complete from here on
     const WaitCtl ctl{abort_flag, p.dev_status, p.wait_limit_ns};
     const int num_kb = p.num_kb;
 
@@ -416,19 +423,8 @@ cudaError_t launch_gemm_mx_sk(const GemmLaunch& L, GemmParams p, int split, cuda
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles * split), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cf::kSmemBytes;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+    return launch_gemm_kernel(kern, static_cast<unsigned>(tiles * split), static_cast<unsigned>(split), Cf::kSmemBytes,
+                              st, ta, tb, p);
 }
 
 }  // namespace ql
