@@ -428,7 +428,8 @@ def run_workloads(dev, pk, reps):
     - the Linear layer's step, X [4096, 7168], dY [4096, 4096], W [4096, 7168]:
       weight casts (W and W^T, 128x128), forward (cast X + GEMM), dgrad (cast dY
       + GEMM against W^T), wgrad (transposed casts of dY and X + fp32 GEMM),
-      L2 flushed before each step;
+      L2 flushed before each step; and its weight gradient with the operands
+      cast from transposed views against cast in place and read MN-major;
     - the low-latency per-token cast (hidden 4096, group 32, packed UE8M0) at
       1, 64 and 512 tokens: eager with a flushed L2, and the device time per
       cast inside a captured CUDA graph of 50 casts;
@@ -494,6 +495,12 @@ def run_workloads(dev, pk, reps):
         "us_dgrad": round(part[2] * 1e3, 1), "us_wgrad": round(part[3] * 1e3, 1),
         "us_step": round(step * 1e3, 1), "tflops_step": round(3 * fl / step / 1e9, 1),
         "tflops_without_weight_casts": round(3 * fl / (step - part[0]) / 1e9, 1)}
+    # the weight gradient with transposed casts against MN-major operands
+    t_tr = _median_ms(lambda: linear.wgrad(dy, x, P), reps, flush)
+    t_mn = _median_ms(lambda: linear.wgrad(dy, x, P, mn_major=True), reps, flush)
+    launches += 6 * reps
+    out["wgrad_transposed_vs_mn_major_4096x7168x4096"] = {
+        "us_transposed_casts": round(t_tr * 1e3, 1), "us_mn_major": round(t_mn * 1e3, 1)}
     del x, dy, w8, w, wq, ws
 
     # GEMM whose output feeds the next FP8 layer: bf16 output then the

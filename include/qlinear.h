@@ -240,6 +240,42 @@ ql_status gemm_fp8_nt_fp8out(const uint8_t* a, int64_t lda, const void* sfa,
                              int64_t d_sf_stride_g, int d_gran_k, int d_fmt,
                              int64_t m, int64_t n, int64_t k, ql_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * gemm_fp8_wgrad_fp32_mn
+ * gemm_fp8_wgrad_fp32 with both operands MN-major: A stored [k][m] and B
+ * stored [k][n] (K = tokens outermost, row strides lda / ldb bytes), i.e. the
+ * E4M3 casts of dY [T, out] and X [T, in] kept in their own layout, so the
+ * weight gradient of "[Help] Starter script for nn.Linear for fwd,bwd" needs
+ * no transposed copies. Scales are those of gemm_fp8_wgrad_fp32 (1x128 along
+ * K for every row of A and of B): fp8_cast_per_token of dY^T written into a
+ * transposed output view produces both data and scales in this form.
+ * Requirements: a, b 16-byte aligned; lda, ldb multiples of 16, lda >= m,
+ * ldb >= n (QL_ERR_ALIGNMENT / QL_ERR_INVALID_ARG otherwise).
+ * ------------------------------------------------------------------------- */
+ql_status gemm_fp8_wgrad_fp32_mn(const uint8_t* a, int64_t lda, const void* sfa,
+                                 int64_t sfa_stride_m, int64_t sfa_stride_k,
+                                 const uint8_t* b, int64_t ldb, const void* sfb,
+                                 int64_t sfb_stride_n, int64_t sfb_stride_k,
+                                 int fmt, float* d, int64_t ldd,
+                                 int64_t m, int64_t n, int64_t k, int accumulate, ql_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gemm_fp8_nn_bf16
+ * gemm_fp8_nt_bf16 with B MN-major: B stored [k][n] (row stride ldb bytes),
+ * D = A * B. For the data gradient dX = dY * W of "[Help] Starter script for
+ * nn.Linear for fwd,bwd", B is W's own E4M3 cast [out, in] and its 128x128
+ * block grid read transposed (sfb row r = block column r of W's grid), so no
+ * cast of W^T is needed. sfb: [ceil(n/128), ceil(k/128)] at
+ * sfb[r*sfb_stride_n + kb*sfb_stride_k] (packed UE8M0: words along K).
+ * Requirements: as gemm_fp8_nt_bf16, with ldb >= n.
+ * ------------------------------------------------------------------------- */
+ql_status gemm_fp8_nn_bf16(const uint8_t* a, int64_t lda, const void* sfa,
+                           int64_t sfa_stride_m, int64_t sfa_stride_k,
+                           const uint8_t* b, int64_t ldb, const void* sfb,
+                           int64_t sfb_stride_n, int64_t sfb_stride_k,
+                           int fmt, uint16_t* d, int64_t ldd,
+                           int64_t m, int64_t n, int64_t k, ql_stream_t stream);
+
 /* Workspace bytes a GEMM of this shape needs (0 in this build). */
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k);
 

@@ -67,7 +67,7 @@ ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sa
                       int64_t ldb, const void* sfb, int64_t sbn, int64_t sbk, int fmt, void* d, int64_t ldd,
                       int64_t m, int64_t n, int64_t k, bool wgrad, int accumulate, cudaStream_t st,
                       const int32_t* m_indices = nullptr, int num_groups = 1, int64_t sbg = 0,
-                      const ql::GemmLaunch* fp8out = nullptr) {
+                      const ql::GemmLaunch* fp8out = nullptr, bool a_mn = false, bool b_mn = false) {
     if (m < 0 || n < 0 || k < 0) return QL_ERR_INVALID_ARG;
     if (fmt < QL_SF_FP32 || fmt > QL_SF_PACKED_UE8M0) return QL_ERR_INVALID_ARG;
     if (m >= (int64_t(1) << 31) || n >= (int64_t(1) << 31) || k >= (int64_t(1) << 31)) return QL_ERR_UNSUPPORTED;
@@ -81,7 +81,8 @@ ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sa
                                            static_cast<size_t>(m), st));
     }
     if (a == nullptr || b == nullptr || sfa == nullptr || sfb == nullptr) return QL_ERR_INVALID_ARG;
-    if (lda < k || ldb < k) return QL_ERR_INVALID_ARG;
+    // a K-major operand has rows of k bytes; an MN-major one rows of m (or n) bytes
+    if (lda < (a_mn ? m : k) || ldb < (b_mn ? n : k)) return QL_ERR_INVALID_ARG;
     if (!aligned16(a) || !aligned16(b) || lda % 16 != 0 || ldb % 16 != 0) return QL_ERR_ALIGNMENT;
     DeviceInfo di;
     ql_status s = device_info(di);
@@ -114,6 +115,8 @@ ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sa
     L.m_indices = m_indices;
     L.num_groups = num_groups;
     L.sbg = sbg;
+    L.a_mn = a_mn;
+    L.b_mn = b_mn;
     if (fp8out != nullptr) {
         L.out_fp8 = true;
         L.dsf = fp8out->dsf;
@@ -253,6 +256,24 @@ ql_status m_grouped_gemm_fp8_nt_bf16_contiguous(const uint8_t* a, int64_t lda, c
 }
 
 int ql_get_m_alignment_for_contiguous_layout(void) { return ql::kGroupAlignM; }
+
+ql_status gemm_fp8_wgrad_fp32_mn(const uint8_t* a, int64_t lda, const void* sfa, int64_t sfa_stride_m,
+                                 int64_t sfa_stride_k, const uint8_t* b, int64_t ldb, const void* sfb,
+                                 int64_t sfb_stride_n, int64_t sfb_stride_k, int fmt, float* d, int64_t ldd,
+                                 int64_t m, int64_t n, int64_t k, int accumulate, ql_stream_t stream) {
+    return gemm_common(a, lda, sfa, sfa_stride_m, sfa_stride_k, b, ldb, sfb, sfb_stride_n, sfb_stride_k, fmt, d, ldd,
+                       m, n, k, true, accumulate, reinterpret_cast<cudaStream_t>(stream), nullptr, 1, 0, nullptr,
+                       true, true);
+}
+
+ql_status gemm_fp8_nn_bf16(const uint8_t* a, int64_t lda, const void* sfa, int64_t sfa_stride_m,
+                           int64_t sfa_stride_k, const uint8_t* b, int64_t ldb, const void* sfb,
+                           int64_t sfb_stride_n, int64_t sfb_stride_k, int fmt, uint16_t* d, int64_t ldd, int64_t m,
+                           int64_t n, int64_t k, ql_stream_t stream) {
+    return gemm_common(a, lda, sfa, sfa_stride_m, sfa_stride_k, b, ldb, sfb, sfb_stride_n, sfb_stride_k, fmt, d, ldd,
+                       m, n, k, false, 0, reinterpret_cast<cudaStream_t>(stream), nullptr, 1, 0, nullptr, false,
+                       true);
+}
 
 ql_status gemm_fp8_nt_fp8out(const uint8_t* a, int64_t lda, const void* sfa, int64_t sfa_stride_m,
                              int64_t sfa_stride_k, const uint8_t* b, int64_t ldb, const void* sfb,

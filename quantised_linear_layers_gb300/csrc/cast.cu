@@ -422,6 +422,134 @@ __global__ void __launch_bounds__(96) cast_cols_tma_kernel(const __grid_constant
 }
 
 // ---------------------------------------------------------------------------
+// Column-major per-token cast (x_stride_m == 1 and out_stride_m == 1): the
+// logical row i is a column of the physical array P[j][i], and the cast's
+// output is written in the same physical layout (Q[j][i]), e.g. dY [T, C]
+// cast with 1x128 groups along T for the weight gradient, read by the GEMM as
+// an MN-major operand, so nothing is transposed in memory. One CTA (16 warps)
+// covers 128 physical rows (j) x 32*V columns (i), V = 8 bytes of input per
+// lane; warp w takes rows 8w .. 8w+8 and lane l columns l*V .. l*V+V of each,
+// so every load and store of a warp is one contiguous run of a physical row.
+// Column amaxes are combined over the warps of a group through shared memory.
+// 16 registers of input per thread keep two CTAs (32 warps) on each SM.
+// ---------------------------------------------------------------------------
+namespace colmajor {
+constexpr int kWarps = 16;
+constexpr int kRowsPerWarp = 8;
+constexpr int kLaneBytes = 8;
+}  // namespace colmajor
+
+template <typename T, int GRAN, int FMT, bool RECIP>
+__global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restrict__ x, int64_t m, int64_t n,
+                                                               int64_t ldx, uint8_t* __restrict__ out, int64_t ldo,
+                                                               void* __restrict__ sf, int64_t ssm, int64_t ssg,
+                                                               int vec_in, int vec_out) {
+    pdl_launch_dependents();    // a dependent GEMM may start its prologue
+    using namespace colmajor;
+    constexpr int V = kLaneBytes / sizeof(T);       // columns per lane (4 bf16 or 2 fp32)
+    constexpr int R = kRowsPerWarp;
+    constexpr int WPG = GRAN / R;                   // warps per group (16 or 4)
+    constexpr int NG = kWarps / WPG;                // groups per tile (1 or 4)
+    __shared__ float red[kWarps][32][V + 1];
+    __shared__ uint32_t ebuf[NG][32][V];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * 32 * V + lane * V;   // first logical row of this lane
+    const int64_t jt = static_cast<int64_t>(blockIdx.y) * (kWarps * R);        // first physical row of the tile
+    const int64_t j0 = jt + warp * R;
+    const int64_t G = (n + GRAN - 1) / GRAN;
+
+    uint2 raw[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t j = j0 + r;
+        const T* src = x + j * ldx + i0;
+        if (j < n && vec_in && i0 + V <= m) {
+            raw[r] = __ldg(reinterpret_cast<const uint2*>(src));
+        } else {
+            T t[V];
+#pragma unroll
+            for (int c = 0; c < V; ++c) t[c] = (j < n && i0 + c < m) ? src[c] : T(0.0f);
+            raw[r] = *reinterpret_cast<const uint2*>(t);
+        }
+    }
+    {
+        float amax[V];
+#pragma unroll
+        for (int c = 0; c < V; ++c) amax[c] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const T* t = reinterpret_cast<const T*>(&raw[r]);
+#pragma unroll
+            for (int c = 0; c < V; ++c) amax[c] = fmaxf(amax[c], fabsf(to_f32(t[c])));
+        }
+#pragma unroll
+        for (int c = 0; c < V; ++c) red[warp][lane][c] = amax[c];
+    }
+    __syncthreads();
+    const int w0 = (warp / WPG) * WPG;              // first warp of this warp's group
+    const int64_t g = (jt + w0 * R) / GRAN;         // this warp's group index along j
+    const bool group_lead = warp == w0;
+    float f[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+        float a = red[w0][lane][c];
+#pragma unroll
+        for (int w = 1; w < WPG; ++w) a = fmaxf(a, red[w0 + w][lane][c]);
+        float sc;
+        uint32_t eb;
+        group_scale<FMT, RECIP>(a, sc, f[c], eb);
+        const int64_t i = i0 + c;
+        if constexpr (FMT != kSfPacked) {
+            if (group_lead && i < m && g < G) static_cast<float*>(sf)[i * ssm + g * ssg] = sc;
+        } else if constexpr (GRAN == 128) {
+            if (group_lead && i < m && g < G) {
+                uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + i * ssm + (g / 4) * ssg);
+                word[g % 4] = static_cast<uint8_t>(eb);
+                if (g == G - 1)
+                    for (int z = static_cast<int>(g % 4) + 1; z < 4; ++z) word[z] = 0;
+            }
+        } else {
+            if (group_lead) ebuf[warp / WPG][lane][c] = (g < G) ? eb : 0u;
+        }
+    }
+    // quantise: row r of this lane -> V bytes at Q[j0 + r][i0 .. i0+V)
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t j = j0 + r;
+        if (j >= n) break;
+        const T* t = reinterpret_cast<const T*>(&raw[r]);
+        uint8_t* dst = out + j * ldo + i0;
+        uint32_t w = e4m3x2(__fmul_rn(to_f32(t[0]), f[0]), __fmul_rn(to_f32(t[1]), f[1]));
+        if constexpr (V == 4)
+            w |= e4m3x2(__fmul_rn(to_f32(t[2]), f[2]), __fmul_rn(to_f32(t[3]), f[3])) << 16;
+        if (vec_out && i0 + V <= m) {
+            if constexpr (V == 4) *reinterpret_cast<uint32_t*>(dst) = w;
+            else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w);
+        } else {
+#pragma unroll
+            for (int c = 0; c < V; ++c)
+                if (i0 + c < m) dst[c] = static_cast<uint8_t>(w >> (8 * c));
+        }
+    }
+    if constexpr (FMT == kSfPacked && GRAN == 32) {
+        // the four 32-row groups of the tile make one word per logical row
+        __syncthreads();
+        if (warp == 0) {
+            const int64_t gw = jt / 32;                // first group of the tile (a multiple of 4)
+#pragma unroll
+            for (int c = 0; c < V; ++c) {
+                const int64_t i = i0 + c;
+                if (i < m && gw < G) {
+                    const uint32_t word = ebuf[0][lane][c] | (ebuf[1][lane][c] << 8) | (ebuf[2][lane][c] << 16) |
+                                          (ebuf[3][lane][c] << 24);
+                    static_cast<int32_t*>(sf)[i * ssm + (gw / 4) * ssg] = static_cast<int32_t>(word);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Generic per-token cast: any strides. One thread per (row, run of four
 // groups), so a packed int32 word is always written whole. Slow path.
 // ---------------------------------------------------------------------------
@@ -665,6 +793,15 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         if (blocks > cap) blocks = cap;
         cast_rows_kernel<T, GRAN, FMT, RECIP><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
             x, a.m, a.n, a.sxm, a.out, a.som, a.sf, a.ssm, a.ssg, chunks, vec_in, vec_out);
+        return cudaGetLastError();
+    }
+    if (a.sxm == 1 && a.som == 1) {
+        constexpr int V = colmajor::kLaneBytes / sizeof(T);
+        const int vec_in = (reinterpret_cast<uintptr_t>(x) % 8 == 0) && ((a.sxn * static_cast<int64_t>(sizeof(T))) % 8 == 0);
+        const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) % V) == 0) && (a.son % V == 0);
+        dim3 grid(static_cast<unsigned>((a.m + 32 * V - 1) / (32 * V)), static_cast<unsigned>((a.n + 127) / 128));
+        cast_colmajor_kernel<T, GRAN, FMT, RECIP><<<grid, 32 * colmajor::kWarps, 0, st>>>(
+            x, a.m, a.n, a.sxn, a.out, a.son, a.sf, a.ssm, a.ssg, vec_in, vec_out);
         return cudaGetLastError();
     }
     if (a.sxm == 1 && a.son == 1 && a.tma_ok) {

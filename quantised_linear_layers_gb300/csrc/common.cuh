@@ -398,6 +398,34 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory descriptor of an MN-major operand tile with 128-byte swizzle:
+// rows are K, each row 128 bytes of M (or N) elements, as a TMA box of
+// [K rows][128 B] with 128-byte swizzle lays it out. The tile's MN extent is
+// one 128-byte swizzle atom, so only the step between 8-row groups along K
+// (1024 B) is ever taken; both offset fields carry it.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1024u >> 4) << 16;    // leading offset
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;    // stride offset: 8 K-rows x 128 B
+    d |= static_cast<uint64_t>(1u) << 46;            // version
+    d |= static_cast<uint64_t>(2u) << 61;            // 128-byte swizzle
+    return d;
+}
+
+// Descriptor of an operand tile in either major-ness, and its advance (in the
+// 16-byte address units of the descriptor) per 32-wide K slice: 32 bytes along
+// a K-major row, or 32 rows of 128 bytes when MN-major.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, bool mn_major) {
+    return mn_major ? sw128_mnmajor_desc(saddr) : sw128_kmajor_desc(saddr);
+}
+__device__ __forceinline__ uint64_t k32_step(bool mn_major) { return mn_major ? (32u * 128u) >> 4 : 32u >> 4; }
+
+// Instruction-descriptor bits that mark A (bit 15) and B (bit 16) MN-major.
+__host__ __device__ constexpr uint32_t idesc_mn_bits(bool a_mn, bool b_mn) {
+    return (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
+}
+
 // Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B E4M3
 // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at [17,23),
 // M >> 4 at [24,29).

@@ -216,7 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.m_indices == nullptr && static_cast<int>(blockIdx.x) < p.tiles_m * p.tiles_n) {
             int mb0, nb0;
             tile_coords(blockIdx.x, p, mb0, nb0);
-            for (int kb = 0; kb < p.num_kb && kb < C::kStages; ++kb) tma_prefetch_l2_2d(&tmap_b, kb * BK, nb0 * BN);
+            for (int kb = 0; kb < p.num_kb && kb < C::kStages; ++kb) {
+                if (p.b_mn) tma_prefetch_l2_2d(&tmap_b, nb0 * BN, kb * BK);
+                else tma_prefetch_l2_2d(&tmap_b, kb * BK, nb0 * BN);
+            }
         }
     }
     if (warp == 1) { tmem_alloc(tmem_base_sm, C::kTmemCols); tmem_relinquish(); }
@@ -247,8 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                         if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
                         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                        tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], kb * BK, mb * BM);
-                        tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, brow);
+                        if (p.a_mn) tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], mb * BM, kb * BK);
+                        else tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], kb * BK, mb * BM);
+                        if (p.b_mn) tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], brow, kb * BK);
+                        else tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, brow);
                     }
                 }
                 if (!ok) {
@@ -262,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == 1) {
             // ---------------- MMA issuer ----------------
             if (elect_one()) {
-                constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+                const uint32_t idesc = idesc_e4m3_f32(BM, BN) | idesc_mn_bits(p.a_mn, p.b_mn);
+                const uint64_t astep = k32_step(p.a_mn), bstep = k32_step(p.b_mn);
                 uint32_t it = 0, tc = 0;
                 bool ok = true;
                 for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -276,12 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                         if (!mbar_wait(&full[s], ph, ctl)) { ok = false; break; }
                         tc_fence_after_sync();
-                        const uint64_t adesc = sw128_kmajor_desc(smem_addr(sA + s * C::kStageA));
-                        const uint64_t bdesc = sw128_kmajor_desc(smem_addr(sB + s * C::kStageB));
+                        const uint64_t adesc = sw128_desc(smem_addr(sA + s * C::kStageA), p.a_mn);
+                        const uint64_t bdesc = sw128_desc(smem_addr(sB + s * C::kStageB), p.b_mn);
                         const uint32_t d_tmem = tmem_base + ts * BN;
 #pragma unroll
-                        for (int k4 = 0; k4 < BK / 32; ++k4)   // +32 bytes along K = +2 in the address field
-                            mma_e4m3(d_tmem, adesc + 2 * k4, bdesc + 2 * k4, idesc, k4 > 0 ? 1u : 0u);
+                        for (int k4 = 0; k4 < BK / 32; ++k4)
+                            mma_e4m3(d_tmem, adesc + astep * k4, bdesc + bstep * k4, idesc, k4 > 0 ? 1u : 0u);
                         mma_commit(&empty[s]);
                         mma_commit(&tfull[ts]);
                     }
@@ -494,8 +500,10 @@ template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
     using Cf = Cfg<BN, PER_ROW_B>;
     CUtensorMap ta, tb;
-    if (!encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)) return cudaErrorInvalidValue;
-    if (!encode_kmajor_map(&tb, L.b, L.n * (L.m_indices ? L.num_groups : 1), L.k, L.ldb, BN))
+    if (!(L.a_mn ? encode_kmajor_map(&ta, L.a, L.k, L.m, L.lda, BK) : encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)))
+        return cudaErrorInvalidValue;
+    if (!(L.b_mn ? encode_kmajor_map(&tb, L.b, L.k, L.n, L.ldb, BK)
+                 : encode_kmajor_map(&tb, L.b, L.n * (L.m_indices ? L.num_groups : 1), L.k, L.ldb, BN)))
         return cudaErrorInvalidValue;
     p.tiles_m = static_cast<int>((L.m + BM - 1) / BM);
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
@@ -562,6 +570,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     p.dgran = L.dgran;
     p.dfmt = L.dfmt;
     p.drecip = L.drecip;
+    p.a_mn = L.a_mn ? 1 : 0;
+    p.b_mn = L.b_mn ? 1 : 0;
     const int64_t es = L.out_fp8 ? 1 : (L.out_f32 ? 4 : 2);
     p.vec_store = ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && (L.ldd * es) % 16 == 0) ? 1 : 0;
     const int bn = L.block_n > 0 ? L.block_n : choose_block_n(L.m, L.n, num_sms);
@@ -569,6 +579,17 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     // tensor core's block-scaled MMA unless the CUDA-core path is requested.
     const bool ue8m0 = L.fmt == 1 || L.fmt == 2;
     const bool grouped = L.m_indices != nullptr;   // the pair kernel's two M halves share one B
+    if (L.a_mn || L.b_mn) {
+        // MN-major operands: one 128-byte swizzle atom of M / N per CTA, so
+        // 128-column tiles on one SM, or the CTA pair (128 columns per CTA)
+        if (ue8m0 && L.path != 1) {
+            const int64_t pair_tiles = ((L.m + 255) / 256) * ((L.n + 255) / 256);
+            if (L.path == 3 || (L.path == 0 && pair_tiles >= num_sms / 2)) return launch_gemm_mx2(L, p, st, num_sms);
+            return launch_gemm_mx(L, p, 128, st, num_sms);
+        }
+        if (L.out_f32) return launch_t<128, true, true>(L, p, st, num_sms);
+        return launch_t<128, false, false>(L, p, st, num_sms);
+    }
     if (L.out_fp8) {
         // E4M3 output: 256-wide tiles, so every epilogue thread owns whole
         // 128-column groups of its row (pair, single-SM or promotion kernel)

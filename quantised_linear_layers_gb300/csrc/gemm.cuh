@@ -36,6 +36,8 @@ struct GemmParams {
     int dgran;                // 32 or 128
     int dfmt;                 // 0 fp32, 1 UE8M0 (fp32 powers of two), 2 packed UE8M0
     int drecip;               // fp32 scales: factor 1 / s
+    // operands stored K-outer ([K][M] / [K][N]) and read MN-major
+    int a_mn, b_mn;
 };
 
 // Host-side description of one GEMM call.
@@ -69,6 +71,7 @@ struct GemmLaunch {
     void* dsf;
     int64_t dsm, dsg;
     int dgran, dfmt, drecip;
+    bool a_mn, b_mn;          // A stored [k][m] / B stored [k][n] (row strides lda / ldb)
 };
 
 // Rows of A per M tile; in the M-grouped contiguous layout every expert's

@@ -159,7 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.m_indices == nullptr && static_cast<int>(blockIdx.x) < p.tiles_m * p.tiles_n) {
             int mb0, nb0;
             tile_coords(blockIdx.x, p, mb0, nb0);
-            for (int kb = 0; kb < p.num_kb && kb < C::kStages; ++kb) tma_prefetch_l2_2d(&tmap_b, kb * BK, nb0 * BN);
+            for (int kb = 0; kb < p.num_kb && kb < C::kStages; ++kb) {
+                if (p.b_mn) tma_prefetch_l2_2d(&tmap_b, nb0 * BN, kb * BK);
+                else tma_prefetch_l2_2d(&tmap_b, kb * BK, nb0 * BN);
+            }
         }
     }
     if (warp == 1) { tmem_alloc(tmem_base_sm, C::kTmemCols); tmem_relinquish(); }
@@ -190,8 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                         if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
                         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                        tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], kb * BK, mb * BM);
-                        tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, brow);
+                        if (p.a_mn) tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], mb * BM, kb * BK);
+                        else tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], kb * BK, mb * BM);
+                        if (p.b_mn) tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], brow, kb * BK);
+                        else tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, brow);
                     }
                 }
                 if (!ok) {
@@ -233,12 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                             if (!mbar_wait(&full[s], ph, ctl)) { ok = false; break; }
                             tc_fence_after_sync();
-                            const uint64_t adesc = sw128_kmajor_desc(smem_addr(sA + s * C::kStageA));
-                            const uint64_t bdesc = sw128_kmajor_desc(smem_addr(sB + s * C::kStageB));
-                            const uint32_t idesc = idesc_mxf8_ue8m0(BM, BN, kbi, kbi);
+                            const uint64_t adesc = sw128_desc(smem_addr(sA + s * C::kStageA), p.a_mn);
+                            const uint64_t bdesc = sw128_desc(smem_addr(sB + s * C::kStageB), p.b_mn);
+                            const uint32_t idesc = idesc_mxf8_ue8m0(BM, BN, kbi, kbi) | idesc_mn_bits(p.a_mn, p.b_mn);
+                            const uint64_t astep = k32_step(p.a_mn), bstep = k32_step(p.b_mn);
 #pragma unroll
                             for (int k4 = 0; k4 < BK / 32; ++k4)
-                                mma_mxf8_block_scaled(d_tmem, adesc + 2 * k4, bdesc + 2 * k4, idesc, sf_col,
+                                mma_mxf8_block_scaled(d_tmem, adesc + astep * k4, bdesc + bstep * k4, idesc, sf_col,
                                                       sf_col + 4, (kb > 0 || k4 > 0) ? 1u : 0u);
                             mma_commit(&empty[s]);
                             ++it;
@@ -435,8 +441,10 @@ template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_mx_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
     using Cf = MxCfg<BN>;
     CUtensorMap ta, tb;
-    if (!encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)) return cudaErrorInvalidValue;
-    if (!encode_kmajor_map(&tb, L.b, L.n * (L.m_indices ? L.num_groups : 1), L.k, L.ldb, BN))
+    if (!(L.a_mn ? encode_kmajor_map(&ta, L.a, L.k, L.m, L.lda, BK) : encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)))
+        return cudaErrorInvalidValue;
+    if (!(L.b_mn ? encode_kmajor_map(&tb, L.b, L.k, L.n, L.ldb, BK)
+                 : encode_kmajor_map(&tb, L.b, L.n * (L.m_indices ? L.num_groups : 1), L.k, L.ldb, BN)))
         return cudaErrorInvalidValue;
     p.tiles_m = static_cast<int>((L.m + BM - 1) / BM);
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);

@@ -160,8 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (cid < p.tiles_m * p.tiles_n) {
             int mb0, nb0;
             tile_coords(cid, p, mb0, nb0);
-            for (int kb = 0; kb < p.num_kb && kb < C::kStages; ++kb)
-                tma_prefetch_l2_2d(&tmap_b, kb * BK, nb0 * BN + static_cast<int>(rank) * BNH);
+            for (int kb = 0; kb < p.num_kb && kb < C::kStages; ++kb) {
+                const int brow0 = nb0 * BN + static_cast<int>(rank) * BNH;
+                if (p.b_mn) tma_prefetch_l2_2d(&tmap_b, brow0, kb * BK);
+                else tma_prefetch_l2_2d(&tmap_b, kb * BK, brow0);
+            }
         }
     }
     if (warp == 1) { tmem_alloc_pair(tmem_base_sm, C::kTmemCols); tmem_relinquish_pair(); }
@@ -195,11 +198,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
                         if (leader) {
                             mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
-                            tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], kb * BK, a_row);
-                            tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, b_row);
+                            if (p.a_mn) tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], a_row, kb * BK);
+                            else tma_load_2d(sA + s * C::kStageA, &tmap_a, &full[s], kb * BK, a_row);
+                            if (p.b_mn) tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], b_row, kb * BK);
+                            else tma_load_2d(sB + s * C::kStageB, &tmap_b, &full[s], kb * BK, b_row);
                         } else {
-                            tma_load_2d_pair(sA + s * C::kStageA, &tmap_a, leader_full0 + s * 8u, kb * BK, a_row);
-                            tma_load_2d_pair(sB + s * C::kStageB, &tmap_b, leader_full0 + s * 8u, kb * BK, b_row);
+                            if (p.a_mn) tma_load_2d_pair(sA + s * C::kStageA, &tmap_a, leader_full0 + s * 8u, a_row, kb * BK);
+                            else tma_load_2d_pair(sA + s * C::kStageA, &tmap_a, leader_full0 + s * 8u, kb * BK, a_row);
+                            if (p.b_mn) tma_load_2d_pair(sB + s * C::kStageB, &tmap_b, leader_full0 + s * 8u, b_row, kb * BK);
+                            else tma_load_2d_pair(sB + s * C::kStageB, &tmap_b, leader_full0 + s * 8u, kb * BK, b_row);
                         }
                     }
                 }
@@ -235,12 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                                 if (!mbar_wait_cluster(&full[s], ph, ctl)) { ok = false; break; }
                                 tc_fence_after_sync();
-                                const uint64_t adesc = sw128_kmajor_desc(smem_addr(sA + s * C::kStageA));
-                                const uint64_t bdesc = sw128_kmajor_desc(smem_addr(sB + s * C::kStageB));
-                                const uint32_t idesc = idesc_mxf8_ue8m0(2 * BM, BN, kbi, kbi);
+                                const uint64_t adesc = sw128_desc(smem_addr(sA + s * C::kStageA), p.a_mn);
+                                const uint64_t bdesc = sw128_desc(smem_addr(sB + s * C::kStageB), p.b_mn);
+                                const uint32_t idesc =
+                                    idesc_mxf8_ue8m0(2 * BM, BN, kbi, kbi) | idesc_mn_bits(p.a_mn, p.b_mn);
+                                const uint64_t astep = k32_step(p.a_mn), bstep = k32_step(p.b_mn);
 #pragma unroll
                                 for (int k4 = 0; k4 < BK / 32; ++k4)
-                                    mma_mxf8_block_scaled_pair(tmem_base, adesc + 2 * k4, bdesc + 2 * k4, idesc,
+                                    mma_mxf8_block_scaled_pair(tmem_base, adesc + astep * k4, bdesc + bstep * k4, idesc,
                                                                sf_col, sf_col + 4, (kb > 0 || k4 > 0) ? 1u : 0u);
                                 mma_commit_pair_multicast(&empty[s], 0x3);
                                 ++it;
@@ -442,8 +451,10 @@ template <bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
     using Cf = Mx2Cfg;
     CUtensorMap ta, tb;
-    if (!encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)) return cudaErrorInvalidValue;
-    if (!encode_kmajor_map(&tb, L.b, L.n, L.k, L.ldb, BNH)) return cudaErrorInvalidValue;
+    if (!(L.a_mn ? encode_kmajor_map(&ta, L.a, L.k, L.m, L.lda, BK) : encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)))
+        return cudaErrorInvalidValue;
+    if (!(L.b_mn ? encode_kmajor_map(&tb, L.b, L.k, L.n, L.ldb, BK) : encode_kmajor_map(&tb, L.b, L.n, L.k, L.ldb, BNH)))
+        return cudaErrorInvalidValue;
     p.tiles_m = static_cast<int>((L.m + 2 * BM - 1) / (2 * BM));
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
     const int tiles = p.tiles_m * p.tiles_n;

@@ -5,13 +5,22 @@ fwd,bwd" (maintainer's pseudo-code) and the integration of "DeepGEMM
 Essentials: High-Performance FP8 Matrix Multiplication" Part 18:
 
   fwd    Y  = X  W^T  : cast X per token; GEMM against W's 128x128 block cast
-  dgrad  dX = dY W    : cast dY per token; GEMM against W^T's block cast
+  dgrad  dX = dY W    : cast dY per token; GEMM against W^T's block cast (read
+                        from W column-wise, no transposed copy of W)
   wgrad  dW = dY^T X  : cast dY^T and X^T per token along the token axis (the
                         transposed views are read in place); wgrad GEMM with
                         fp32 output, optionally accumulated into a main grad
 
-W and W^T are cast once per weight update (``FP8Weight``), not every forward.
-Every step runs in the CUDA library; torch only allocates outputs.
+With ``mn_major=True`` no operand is transposed: wgrad casts dY and X with
+1x128 groups along the token axis into their own [T, features] layout and the
+GEMM reads both MN-major; dgrad reads W's own cast MN-major with its grid
+transposed (except with packed UE8M0 scales, whose words run along the
+forward K, where W^T's cast is kept). The default is the faster form as
+measured on GB300 (the transposed casts, while the column-major cast is
+slower than the TMA-staged transposed one).
+
+W is cast once per weight update (``FP8Weight``), not every forward. Every
+step runs in the CUDA library; torch only allocates outputs.
 """
 from __future__ import annotations
 
@@ -21,12 +30,14 @@ from . import ops
 
 
 class FP8Weight:
-    """A weight W [out, in] and its two E4M3 casts with 128x128 block scales:
-    W (the forward operand) and W^T (the dgrad operand, read from W column-wise,
-    so no transposed copy of W is made)."""
+    """A weight W [out, in] and its E4M3 casts with 128x128 block scales: W
+    (the forward operand) and W^T (the dgrad operand ``wtq`` / ``wts``, read
+    from W column-wise). With ``mn_major`` and fp32 or UE8M0 scales the dgrad
+    GEMM reads W's own cast MN-major instead and ``wtq`` / ``wts`` are None."""
 
-    def __init__(self, w: torch.Tensor, fmt: int = ops.SF_PACKED_UE8M0):
+    def __init__(self, w: torch.Tensor, fmt: int = ops.SF_PACKED_UE8M0, mn_major: bool = False):
         self.fmt = fmt
+        self.mn_major = mn_major
         self.update(w)
 
     def update(self, w: torch.Tensor) -> None:
@@ -34,7 +45,10 @@ class FP8Weight:
             raise ValueError("weight must be 2-D [out_features, in_features]")
         self.shape = tuple(w.shape)
         self.wq, self.ws = ops.fp8_cast_per_block(w, self.fmt)
-        self.wtq, self.wts = ops.fp8_cast_per_block(w.t(), self.fmt)
+        if self.mn_major and self.fmt != ops.SF_PACKED_UE8M0:
+            self.wtq = self.wts = None
+        else:
+            self.wtq, self.wts = ops.fp8_cast_per_block(w.t(), self.fmt)
 
 
 def _cast_rows(x: torch.Tensor, fmt: int, mn_major: bool = True):
@@ -46,6 +60,17 @@ def _cast_rows(x: torch.Tensor, fmt: int, mn_major: bool = True):
     return ops.fp8_cast_per_token(x, 128, fmt, out=out, sf_mn_major=mn_major)
 
 
+def _cast_cols(x: torch.Tensor, fmt: int):
+    """Per-token cast of x^T (groups of 128 down the columns of x [T, C]) with
+    the E4M3 output kept in x's own layout: returns (q [T, C] with 16-byte
+    aligned rows, scales [C, ceil(T/128)] M-major)."""
+    t, c = x.shape
+    ld = -(-max(c, 1) // 16) * 16
+    q = torch.empty((t, ld), dtype=torch.float8_e4m3fn, device=x.device)[:, :c]
+    _, s = ops.fp8_cast_per_token(x.t(), 128, fmt, out=q.t(), sf_mn_major=True)
+    return q, s
+
+
 def forward(x: torch.Tensor, w: FP8Weight, out: torch.Tensor | None = None) -> torch.Tensor:
     """Y [T, out] = X [T, in] W^T (bf16)."""
     xq, xs = _cast_rows(x, w.fmt)
@@ -55,13 +80,20 @@ def forward(x: torch.Tensor, w: FP8Weight, out: torch.Tensor | None = None) -> t
 def dgrad(dy: torch.Tensor, w: FP8Weight, out: torch.Tensor | None = None) -> torch.Tensor:
     """dX [T, in] = dY [T, out] W (bf16)."""
     dq, ds = _cast_rows(dy, w.fmt)
+    if w.wtq is None:
+        return ops.gemm_fp8_nn_bf16(dq, ds, w.wq, w.ws.t(), w.fmt, out=out)
     return ops.gemm_fp8_nt_bf16(dq, ds, w.wtq, w.wts, w.fmt, out=out)
 
 
 def wgrad(dy: torch.Tensor, x: torch.Tensor, fmt: int = ops.SF_PACKED_UE8M0,
-          out: torch.Tensor | None = None, accumulate: bool = False) -> torch.Tensor:
+          out: torch.Tensor | None = None, accumulate: bool = False, mn_major: bool = False) -> torch.Tensor:
     """dW [out, in] (+)= dY^T X (fp32); K is the token axis, both operands with
-    1x128 scales along it."""
+    1x128 scales along it: cast from the transposed views, or with
+    ``mn_major`` cast into their own [T, features] layout and read MN-major."""
+    if mn_major:
+        aq, sa = _cast_cols(dy, fmt)
+        bq, sb = _cast_cols(x, fmt)
+        return ops.gemm_fp8_wgrad_fp32_mn(aq, sa, bq, sb, out=out, accumulate=accumulate, fmt=fmt)
     aq, sa = _cast_rows(dy.t(), fmt)
     bq, sb = _cast_rows(x.t(), fmt, mn_major=False)
     return ops.gemm_fp8_wgrad_fp32(aq, sa, bq, sb, out=out, accumulate=accumulate, fmt=fmt)
@@ -81,11 +113,12 @@ class _FP8LinearFn(torch.autograd.Function):
         dy = dy.contiguous()
         dx = dgrad(dy, ctx.w8) if ctx.needs_input_grad[0] else None
         module = ctx.module
+        mn = ctx.w8.mn_major
         if module is not None and module.main_grad is not None:
-            wgrad(dy, x, ctx.w8.fmt, out=module.main_grad, accumulate=True)
+            wgrad(dy, x, ctx.w8.fmt, out=module.main_grad, accumulate=True, mn_major=mn)
             dw = None
         else:
-            dw = wgrad(dy, x, ctx.w8.fmt).to(x.dtype) if ctx.needs_input_grad[1] else None
+            dw = wgrad(dy, x, ctx.w8.fmt, mn_major=mn).to(x.dtype) if ctx.needs_input_grad[1] else None
         return dx, dw, None, None
 
 
@@ -93,11 +126,13 @@ class FP8Linear(torch.nn.Module):
     """nn.Linear (no bias) whose fwd / dgrad / wgrad run through the FP8 cast and
     GEMM. With ``accumulate_main_grad`` the weight gradient accumulates into the
     fp32 buffer ``main_grad`` (as the wgrad GEMM's accumulate form) instead of
-    being returned to autograd."""
+    being returned to autograd; ``mn_major`` selects the MN-major backward
+    (no transposed operands)."""
 
     def __init__(self, in_features: int, out_features: int, fmt: int = ops.SF_PACKED_UE8M0,
-                 device=None, dtype=torch.bfloat16, accumulate_main_grad: bool = False):
+                 device=None, dtype=torch.bfloat16, accumulate_main_grad: bool = False, mn_major: bool = False):
         super().__init__()
+        self.mn_major = mn_major
         self.weight = torch.nn.Parameter(torch.empty((out_features, in_features), device=device, dtype=dtype))
         torch.nn.init.normal_(self.weight, std=0.02)
         self.fmt = fmt
@@ -111,7 +146,7 @@ class FP8Linear(torch.nn.Module):
         v = self.weight._version
         if self._w8 is None or self._w8_version != v:
             with torch.no_grad():
-                self._w8 = FP8Weight(self.weight.detach(), self.fmt)
+                self._w8 = FP8Weight(self.weight.detach(), self.fmt, self.mn_major)
             self._w8_version = v
         return self._w8
 

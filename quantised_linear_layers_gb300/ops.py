@@ -37,6 +37,10 @@ _SIGS = {
     "ql_get_m_alignment_for_contiguous_layout": [],
     "gemm_fp8_nt_fp8out": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64, _vp, _i64,
                            _i64, _int, _int, _i64, _i64, _i64, _vp],
+    "gemm_fp8_wgrad_fp32_mn": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
+                               _i64, _i64, _i64, _int, _vp],
+    "gemm_fp8_nn_bf16": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
+                         _i64, _i64, _i64, _vp],
     "ql_gemm_workspace_size": [_i64, _i64, _i64],
     "ql_set_num_sms": [_int],
     "ql_get_num_sms": [],
@@ -273,6 +277,57 @@ def m_grouped_gemm_fp8_nt_bf16_contiguous(a: torch.Tensor, sfa: torch.Tensor, b:
 
 def get_m_alignment_for_contiguous_layout() -> int:
     return int(load_library().ql_get_m_alignment_for_contiguous_layout())
+
+
+def gemm_fp8_wgrad_fp32_mn(a_t: torch.Tensor, sfa: torch.Tensor, b_t: torch.Tensor, sfb: torch.Tensor,
+                           out: torch.Tensor | None = None, accumulate: bool = False,
+                           fmt: int = SF_FP32) -> torch.Tensor:
+    """D [m, n] (+)= A B^T, fp32, with both operands given K-outer: a_t [k, m]
+    and b_t [k, n] (contiguous rows); sfa [m, ceil(k/128)], sfb [n, ceil(k/128)]."""
+    _bytes8(a_t)
+    _bytes8(b_t)
+    if a_t.dim() != 2 or b_t.dim() != 2 or a_t.stride(1) != 1 or b_t.stride(1) != 1:
+        raise ValueError("a_t and b_t must be 2-D with contiguous rows")
+    if a_t.shape[0] != b_t.shape[0]:
+        raise ValueError("a_t and b_t must share K (their first dimension)")
+    k, m = a_t.shape
+    n = b_t.shape[1]
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate needs an existing out")
+        out = torch.empty((m, n), dtype=torch.float32, device=a_t.device)
+    if out.dtype != torch.float32 or out.stride(1) != 1:
+        raise ValueError("out must be fp32 with contiguous rows")
+    st = load_library().gemm_fp8_wgrad_fp32_mn(
+        a_t.data_ptr(), a_t.stride(0), sfa.data_ptr(), sfa.stride(0), sfa.stride(1),
+        b_t.data_ptr(), b_t.stride(0), sfb.data_ptr(), sfb.stride(0), sfb.stride(1),
+        fmt, out.data_ptr(), out.stride(0), m, n, k, int(bool(accumulate)), _stream(a_t))
+    _check("gemm_fp8_wgrad_fp32_mn", st)
+    return out
+
+
+def gemm_fp8_nn_bf16(a: torch.Tensor, sfa: torch.Tensor, b_kn: torch.Tensor, sfb: torch.Tensor,
+                     fmt: int = SF_FP32, out: torch.Tensor | None = None) -> torch.Tensor:
+    """D = A B, bf16 [m, n]: A [m, k] with 1x128 scales, B given as [k, n]
+    (contiguous rows) with 128x128 scales sfb [ceil(n/128), ceil(k/128)] (any strides)."""
+    _bytes8(a)
+    _bytes8(b_kn)
+    if a.dim() != 2 or b_kn.dim() != 2 or a.stride(1) != 1 or b_kn.stride(1) != 1:
+        raise ValueError("a and b_kn must be 2-D with contiguous rows")
+    if a.shape[1] != b_kn.shape[0]:
+        raise ValueError("a [m, k] and b_kn [k, n] must share K")
+    m, k = a.shape
+    n = b_kn.shape[1]
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    if out.dtype != torch.bfloat16 or out.stride(1) != 1:
+        raise ValueError("out must be bf16 with contiguous rows")
+    st = load_library().gemm_fp8_nn_bf16(
+        a.data_ptr(), a.stride(0), sfa.data_ptr(), sfa.stride(0), sfa.stride(1),
+        b_kn.data_ptr(), b_kn.stride(0), sfb.data_ptr(), sfb.stride(0), sfb.stride(1),
+        fmt, out.data_ptr(), out.stride(0), m, n, k, _stream(a))
+    _check("gemm_fp8_nn_bf16", st)
+    return out
 
 
 def set_num_sms(n: int) -> None:

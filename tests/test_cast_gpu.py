@@ -219,3 +219,27 @@ def test_block_cast_packed(orc, ops, shape, transposed_input):
         oq, os_ = orc.cast_per_block(np_input(w), 2)
     assert np.array_equal(np_bytes(q), oq)
     assert np.array_equal(np_sf(s).view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("gran", GRANS)
+@pytest.mark.parametrize("fmt", FMTS, ids=["fp32", "ue8m0", "packed"])
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(4096, 1024), (300, 200), (7168, 640), (130, 36), (1, 24)],
+                         ids=lambda s: f"{s[0]}x{s[1]}")
+def test_cast_column_major_in_and_out(orc, ops, dtype, gran, fmt, shape):
+    """Cast of x^T written as q^T (x_stride_m == out_stride_m == 1): groups run
+    down the columns of the physical [tokens, features] array and the E4M3
+    output keeps that layout (the MN-major GEMM operand); ragged token counts,
+    ragged and narrow feature counts, all-zero and huge groups."""
+    t_rows, feats = shape
+    x = make_x(t_rows, feats, dtype, gran, huge=False)
+    x[min(5, t_rows - 1), :] = 3.0e38 if t_rows > 1 else x[0, :]
+    q_phys = torch.empty((t_rows, feats), dtype=torch.float8_e4m3fn, device="cuda")
+    q, s = ops.fp8_cast_per_token(x.cuda().t(), gran, fmt, out=q_phys.t(), sf_mn_major=True)
+    oq, os_ = orc.cast_per_token(np_input(x).T, gran, fmt)
+    assert np.array_equal(np_bytes(q_phys).T, oq), "E4M3 bytes differ"
+    gs = np_sf(s)
+    if fmt == 2:
+        assert np.array_equal(np.ascontiguousarray(gs), os_)
+    else:
+        assert np.array_equal(np.ascontiguousarray(gs).view(np.uint32), os_.view(np.uint32))

@@ -3,8 +3,8 @@
 "[Help] Starter script for nn.Linear for fwd,bwd" (maintainer's pseudo-code):
 fwd casts X per token and multiplies by W's block cast; dgrad casts dY and
 multiplies by W^T's block cast (W transposed and requantised in 128x128
-blocks); wgrad casts dY^T and X^T per token along the token axis and writes
-fp32. Every cast is compared bit for bit with the oracle, every GEMM within
+blocks: the same bytes as W's cast read MN-major, by transpose invariance);
+wgrad casts dY^T and X^T per token along the token axis and writes fp32. Every cast is compared bit for bit with the oracle, every GEMM within
 the GEMM tolerance, at the full nn.Linear workload (X [4096, 7168],
 dY [4096, 4096], W [4096, 7168] * 0.02) on sampled rows.
 """
@@ -33,22 +33,26 @@ def oracle_fmt(fmt):
     return fmt
 
 
+@pytest.mark.parametrize("mn_major", [False, True], ids=["transposed", "mn_major"])
 @pytest.mark.parametrize("fmt", [0, 2], ids=["fp32", "packed"])
 @pytest.mark.parametrize("shape", [(4096, 7168, 4096), (300, 640, 384)], ids=["full", "ragged"])
-def test_linear_fwd_dgrad_wgrad(orc, lin, fmt, shape):
+def test_linear_fwd_dgrad_wgrad(orc, lin, fmt, shape, mn_major):
     T, IN, OUT = shape
     x = syn.randn((T, IN), seed=syn.SEED_X)
     dy = syn.randn((T, OUT), seed=syn.SEED_DY)
     w = syn.randn((OUT, IN), seed=syn.SEED_W, mul=0.02)
     xg, dyg, wg = x.cuda(), dy.cuda(), w.cuda()
-    w8 = lin.FP8Weight(wg, fmt)
+    w8 = lin.FP8Weight(wg, fmt, mn_major)
     # weight casts: W and W^T, bit-exact
     bfmt = fmt
     oq, os_ = orc.cast_per_block(np_input(w), bfmt)
     assert np.array_equal(np_bytes(w8.wq), oq) and np.array_equal(np_sf(w8.ws).view(np.uint32), os_.view(np.uint32))
     otq, ots = orc.cast_per_block(np_input(w).T, bfmt)
-    assert np.array_equal(np_bytes(w8.wtq), otq)
-    assert np.array_equal(np_sf(w8.wts).view(np.uint32), ots.view(np.uint32))
+    if w8.wtq is not None:                    # packed words: dgrad's own W^T cast
+        assert np.array_equal(np_bytes(w8.wtq), otq)
+        assert np.array_equal(np_sf(w8.wts).view(np.uint32), ots.view(np.uint32))
+    else:                                     # dgrad reads W's cast MN-major
+        assert mn_major and fmt != 2
 
     rng = np.random.default_rng(11)
     rows_t = np.sort(rng.choice(T, min(T, 24), replace=False))
@@ -65,14 +69,14 @@ def test_linear_fwd_dgrad_wgrad(orc, lin, fmt, shape):
     ref = orc.gemm(dq, ds, otq, ots, fmt, rows=rows_t, out="bf16")
     check_gemm(dx[torch.from_numpy(rows_t).cuda()].float().cpu().numpy(), ref, "dgrad")
     # wgrad, fresh and accumulated into an fp32 main grad
-    dw = lin.wgrad(dyg, xg, fmt)
+    dw = lin.wgrad(dyg, xg, fmt, mn_major=mn_major)
     aq, sa = orc.cast_per_token(np_input(dy).T, 128, fmt)
     bq, sb = orc.cast_per_token(np_input(x).T, 128, fmt)
     ref = orc.gemm(aq, sa, bq, sb, fmt, b_per_row=True, rows=rows_o, out="f32")
     check_gemm(dw[torch.from_numpy(rows_o).cuda()].double().cpu().numpy(), ref, "wgrad")
     main = syn.randn((OUT, IN), seed=5, dtype=torch.float32, mul=0.1).cuda()
     main0 = main.clone()
-    lin.wgrad(dyg, xg, fmt, out=main, accumulate=True)
+    lin.wgrad(dyg, xg, fmt, out=main, accumulate=True, mn_major=mn_major)
     ref_acc = orc.gemm(aq, sa, bq, sb, fmt, b_per_row=True, rows=rows_o,
                        d_in=main0.double().cpu().numpy(), out="f32")
     check_gemm(main[torch.from_numpy(rows_o).cuda()].double().cpu().numpy(), ref_acc, "wgrad accumulate")
@@ -82,10 +86,11 @@ def test_linear_fwd_dgrad_wgrad(orc, lin, fmt, shape):
     assert rel < 0.05
 
 
-def test_fp8_linear_module_autograd(orc, lin):
+@pytest.mark.parametrize("fmt,mn_major", [(2, False), (0, True), (2, True)], ids=["packed", "fp32-mn", "packed-mn"])
+def test_fp8_linear_module_autograd(orc, lin, fmt, mn_major):
     torch.manual_seed(0)
     T, IN, OUT = 512, 1024, 768
-    m = lin.FP8Linear(IN, OUT, device="cuda")
+    m = lin.FP8Linear(IN, OUT, fmt=fmt, device="cuda", mn_major=mn_major)
     x = syn.randn((T, IN), seed=syn.SEED_X).cuda().requires_grad_(True)
     y = m(x)
     dy = syn.randn((T, OUT), seed=syn.SEED_DY).cuda()
@@ -94,7 +99,7 @@ def test_fp8_linear_module_autograd(orc, lin):
     ref_y = lin.forward(x.detach(), w8)
     assert torch.equal(y, ref_y)
     assert torch.equal(x.grad, lin.dgrad(dy, w8))
-    dw = lin.wgrad(dy, x.detach(), m.fmt)
+    dw = lin.wgrad(dy, x.detach(), m.fmt, mn_major=mn_major)
     assert torch.equal(m.weight.grad, dw.to(torch.bfloat16))
     # a weight update refreshes the cached casts
     with torch.no_grad():
