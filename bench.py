@@ -496,7 +496,7 @@ def run_workloads(dev, pk, reps):
         "us_step": round(step * 1e3, 1), "tflops_step": round(3 * fl / step / 1e9, 1),
         "tflops_without_weight_casts": round(3 * fl / (step - part[0]) / 1e9, 1)}
     # the weight gradient with transposed casts against MN-major operands
-    t_tr = _median_ms(lambda: linear.wgrad(dy, x, P), reps, flush)
+    t_tr = _median_ms(lambda: linear.wgrad(dy, x, P, mn_major=False), reps, flush)
     t_mn = _median_ms(lambda: linear.wgrad(dy, x, P, mn_major=True), reps, flush)
     launches += 6 * reps
     out["wgrad_transposed_vs_mn_major_4096x7168x4096"] = {

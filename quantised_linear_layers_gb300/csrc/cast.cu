@@ -550,6 +550,186 @@ __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restri
 }
 
 // ---------------------------------------------------------------------------
+// TMA-staged column-major per-token cast (x_stride_m == 1, out_stride_m == 1,
+// 16-byte-aligned physical rows): the same operation as cast_colmajor_kernel,
+// with one producer thread streaming boxes of 128 physical rows x 256 bytes
+// into a 4-stage shared-memory ring (128 KB in flight per SM) and 16 consumer
+// warps, each taking 8 rows x 8 bytes per lane of a box. Per box the consumers
+// combine their column amaxes through shared memory, one warp per group turns
+// them into scales and factors, and every lane quantises its 8 rows and
+// stores 8 x V bytes; the stage is released as soon as its bytes are in
+// registers. Persistent CTAs walk the boxes row band by row band. Every wait
+// is bounded; on a time-out the CTA records it and drains its copies.
+// ---------------------------------------------------------------------------
+namespace colmajor_tma {
+constexpr int kStages = 4;
+constexpr int kRows = 128;                   // physical rows (j) per box
+constexpr int kBoxBytes = kRows * 256;       // 32 KB
+constexpr int kConsumerWarps = 16;
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+}  // namespace colmajor_tma
+
+template <typename T, int GRAN, int FMT, bool RECIP>
+__global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
+    cast_colmajor_tma_kernel(const __grid_constant__ CUtensorMap tmap, int64_t m, int64_t n, uint8_t* __restrict__ out,
+                             int64_t ldo, void* __restrict__ sf, int64_t ssm, int64_t ssg, int vec_out,
+                             uint32_t* dev_status, uint64_t limit_ns) {
+    pdl_launch_dependents();    // a dependent GEMM may start its prologue
+    using namespace colmajor_tma;
+    constexpr int V = 8 / sizeof(T);                 // columns per lane (4 bf16 or 2 fp32)
+    constexpr int BI = 256 / sizeof(T);              // columns (logical rows i) per box
+    constexpr int R = 8;                             // rows per consumer warp
+    constexpr int WPG = GRAN / R;                    // consumer warps per group (16 or 4)
+    constexpr int NG = kConsumerWarps / WPG;         // groups per box (1 or 4)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* red = reinterpret_cast<float*>(ring + kStages * kBoxBytes);            // [16][32][V+1]
+    float* fbuf = red + kConsumerWarps * 32 * (V + 1);                            // [NG][32][V]
+    uint32_t* ebuf = reinterpret_cast<uint32_t*>(fbuf + NG * 32 * V);             // [NG][32][V]
+    uint64_t* full = reinterpret_cast<uint64_t*>(ebuf + NG * 32 * V);
+    uint64_t* empty = full + kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t strips = (m + BI - 1) / BI;
+    const int64_t bands = (n + kRows - 1) / kRows;
+    const int64_t units = strips * bands;
+    const int64_t G = (n + GRAN - 1) / GRAN;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kConsumerWarps); }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const WaitCtl ctl{abort_flag, dev_status, limit_ns};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+                const int64_t band = u / strips, strip = u % strips;
+                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
+                mbar_arrive_expect_tx(&full[s], kBoxBytes);
+                tma_load_2d(ring + s * kBoxBytes, &tmap, &full[s], static_cast<int32_t>(strip * BI),
+                            static_cast<int32_t>(band * kRows));
+            }
+            if (!ok) {
+                const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+                for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % kStages], (j / kStages) & 1u, limit_ns);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int cw = warp - 1;                       // consumer warp: rows 8cw .. 8cw+8 of a box
+        const int w0 = (cw / WPG) * WPG;
+        const int grp = cw / WPG;
+        const bool group_lead = cw == w0;
+        uint32_t it = 0;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+            const int64_t band = u / strips, strip = u % strips;
+            const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], ph, ctl)) != 0;
+            uint2 raw[R];
+            if (ok) {
+                const uint8_t* box = ring + s * kBoxBytes;
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    raw[r] = *reinterpret_cast<const uint2*>(box + (cw * R + r) * 256 + lane * 8);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                float amax[V];
+#pragma unroll
+                for (int c = 0; c < V; ++c) amax[c] = 0.0f;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const T* t = reinterpret_cast<const T*>(&raw[r]);
+#pragma unroll
+                    for (int c = 0; c < V; ++c) amax[c] = fmaxf(amax[c], fabsf(to_f32(t[c])));
+                }
+#pragma unroll
+                for (int c = 0; c < V; ++c) red[(cw * 32 + lane) * (V + 1) + c] = amax[c];
+            }
+            // every consumer warp arrives here once per box whatever its wait
+            // gave; if any wait ran out, all of them leave together
+            if (named_bar_or(1, 32 * kConsumerWarps, !ok)) break;
+            const int64_t i0 = strip * BI + lane * V;        // first logical row of this lane
+            const int64_t j0 = band * kRows + cw * R;        // first physical row of this warp
+            const int64_t g = (band * kRows + w0 * R) / GRAN;
+            if (group_lead) {
+#pragma unroll
+                for (int c = 0; c < V; ++c) {
+                    float a = red[(w0 * 32 + lane) * (V + 1) + c];
+#pragma unroll
+                    for (int w = 1; w < WPG; ++w) a = fmaxf(a, red[((w0 + w) * 32 + lane) * (V + 1) + c]);
+                    float sc, f;
+                    uint32_t eb;
+                    group_scale<FMT, RECIP>(a, sc, f, eb);
+                    fbuf[(grp * 32 + lane) * V + c] = f;
+                    const int64_t i = i0 + c;
+                    if constexpr (FMT != kSfPacked) {
+                        if (i < m && g < G) static_cast<float*>(sf)[i * ssm + g * ssg] = sc;
+                    } else if constexpr (GRAN == 128) {
+                        if (i < m && g < G) {
+                            uint8_t* word =
+                                reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + i * ssm + (g / 4) * ssg);
+                            word[g % 4] = static_cast<uint8_t>(eb);
+                            if (g == G - 1)
+                                for (int z = static_cast<int>(g % 4) + 1; z < 4; ++z) word[z] = 0;
+                        }
+                    } else {
+                        ebuf[(grp * 32 + lane) * V + c] = (g < G) ? eb : 0u;
+                    }
+                }
+            }
+            named_bar_sync(1, 32 * kConsumerWarps);
+            float f[V];
+#pragma unroll
+            for (int c = 0; c < V; ++c) f[c] = fbuf[(grp * 32 + lane) * V + c];
+            if constexpr (FMT == kSfPacked && GRAN == 32) {
+                if (cw == 0) {
+                    const int64_t gw = band * kRows / 32;   // first group of the box (a multiple of 4)
+#pragma unroll
+                    for (int c = 0; c < V; ++c) {
+                        const int64_t i = i0 + c;
+                        if (i < m && gw < G) {
+                            const uint32_t word = ebuf[(0 * 32 + lane) * V + c] | (ebuf[(1 * 32 + lane) * V + c] << 8) |
+                                                  (ebuf[(2 * 32 + lane) * V + c] << 16) |
+                                                  (ebuf[(3 * 32 + lane) * V + c] << 24);
+                            static_cast<int32_t*>(sf)[i * ssm + (gw / 4) * ssg] = static_cast<int32_t>(word);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int64_t j = j0 + r;
+                if (j >= n) break;
+                const T* t = reinterpret_cast<const T*>(&raw[r]);
+                uint8_t* dst = out + j * ldo + i0;
+                uint32_t w = e4m3x2(__fmul_rn(to_f32(t[0]), f[0]), __fmul_rn(to_f32(t[1]), f[1]));
+                if constexpr (V == 4)
+                    w |= e4m3x2(__fmul_rn(to_f32(t[2]), f[2]), __fmul_rn(to_f32(t[3]), f[3])) << 16;
+                if (vec_out && i0 + V <= m) {
+                    if constexpr (V == 4) *reinterpret_cast<uint32_t*>(dst) = w;
+                    else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < V; ++c)
+                        if (i0 + c < m) dst[c] = static_cast<uint8_t>(w >> (8 * c));
+                }
+            }
+            // red, fbuf and ebuf are rewritten for the next box only after every
+            // consumer has passed this barrier
+            named_bar_sync(1, 32 * kConsumerWarps);
+        }
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
 // Generic per-token cast: any strides. One thread per (row, run of four
 // groups), so a packed int32 word is always written whole. Slow path.
 // ---------------------------------------------------------------------------
@@ -794,6 +974,32 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         cast_rows_kernel<T, GRAN, FMT, RECIP><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
             x, a.m, a.n, a.sxm, a.out, a.som, a.sf, a.ssm, a.ssg, chunks, vec_in, vec_out);
         return cudaGetLastError();
+    }
+    if (a.sxm == 1 && a.som == 1 && a.tma_ok) {
+        using namespace colmajor_tma;
+        constexpr int V = 8 / sizeof(T);
+        constexpr int BI = 256 / sizeof(T);
+        CUtensorMap tmap;
+        if (encode_2d_map(&tmap, x, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          a.n, a.m, a.sxn * static_cast<int64_t>(sizeof(T)), kRows, BI)) {
+            const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) % V) == 0) && (a.son % V == 0);
+            constexpr int NG = kConsumerWarps / (GRAN / 8);
+            const int smem = kStages * kBoxBytes + kConsumerWarps * 32 * (V + 1) * 4 + 2 * NG * 32 * V * 4 +
+                             2 * kStages * 8 + 16 + 1024;
+            auto kern = cast_colmajor_tma_kernel<T, GRAN, FMT, RECIP>;
+            static bool attr = false;
+            if (!attr) {
+                cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                if (e != cudaSuccess) return e;
+                attr = true;
+            }
+            const int64_t units = ((a.m + BI - 1) / BI) * ((a.n + kRows - 1) / kRows);
+            int64_t grid = num_sms;
+            if (grid > units) grid = units;
+            kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tmap, a.m, a.n, a.out, a.son, a.sf, a.ssm, a.ssg,
+                                                                    vec_out, a.dev_status, a.wait_limit_ns);
+            return cudaGetLastError();
+        }
     }
     if (a.sxm == 1 && a.som == 1) {
         constexpr int V = colmajor::kLaneBytes / sizeof(T);
