@@ -17,7 +17,9 @@ workloads, timed apart from the step: forward GEMMs at M = 64/128/4096, the
 Linear layer's fwd+dgrad+wgrad step, the low-latency cast at 1-512 tokens
 eager and inside a CUDA graph), e2e (host buffers,
 copies inside the timed region), cpu_baseline (the CPU oracle on a bounded
-sample), clocks (nvidia-smi during the timed region), gpu_launches.
+sample), clocks (nvidia-smi during the timed region), gpu_launches. e2e runs
+the library's host-buffer call, which overlaps the copies of one row chunk
+with the kernels of the next.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs an independent replica (rows are independent:
@@ -60,6 +62,7 @@ def parse():
     ap.add_argument("--only-workloads", action="store_true",
                     help="run only the other workloads and print them as one JSON line")
     ap.add_argument("--reps", type=int, default=20, help="timed repetitions per other workload")
+    ap.add_argument("--e2e-chunk", type=int, default=1024, help="rows per step of the host-buffer pipeline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-oracle sample time")
     return ap.parse_args()
 
@@ -333,15 +336,18 @@ def run_ours(args, world, rank, local):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
+        # end to end through the library's host-buffer call: X from pinned host
+        # memory in, D to pinned host memory out, every step; the copies of one
+        # row chunk overlap the kernels of the next (ql_cast_gemm_host)
         xh = torch.empty((m, k), dtype=torch.bfloat16, pin_memory=True)
         xh.copy_(x.cpu())
         dh = torch.empty((m, n), dtype=torch.bfloat16, pin_memory=True)
         ke = min(K, 5)
+        chunk = args.e2e_chunk
+        wsp = torch.empty(ops.cast_gemm_host_workspace_size(n, k, chunk, fmt), dtype=torch.uint8, device=dev)
 
         def e2e_step():
-            x.copy_(xh, non_blocking=True)
-            step()
-            dh.copy_(d, non_blocking=True)
+            ops.cast_gemm_host(xh, wq, ws, fmt, dh, chunk, wsp)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -352,7 +358,10 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         te = max_over_ranks(world, time.perf_counter() - t0)
         e2e = {"value": round(flops_step * world * ke / te / 1e12, 2), "unit": UNIT,
-               "h2d_bytes_per_step": m * k * 2, "d2h_bytes_per_step": m * n * 2, "steps": ke}
+               "h2d_bytes_per_step": m * k * 2, "d2h_bytes_per_step": m * n * 2, "steps": ke,
+               "call": "ql_cast_gemm_host", "chunk_rows": chunk,
+               "ms_per_step": round(te / ke * 1e3, 3)}
+        del wsp
 
     workloads = None
     if not args.no_workloads:

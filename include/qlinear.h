@@ -276,6 +276,32 @@ ql_status gemm_fp8_nn_bf16(const uint8_t* a, int64_t lda, const void* sfa,
                            int fmt, uint16_t* d, int64_t ldd,
                            int64_t m, int64_t n, int64_t k, ql_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * ql_cast_gemm_host
+ * The forward step of the linear layer ("[Help] Starter script for nn.Linear
+ * for fwd,bwd": cast X per token, GEMM against W's block cast) with X and D
+ * in HOST memory: D = bf16( fp8_cast_per_token(X, 128, fmt) * B^T ).
+ *   x_host  bf16 [m, k] on the host, row stride ldx elements (pinned memory
+ *           lets the copies overlap the kernels; pageable memory works).
+ *   b, sfb  the device-resident E4M3 weight [n, k] and its 128x128 scales, as
+ *           gemm_fp8_nt_bf16.
+ *   d_host  bf16 [m, n] on the host, row stride ldd elements.
+ *   chunk_rows  rows per pipeline step; workspace: caller-owned device memory
+ *           of at least ql_cast_gemm_host_workspace_size(n, k, chunk_rows, fmt)
+ *           bytes, 256-byte aligned (QL_ERR_INVALID_ARG / QL_ERR_ALIGNMENT).
+ * Rows are copied in, cast, multiplied and copied out chunk by chunk, the
+ * copies of one chunk overlapping the kernels of the next on three library
+ * streams (created once per device) that start after the work already on
+ * `stream` and that `stream` waits for at the end. The result equals the
+ * device-buffer calls on the same data, bit for bit. Concurrent calls on one
+ * device are serialised by a lock.
+ * ------------------------------------------------------------------------- */
+size_t ql_cast_gemm_host_workspace_size(int64_t n, int64_t k, int64_t chunk_rows, int fmt);
+ql_status ql_cast_gemm_host(const void* x_host, int64_t ldx, const uint8_t* b, int64_t ldb,
+                            const void* sfb, int64_t sfb_stride_n, int64_t sfb_stride_k, int fmt,
+                            uint16_t* d_host, int64_t ldd, int64_t m, int64_t n, int64_t k,
+                            int64_t chunk_rows, void* workspace, size_t ws_bytes, ql_stream_t stream);
+
 /* Workspace bytes a GEMM of this shape needs (0 in this build). */
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k);
 

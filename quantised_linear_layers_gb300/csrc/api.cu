@@ -129,6 +129,68 @@ ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sa
     return from_cuda(ql::launch_gemm(L, st, effective_sms(di)));
 }
 
+// ---------------------------------------------------------------------------
+// Host-buffer forward pipeline (ql_cast_gemm_host): rows of X are copied to
+// the device, cast and multiplied chunk by chunk, and D comes back, with the
+// copy in, the kernels and the copy out of successive chunks overlapped on
+// three streams. The streams and events are created once per device and kept.
+// ---------------------------------------------------------------------------
+constexpr int kPipeSlots = 2;
+
+struct Pipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t in_done[kPipeSlots] = {}, comp_done[kPipeSlots] = {}, out_done[kPipeSlots] = {};
+    std::mutex mu;
+};
+Pipe g_pipe[kMaxDevices];
+
+ql_status pipe_for_device(Pipe*& out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QL_ERR_CUDA;
+    Pipe& p = g_pipe[dev];
+    if (!p.ready) {
+        const unsigned fl = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&p.start, fl) != cudaSuccess || cudaEventCreateWithFlags(&p.end, fl) != cudaSuccess)
+            return QL_ERR_CUDA;
+        for (int i = 0; i < kPipeSlots; ++i)
+            if (cudaEventCreateWithFlags(&p.in_done[i], fl) != cudaSuccess ||
+                cudaEventCreateWithFlags(&p.comp_done[i], fl) != cudaSuccess ||
+                cudaEventCreateWithFlags(&p.out_done[i], fl) != cudaSuccess)
+                return QL_ERR_CUDA;
+        p.ready = true;
+    }
+    out = &p;
+    return QL_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Byte sizes of one slot's buffers: X rows (bf16), their E4M3 cast (rows of
+// ldq bytes), the M-major scales, and D rows (bf16).
+struct SlotLayout {
+    size_t x, q, s, d, total;
+    int64_t ldq, sld, scols;
+};
+
+SlotLayout slot_layout(int64_t n, int64_t k, int64_t rows, int fmt) {
+    SlotLayout L{};
+    L.ldq = (k + 15) / 16 * 16;
+    const int64_t g = (k + 127) / 128;
+    L.scols = (fmt == QL_SF_PACKED_UE8M0) ? (g + 3) / 4 : g;
+    L.sld = (rows + 3) / 4 * 4;
+    L.x = align256(static_cast<size_t>(rows) * k * 2);
+    L.q = align256(static_cast<size_t>(rows) * L.ldq);
+    L.s = align256(static_cast<size_t>(L.scols) * L.sld * 4);
+    L.d = align256(static_cast<size_t>(rows) * n * 2);
+    L.total = L.x + L.q + L.s + L.d;
+    return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -295,6 +357,77 @@ ql_status gemm_fp8_nt_fp8out(const uint8_t* a, int64_t lda, const void* sfa, int
     o.drecip = recip ? 1 : 0;
     return gemm_common(a, lda, sfa, sfa_stride_m, sfa_stride_k, b, ldb, sfb, sfb_stride_n, sfb_stride_k, fmt, d, ldd,
                        m, n, k, false, 0, reinterpret_cast<cudaStream_t>(stream), nullptr, 1, 0, &o);
+}
+
+size_t ql_cast_gemm_host_workspace_size(int64_t n, int64_t k, int64_t chunk_rows, int fmt) {
+    if (n <= 0 || k <= 0 || chunk_rows <= 0) return 0;
+    return kPipeSlots * slot_layout(n, k, chunk_rows, fmt).total;
+}
+
+ql_status ql_cast_gemm_host(const void* x_host, int64_t ldx, const uint8_t* b, int64_t ldb, const void* sfb,
+                            int64_t sfb_stride_n, int64_t sfb_stride_k, int fmt, uint16_t* d_host, int64_t ldd,
+                            int64_t m, int64_t n, int64_t k, int64_t chunk_rows, void* workspace, size_t ws_bytes,
+                            ql_stream_t stream) {
+    if (m < 0 || n < 0 || k <= 0 || chunk_rows <= 0) return QL_ERR_INVALID_ARG;
+    if (fmt < QL_SF_FP32 || fmt > QL_SF_PACKED_UE8M0) return QL_ERR_INVALID_ARG;
+    if (m == 0 || n == 0) return QL_OK;
+    if (x_host == nullptr || d_host == nullptr || b == nullptr || sfb == nullptr || workspace == nullptr)
+        return QL_ERR_INVALID_ARG;
+    if (ldx < k || ldd < n) return QL_ERR_INVALID_ARG;
+    const SlotLayout sl = slot_layout(n, k, chunk_rows, fmt);
+    if (ws_bytes < kPipeSlots * sl.total) return QL_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QL_ERR_ALIGNMENT;
+    Pipe* pp = nullptr;
+    ql_status st = pipe_for_device(pp);
+    if (st != QL_OK) return st;
+    Pipe& P = *pp;
+    std::lock_guard<std::mutex> lk(P.mu);
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    auto ck = [](cudaError_t e) { return e == cudaSuccess; };
+    // the pipeline starts after the caller's earlier work and the caller's
+    // stream resumes after its last copy
+    if (!ck(cudaEventRecord(P.start, cs)) || !ck(cudaStreamWaitEvent(P.in, P.start, 0)) ||
+        !ck(cudaStreamWaitEvent(P.comp, P.start, 0)) || !ck(cudaStreamWaitEvent(P.out, P.start, 0)))
+        return QL_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int64_t chunks = (m + chunk_rows - 1) / chunk_rows;
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int slot = static_cast<int>(c % kPipeSlots);
+        const int64_t r0 = c * chunk_rows;
+        const int64_t rc = (m - r0) < chunk_rows ? (m - r0) : chunk_rows;
+        uint8_t* base = ws + slot * sl.total;
+        uint16_t* xb = reinterpret_cast<uint16_t*>(base);
+        uint8_t* qb = base + sl.x;
+        void* sb = base + sl.x + sl.q;
+        uint16_t* db = reinterpret_cast<uint16_t*>(base + sl.x + sl.q + sl.s);
+        // copy in: the slot's X buffer is free once chunk c - slots was cast
+        if (c >= kPipeSlots && !ck(cudaStreamWaitEvent(P.in, P.comp_done[slot], 0))) return QL_ERR_CUDA;
+        if (!ck(cudaMemcpy2DAsync(xb, static_cast<size_t>(k) * 2,
+                                  static_cast<const uint8_t*>(x_host) + static_cast<size_t>(r0) * ldx * 2,
+                                  static_cast<size_t>(ldx) * 2, static_cast<size_t>(k) * 2, static_cast<size_t>(rc),
+                                  cudaMemcpyHostToDevice, P.in)) ||
+            !ck(cudaEventRecord(P.in_done[slot], P.in)))
+            return QL_ERR_CUDA;
+        // cast + GEMM: after the copy in, and after the slot's D went out
+        if (!ck(cudaStreamWaitEvent(P.comp, P.in_done[slot], 0))) return QL_ERR_CUDA;
+        if (c >= kPipeSlots && !ck(cudaStreamWaitEvent(P.comp, P.out_done[slot], 0))) return QL_ERR_CUDA;
+        st = fp8_cast_per_token(xb, QL_BF16, rc, k, k, 1, 128, fmt, qb, sl.ldq, 1, sb, 1, sl.sld,
+                                reinterpret_cast<ql_stream_t>(P.comp));
+        if (st != QL_OK) return st;
+        st = gemm_fp8_nt_bf16(qb, sl.ldq, sb, 1, sl.sld, b, ldb, sfb, sfb_stride_n, sfb_stride_k, fmt, db, n, rc, n, k,
+                              nullptr, 0, reinterpret_cast<ql_stream_t>(P.comp));
+        if (st != QL_OK) return st;
+        if (!ck(cudaEventRecord(P.comp_done[slot], P.comp))) return QL_ERR_CUDA;
+        // copy out
+        if (!ck(cudaStreamWaitEvent(P.out, P.comp_done[slot], 0)) ||
+            !ck(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(d_host) + static_cast<size_t>(r0) * ldd * 2,
+                                  static_cast<size_t>(ldd) * 2, db, static_cast<size_t>(n) * 2,
+                                  static_cast<size_t>(n) * 2, static_cast<size_t>(rc), cudaMemcpyDeviceToHost, P.out)) ||
+            !ck(cudaEventRecord(P.out_done[slot], P.out)))
+            return QL_ERR_CUDA;
+    }
+    if (!ck(cudaEventRecord(P.end, P.out)) || !ck(cudaStreamWaitEvent(cs, P.end, 0))) return QL_ERR_CUDA;
+    return QL_OK;
 }
 
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k) {

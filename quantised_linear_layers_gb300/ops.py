@@ -41,6 +41,9 @@ _SIGS = {
                                _i64, _i64, _i64, _int, _vp],
     "gemm_fp8_nn_bf16": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
                          _i64, _i64, _i64, _vp],
+    "ql_cast_gemm_host_workspace_size": [_i64, _i64, _i64, _int],
+    "ql_cast_gemm_host": [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64, _i64, _i64, _i64, _i64,
+                          _vp, _sz, _vp],
     "ql_gemm_workspace_size": [_i64, _i64, _i64],
     "ql_set_num_sms": [_int],
     "ql_get_num_sms": [],
@@ -73,6 +76,7 @@ def load_library(path: str = LIB_PATH):
                 fn.restype = _int
             lib.ql_status_string.restype = ctypes.c_char_p
             lib.ql_gemm_workspace_size.restype = _sz
+            lib.ql_cast_gemm_host_workspace_size.restype = _sz
             _lib = lib
     return _lib
 
@@ -328,6 +332,37 @@ def gemm_fp8_nn_bf16(a: torch.Tensor, sfa: torch.Tensor, b_kn: torch.Tensor, sfb
         fmt, out.data_ptr(), out.stride(0), m, n, k, _stream(a))
     _check("gemm_fp8_nn_bf16", st)
     return out
+
+
+def cast_gemm_host_workspace_size(n: int, k: int, chunk_rows: int, fmt: int) -> int:
+    return int(load_library().ql_cast_gemm_host_workspace_size(n, k, chunk_rows, fmt))
+
+
+def cast_gemm_host(x_host: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor, fmt: int, out_host: torch.Tensor,
+                   chunk_rows: int, workspace: torch.Tensor) -> torch.Tensor:
+    """out_host [m, n] = bf16(cast_per_token(x_host) @ b^T) with x_host / out_host
+    bf16 tensors in host memory (pinned for overlap), b / sfb on the device and
+    a device workspace of cast_gemm_host_workspace_size bytes; copies and
+    kernels of successive row chunks overlap. Stream-ordered on the current stream."""
+    if x_host.device.type != "cpu" or out_host.device.type != "cpu":
+        raise ValueError("x_host and out_host must be host tensors")
+    if x_host.dtype != torch.bfloat16 or out_host.dtype != torch.bfloat16:
+        raise ValueError("x_host and out_host must be bf16")
+    if x_host.stride(1) != 1 or out_host.stride(1) != 1 or b.stride(1) != 1:
+        raise ValueError("rows must be contiguous")
+    _bytes8(b)
+    m, k = x_host.shape
+    n = b.shape[0]
+    if b.shape[1] != k or tuple(out_host.shape) != (m, n):
+        raise ValueError("shapes of x_host, b and out_host do not agree")
+    if not workspace.is_cuda or workspace.device != b.device:
+        raise ValueError("workspace must be device memory on b's device")
+    st = load_library().ql_cast_gemm_host(
+        x_host.data_ptr(), x_host.stride(0), b.data_ptr(), b.stride(0), sfb.data_ptr(), sfb.stride(0), sfb.stride(1),
+        fmt, out_host.data_ptr(), out_host.stride(0), m, n, k, chunk_rows,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(b))
+    _check("ql_cast_gemm_host", st)
+    return out_host
 
 
 def set_num_sms(n: int) -> None:

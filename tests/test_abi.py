@@ -98,6 +98,12 @@ def test_host_validation_rejects_before_cuda(lib):
     assert G(p, 32, p, 1, 1, p, 32, p, 1, 1, 1, 0, p, 8, p, 2, 128, 8, 0, None) == 2
     assert G(None, 32, None, 1, 1, None, 32, None, 1, 1, 1, 0, None, 8, None, 2, 0, 8, 32, None) == 0
     assert L.ql_get_m_alignment_for_contiguous_layout() == 128
+    # host pipeline: workspace too small, chunk_rows 0, unknown format (host checks only)
+    H = L.ql_cast_gemm_host
+    assert H(p, 64, p, 64, p, 1, 1, 0, p, 64, 64, 64, 64, 16, p, 10, None) == 1
+    assert H(p, 64, p, 64, p, 1, 1, 0, p, 64, 64, 64, 64, 0, p, 1 << 30, None) == 1
+    assert H(p, 64, p, 64, p, 1, 1, 7, p, 64, 64, 64, 64, 16, p, 1 << 30, None) == 1
+    assert L.ql_cast_gemm_host_workspace_size(64, 64, 16, 0) > 0
     # GEMM with E4M3 output: group 64, unknown format, recip with UE8M0, no scale buffer, k == 0
     F = L.gemm_fp8_nt_fp8out
     assert F(p, 32, p, 1, 1, p, 32, p, 1, 1, 0, p, 32, p, 1, 1, 64, 0, 4, 8, 32, None) == 1
