@@ -302,6 +302,37 @@ ql_status ql_cast_gemm_host(const void* x_host, int64_t ldx, const uint8_t* b, i
                             uint16_t* d_host, int64_t ldd, int64_t m, int64_t n, int64_t k,
                             int64_t chunk_rows, void* workspace, size_t ws_bytes, ql_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * ql_cast_gemm_host_noalloc
+ * The pages have no counterpart to this call. It is ql_cast_gemm_host for
+ * callers that cannot allocate device memory when they call it: a plug-in
+ * inside an application whose device memory is all owned by the
+ * application's own pool, or a serving process that makes no new device
+ * allocation after warm-up so that its footprint stays fixed. Instead of a
+ * caller-supplied workspace, the row chunks are staged in one array of
+ * QL_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU that loads
+ * the library holds that array until the process exits. The call allocates
+ * nothing.
+ *   Arguments as ql_cast_gemm_host without the workspace. chunk_rows must be
+ *   small enough that ql_cast_gemm_host_workspace_size(n, k, chunk_rows, fmt)
+ *   <= QL_NOALLOC_SCRATCH_BYTES, else QL_ERR_UNSUPPORTED (the call needs more
+ *   staging than the array holds: pass fewer rows per chunk).
+ *   The first call on a device looks up the array's device address and, if
+ *   ql_cast_gemm_host has not run on that device yet, creates the pipeline's
+ *   three streams and its events (driver objects, no device memory); make that
+ *   first call before any stream capture.
+ *   All calls share the array, and each call writes every staged byte before
+ *   reading it, so nothing needs to start at zero. Calls ordered on one
+ *   stream are safe; calls that overlap on the GPU (for example issued on two
+ *   streams without ordering) race on the array and may corrupt each other's
+ *   results.
+ * ------------------------------------------------------------------------- */
+#define QL_NOALLOC_SCRATCH_BYTES (64u << 20)
+ql_status ql_cast_gemm_host_noalloc(const void* x_host, int64_t ldx, const uint8_t* b, int64_t ldb,
+                                    const void* sfb, int64_t sfb_stride_n, int64_t sfb_stride_k, int fmt,
+                                    uint16_t* d_host, int64_t ldd, int64_t m, int64_t n, int64_t k,
+                                    int64_t chunk_rows, ql_stream_t stream);
+
 /* Workspace bytes a GEMM of this shape needs (0 in this build). */
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k);
 

@@ -44,6 +44,8 @@ _SIGS = {
     "ql_cast_gemm_host_workspace_size": [_i64, _i64, _i64, _int],
     "ql_cast_gemm_host": [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64, _i64, _i64, _i64, _i64,
                           _vp, _sz, _vp],
+    "ql_cast_gemm_host_noalloc": [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64, _i64, _i64, _i64, _i64,
+                                  _vp],
     "ql_gemm_workspace_size": [_i64, _i64, _i64],
     "ql_set_num_sms": [_int],
     "ql_get_num_sms": [],
