@@ -24,6 +24,14 @@
 // Exit: a cluster barrier; then the leader drains every copy either CTA
 // issued (balancing stages that only one side armed or issued, after a
 // time-out); a second cluster barrier; then tensor memory is freed.
+//
+// Tile width: 256 columns leave room in tensor memory (512 columns) for one
+// fp32 accumulator beside the exponents, so the next tile's MMAs wait until
+// both epilogues have read the last one out. 224-column tiles fit two
+// accumulators (at columns 0 and 256) and the exponents (at 480): the MMAs of
+// tile t+1 run while the epilogues drain tile t. The 224-wide form is the
+// default; 256 remains for the E4M3-output epilogue (whole 128-column groups
+// per thread) and for MN-major B (one 128-byte swizzle atom per CTA).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,28 +47,33 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kMathThreads = 256;
 constexpr int BM = 128;      // rows of A per CTA (256 per pair)
-constexpr int BN = 256;      // columns of D per pair
-constexpr int BNH = 128;     // rows of B per CTA
 constexpr int BK = 128;
 constexpr int kSfSlots = 8;
 
+// BN: columns of D per pair (256 or 224); each CTA holds BN / 2 rows of B.
+template <int BN>
 struct Mx2Cfg {
+    static constexpr int BNH = BN / 2;
     static constexpr int kStageA = BM * BK;
     static constexpr int kStageB = BNH * BK;
     static constexpr int kStageBytes = kStageA + kStageB;
     static constexpr int kStages = 6;
-    static constexpr int kSfbChunks = 2;         // all 256 B rows in each CTA
+    static constexpr int kSfbChunks = 2;         // all B rows of the tile (up to 256) in each CTA
     static constexpr int kSfCols = 4 + 4 * kSfbChunks;
-    static constexpr int kSfColBase = BN;
     static constexpr int kTmemCols = 512;
+    static constexpr int kAccStride = 256;       // accumulator stages start on 256-column boundaries
+    static constexpr int kAccStages = (kAccStride + BN + 2 * kSfCols <= kTmemCols) ? 2 : 1;
+    static constexpr int kSfColBase = (kAccStages - 1) * kAccStride + BN;
     static constexpr int kSlotWords = BM + 128 * kSfbChunks;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kStageA;
     static constexpr int kOffSf = kOffB + kStages * kStageB;
     static constexpr int kOffBar = kOffSf + kSfSlots * kSlotWords * 4;
-    static constexpr int kNumBars = 2 * kStages + 2 + 2 * kSfSlots + 2 + 1;
+    static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 2 * kSfSlots + 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static_assert(BN % 32 == 0 && BN <= 256, "pair tile width");
+    static_assert(kStageB % 1024 == 0, "B stages stay 1024-byte aligned for the 128-byte swizzle");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kSfColBase + 2 * kSfCols <= kTmemCols, "tensor memory budget");
 };
@@ -106,11 +119,12 @@ __device__ __forceinline__ void exp_words(const void* base, int fmt, const int64
     }
 }
 
-template <bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
+template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmParams p) {
-    using C = Mx2Cfg;
+    using C = Mx2Cfg<BN>;
+    constexpr int BNH = C::BNH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + C::kOffA;
@@ -119,9 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint64_t* full = bars;                       // leader: both CTAs' copies landed
     uint64_t* empty = full + C::kStages;         // stage free (multicast commit)
-    uint64_t* tfull = empty + C::kStages;        // accumulator ready (multicast commit)
-    uint64_t* tempty = tfull + 1;                // leader: both epilogues drained TMEM
-    uint64_t* sfull = tempty + 1;                // leader: both CTAs' exponent slots written
+    uint64_t* tfull = empty + C::kStages;        // [kAccStages] accumulator ready (multicast commit)
+    uint64_t* tempty = tfull + C::kAccStages;    // [kAccStages] leader: both epilogues drained it
+    uint64_t* sfull = tempty + C::kAccStages;    // leader: both CTAs' exponent slots written
     uint64_t* sempty = sfull + kSfSlots;         // exponent slot free (multicast commit)
     uint64_t* sftfree = sempty + kSfSlots;       // leader: TMEM exponent stage free
     uint64_t* done_bar = sftfree + 2;
@@ -142,8 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[s], 1);
         }
         *peer_issued = 0;
-        mbar_init(tfull, 1);
-        mbar_init(tempty, 2 * kMathThreads);
+        for (int s = 0; s < C::kAccStages; ++s) {
+            mbar_init(&tfull[s], 1);
+            mbar_init(&tempty[s], 2 * kMathThreads);
+        }
         for (int s = 0; s < kSfSlots; ++s) { mbar_init(&sfull[s], 64); mbar_init(&sempty[s], 1); }
         mbar_init(&sftfree[0], 1);
         mbar_init(&sftfree[1], 1);
@@ -221,8 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t it = 0, g = 0, tc = 0;
                     bool ok = true;
                     for (int t = cid; t < num_tiles && ok; t += ncl, ++tc) {
-                        if (!mbar_wait_cluster(tempty, (tc & 1u) ^ 1u, ctl)) { ok = false; break; }
+                        const uint32_t as = tc % C::kAccStages, aph = (tc / C::kAccStages) & 1u;
+                        if (!mbar_wait_cluster(&tempty[as], aph ^ 1u, ctl)) { ok = false; break; }
                         tc_fence_after_sync();
+                        const uint32_t d_tmem = tmem_base + as * C::kAccStride;
                         for (int kg = 0; kg < num_groups && ok; ++kg, ++g) {
                             const uint32_t slot = g % kSfSlots, sph = (g / kSfSlots) & 1u;
                             const uint32_t st = g & 1u;
@@ -249,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const uint64_t astep = k32_step(p.a_mn), bstep = k32_step(p.b_mn);
 #pragma unroll
                                 for (int k4 = 0; k4 < BK / 32; ++k4)
-                                    mma_mxf8_block_scaled_pair(tmem_base, adesc + astep * k4, bdesc + bstep * k4, idesc,
+                                    mma_mxf8_block_scaled_pair(d_tmem, adesc + astep * k4, bdesc + bstep * k4, idesc,
                                                                sf_col, sf_col + 4, (kb > 0 || k4 > 0) ? 1u : 0u);
                                 mma_commit_pair_multicast(&empty[s], 0x3);
                                 ++it;
@@ -259,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_commit_pair_multicast(&sftfree[st], 0x1);
                         }
                         if (!ok) break;
-                        mma_commit_pair_multicast(tfull, 0x3);
+                        mma_commit_pair_multicast(&tfull[as], 0x3);
                     }
                     mma_commit_pair_multicast(done_bar, 0x1);
                     mbar_wait_drain(done_bar, 0, p.wait_limit_ns);
@@ -268,8 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         } else {
             // ---------------- exponent loaders (both CTAs) ----------------
-            constexpr int R = PER_ROW_B ? 2 : 4;
-            constexpr int NB = PER_ROW_B ? 4 * C::kSfbChunks : C::kSfbChunks;
+            // a word per B row when B has per-row exponents or when the tile's
+            // rows do not start on a 128-row block (224-wide tiles)
+            constexpr bool kRowWords = PER_ROW_B || (BN % 128 != 0);
+            constexpr int R = kRowWords ? 2 : 4;
+            constexpr int NB = kRowWords ? 4 * C::kSfbChunks : C::kSfbChunks;
             const uint32_t mine = static_cast<uint32_t>(warp - 2);
             const int run_len = (p.fmt == 2) ? R : 1;
             const uint32_t leader_sfull0 = mapa_shared(&sfull[0], 0);
@@ -295,10 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int i = 0; i < NB; ++i) {
-                        if constexpr (PER_ROW_B) {
+                        if constexpr (kRowWords) {
                             const int64_t row = b_row0 + 32 * i + lane;    // chunk i/4, quarter i%4
-                            valb[i] = row < p.n;
-                            offb[i] = row * p.sbn;
+                            valb[i] = row < p.n && 32 * i + lane < BN;
+                            offb[i] = PER_ROW_B ? row * p.sbn : (row / 128) * p.sbn;
                         } else {
                             const int64_t r = b_row0 / 128 + i;            // chunk i: one block word
                             valb[i] = r < nblocks_b;
@@ -330,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < C::kSfbChunks; ++c) {
                             uint4 v;
-                            if constexpr (PER_ROW_B) {
+                            if constexpr (kRowWords) {
                                 v = make_uint4(wb[j][4 * c], wb[j][4 * c + 1], wb[j][4 * c + 2], wb[j][4 * c + 3]);
                             } else {
                                 v = make_uint4(wb[j][c], wb[j][c], wb[j][c], wb[j][c]);
@@ -355,23 +376,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r_local = q * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const bool vec_store = p.vec_store != 0;
-        const uint32_t leader_tempty = mapa_shared(tempty, 0);
+        const uint32_t leader_tempty0 = mapa_shared(&tempty[0], 0);
         uint32_t tc = 0;
         for (int t = cid; t < num_tiles; t += ncl, ++tc) {
             int mb, nb;
             tile_coords(t, p, mb, nb);
-            if (!warp_wait(tfull, tc & 1u, ctl)) break;
+            const uint32_t as = tc % C::kAccStages, aph = (tc / C::kAccStages) & 1u;
+            if (!warp_wait(&tfull[as], aph, ctl)) break;
             tc_fence_after_sync();
             uint32_t accb[CPT];
-            const uint32_t tcol = tmem_base + lane_base + wg * CPT;
+            const uint32_t tcol = tmem_base + lane_base + as * C::kAccStride + wg * CPT;
+            if constexpr (CPT % 32 == 0) {
 #pragma unroll
-            for (int c0 = 0; c0 < CPT; c0 += 32)
-                tmem_ld_32x32b_x32(tcol + c0, *reinterpret_cast<uint32_t(*)[32]>(&accb[c0]));
-            tmem_wait_ld(accb);            // one wait for all four loads
+                for (int c0 = 0; c0 < CPT; c0 += 32)
+                    tmem_ld_32x32b_x32(tcol + c0, *reinterpret_cast<uint32_t(*)[32]>(&accb[c0]));
+            } else {
+                // 16-column loads, each starting on a 16-column boundary
+#pragma unroll
+                for (int c0 = 0; c0 < CPT; c0 += 16)
+                    tmem_ld_32x32b_x16(tcol + c0, *reinterpret_cast<uint32_t(*)[16]>(&accb[c0]));
+            }
+            tmem_wait_ld(accb);            // one wait for all loads
             float* acc = reinterpret_cast<float*>(accb);
             tc_fence_before_sync();
-            if (leader) mbar_arrive(tempty);
-            else mbar_arrive_remote(leader_tempty);
+            if (leader) mbar_arrive(&tempty[as]);
+            else mbar_arrive_remote(leader_tempty0 + as * 8u);
             const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + r_local;
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
             if (row < p.m) {
@@ -447,9 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
+template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
-    using Cf = Mx2Cfg;
+    using Cf = Mx2Cfg<BN>;
+    constexpr int BNH = Cf::BNH;
     CUtensorMap ta, tb;
     if (!(L.a_mn ? encode_kmajor_map(&ta, L.a, L.k, L.m, L.lda, BK) : encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)))
         return cudaErrorInvalidValue;
@@ -461,7 +491,7 @@ cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int
     int pairs = num_sms / 2;
     if (pairs < 1) pairs = 1;
     if (tiles < pairs) pairs = tiles;
-    auto kern = gemm_mx2_kernel<PER_ROW_B, OUT_F32, OUT_FP8>;
+    auto kern = gemm_mx2_kernel<BN, PER_ROW_B, OUT_F32, OUT_FP8>;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
@@ -497,9 +527,13 @@ cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int
 }  // namespace
 
 cudaError_t launch_gemm_mx2(const GemmLaunch& L, const GemmParams& p, cudaStream_t st, int num_sms) {
-    if (L.out_fp8) return launch_mx2_t<false, false, true>(L, p, st, num_sms);
-    if (L.out_f32) return launch_mx2_t<true, true>(L, p, st, num_sms);
-    return launch_mx2_t<false, false>(L, p, st, num_sms);
+    if (L.out_fp8) return launch_mx2_t<256, false, false, true>(L, p, st, num_sms);
+    if (L.b_mn) {
+        if (L.out_f32) return launch_mx2_t<256, true, true>(L, p, st, num_sms);
+        return launch_mx2_t<256, false, false>(L, p, st, num_sms);
+    }
+    if (L.out_f32) return launch_mx2_t<224, true, true>(L, p, st, num_sms);
+    return launch_mx2_t<224, false, false>(L, p, st, num_sms);
 }
 
 }  // namespace ql
