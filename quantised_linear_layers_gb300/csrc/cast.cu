@@ -13,6 +13,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "cast.cuh"
 #include "common.cuh"
 #include "gemm.cuh"
@@ -40,7 +42,7 @@ __global__ void __launch_bounds__(256, 4) cast_rows_kernel(const T* __restrict__
                                                         uint8_t* __restrict__ out, int64_t ldo,
                                                         void* __restrict__ sf, int64_t ssm, int64_t ssg,
                                                         int64_t chunks_per_row, int vec_in, int vec_out) {
-    pdl_launch_dependents();    // a dependent GEMM may start its prologue
+    pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int kElemsPerLane = 64 / sizeof(T);          // 32 (bf16) or 16 (fp32)
     constexpr int kChunk = 32 * kElemsPerLane;
     constexpr int kLanesPerGroup = GRAN / kElemsPerLane;   // 1, 2, 4 or 8
@@ -134,6 +136,8 @@ __global__ void __launch_bounds__(256, 4) cast_rows_kernel(const T* __restrict__
                 static_cast<int32_t*>(sf)[row * ssm + (g / 4) * ssg] = static_cast<int32_t>(word);
         }
     }
+    // this CTA's work is done: the next kernel of the stream may be scheduled
+    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(256, 1) cast_cols_kernel(const T* __restrict__
                                                            uint8_t* __restrict__ out, int64_t ldo,
                                                            void* __restrict__ sf, int64_t ssm, int64_t ssg,
                                                            int vec_in, int vec_out) {
-    pdl_launch_dependents();    // a dependent GEMM may start its prologue
+    pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int V = 16 / sizeof(T);          // 8 (bf16) or 4 (fp32)
     constexpr int WI = 4 * V;                  // logical rows per warp
     constexpr int WJ = 128;                    // group-axis extent of a subtile
@@ -255,6 +259,8 @@ __global__ void __launch_bounds__(256, 1) cast_cols_kernel(const T* __restrict__
                 static_cast<int32_t*>(sf)[i * ssm + (g0 / 4) * ssg] = static_cast<int32_t>(ebytes[c]);
         }
     }
+    // this CTA's work is done: the next kernel of the stream may be scheduled
+    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(96) cast_cols_tma_kernel(const __grid_constant
                                                           int64_t n, uint8_t* __restrict__ out, int64_t ldo,
                                                           void* __restrict__ sf, int64_t ssm, int64_t ssg,
                                                           int vec_out, uint32_t* dev_status, uint64_t limit_ns) {
-    pdl_launch_dependents();    // a dependent GEMM may start its prologue
+    pdl_wait_prior();           // the previous kernel's writes are complete and visible
     using namespace cols_tma;
     constexpr int V = 16 / sizeof(T);
     constexpr int BI = 128 / sizeof(T);        // columns per box
@@ -419,6 +425,8 @@ __global__ void __launch_bounds__(96) cast_cols_tma_kernel(const __grid_constant
         }
     }
     __syncthreads();
+    // this CTA's work is done: the next kernel of the stream may be scheduled
+    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restri
                                                                int64_t ldx, uint8_t* __restrict__ out, int64_t ldo,
                                                                void* __restrict__ sf, int64_t ssm, int64_t ssg,
                                                                int vec_in, int vec_out) {
-    pdl_launch_dependents();    // a dependent GEMM may start its prologue
+    pdl_wait_prior();           // the previous kernel's writes are complete and visible
     using namespace colmajor;
     constexpr int V = kLaneBytes / sizeof(T);       // columns per lane (4 bf16 or 2 fp32)
     constexpr int R = kRowsPerWarp;
@@ -547,6 +555,8 @@ __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restri
             }
         }
     }
+    // this CTA's work is done: the next kernel of the stream may be scheduled
+    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -574,7 +584,7 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
     cast_colmajor_tma_kernel(const __grid_constant__ CUtensorMap tmap, int64_t m, int64_t n, uint8_t* __restrict__ out,
                              int64_t ldo, void* __restrict__ sf, int64_t ssm, int64_t ssg, int vec_out,
                              uint32_t* dev_status, uint64_t limit_ns) {
-    pdl_launch_dependents();    // a dependent GEMM may start its prologue
+    pdl_wait_prior();           // the previous kernel's writes are complete and visible
     using namespace colmajor_tma;
     constexpr int V = 8 / sizeof(T);                 // columns per lane (4 bf16 or 2 fp32)
     constexpr int BI = 256 / sizeof(T);              // columns (logical rows i) per box
@@ -727,6 +737,8 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
         }
     }
     __syncthreads();
+    // this CTA's work is done: the next kernel of the stream may be scheduled
+    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -738,7 +750,7 @@ __global__ void __launch_bounds__(128) cast_generic_kernel(const T* __restrict__
                                                            int64_t sxm, int64_t sxn, uint8_t* __restrict__ out,
                                                            int64_t som, int64_t son, void* __restrict__ sf,
                                                            int64_t ssm, int64_t ssg) {
-    pdl_launch_dependents();    // a dependent GEMM may start its prologue
+    pdl_wait_prior();           // the previous kernel's writes are complete and visible
     const int64_t G = (n + GRAN - 1) / GRAN;
     const int64_t W = (G + 3) / 4;
     const int64_t total = m * W;
@@ -763,6 +775,8 @@ __global__ void __launch_bounds__(128) cast_generic_kernel(const T* __restrict__
         }
         if constexpr (FMT == kSfPacked) static_cast<int32_t*>(sf)[i * ssm + w * ssg] = static_cast<int32_t>(word);
     }
+    // this CTA's work is done: the next kernel of the stream may be scheduled
+    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -779,7 +793,7 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
                                                          uint8_t* __restrict__ out, int64_t som, int64_t son,
                                                          int out_mode, void* __restrict__ sf, int64_t ssr,
                                                          int64_t ssc) {
-    pdl_launch_dependents();    // a dependent GEMM may start its prologue
+    pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int B = 128;
     // E4M3 bytes of the block, [row][col] with a row pitch of 144 bytes (16-byte
     // rows: 8-byte stores, 16-byte loads) for row-contiguous input, or 129 bytes
@@ -956,9 +970,29 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
                 if (gc + e < n) out[gr * som + (gc + e) * son] = qbuf[line * pitch + off + e];
         }
     }
+    // this CTA's work is done: the next kernel of the stream may be scheduled
+    pdl_launch_dependents();
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel of the stream finishes; every cast kernel waits
+// for that kernel (griddepcontrol.wait) before it reads or writes memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 template <typename T, int GRAN, int FMT, bool RECIP>
 cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms) {
@@ -971,9 +1005,8 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         int64_t blocks = (warps + 7) / 8;
         const int64_t cap = static_cast<int64_t>(num_sms) * 8 * 4;   // enough warps for full-rate HBM
         if (blocks > cap) blocks = cap;
-        cast_rows_kernel<T, GRAN, FMT, RECIP><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-            x, a.m, a.n, a.sxm, a.out, a.som, a.sf, a.ssm, a.ssg, chunks, vec_in, vec_out);
-        return cudaGetLastError();
+        return launch_pdl(cast_rows_kernel<T, GRAN, FMT, RECIP>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                          x, a.m, a.n, a.sxm, a.out, a.som, a.sf, a.ssm, a.ssg, chunks, vec_in, vec_out);
     }
     if (a.sxm == 1 && a.som == 1 && a.tma_ok) {
         using namespace colmajor_tma;
@@ -996,9 +1029,8 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
             const int64_t units = ((a.m + BI - 1) / BI) * ((a.n + kRows - 1) / kRows);
             int64_t grid = num_sms;
             if (grid > units) grid = units;
-            kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tmap, a.m, a.n, a.out, a.son, a.sf, a.ssm, a.ssg,
-                                                                    vec_out, a.dev_status, a.wait_limit_ns);
-            return cudaGetLastError();
+            return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, st, tmap, a.m, a.n, a.out,
+                              a.son, a.sf, a.ssm, a.ssg, vec_out, a.dev_status, a.wait_limit_ns);
         }
     }
     if (a.sxm == 1 && a.som == 1) {
@@ -1006,9 +1038,8 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         const int vec_in = (reinterpret_cast<uintptr_t>(x) % 8 == 0) && ((a.sxn * static_cast<int64_t>(sizeof(T))) % 8 == 0);
         const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) % V) == 0) && (a.son % V == 0);
         dim3 grid(static_cast<unsigned>((a.m + 32 * V - 1) / (32 * V)), static_cast<unsigned>((a.n + 127) / 128));
-        cast_colmajor_kernel<T, GRAN, FMT, RECIP><<<grid, 32 * colmajor::kWarps, 0, st>>>(
-            x, a.m, a.n, a.sxn, a.out, a.son, a.sf, a.ssm, a.ssg, vec_in, vec_out);
-        return cudaGetLastError();
+        return launch_pdl(cast_colmajor_kernel<T, GRAN, FMT, RECIP>, grid, dim3(32 * colmajor::kWarps), 0, st, x, a.m,
+                          a.n, a.sxn, a.out, a.son, a.sf, a.ssm, a.ssg, vec_in, vec_out);
     }
     if (a.sxm == 1 && a.son == 1 && a.tma_ok) {
         using namespace cols_tma;
@@ -1028,9 +1059,8 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
             const int64_t units = ((a.m + BI - 1) / BI) * ((a.n + kUnit * kRows - 1) / (kUnit * kRows));
             int64_t grid = static_cast<int64_t>(num_sms) * 3;
             if (grid > units) grid = units;
-            kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tmap, a.m, a.n, a.out, a.som, a.sf, a.ssm, a.ssg,
-                                                                    vec_out, a.dev_status, a.wait_limit_ns);
-            return cudaGetLastError();
+            return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, st, tmap, a.m, a.n, a.out,
+                              a.som, a.sf, a.ssm, a.ssg, vec_out, a.dev_status, a.wait_limit_ns);
         }
     }
     if (a.sxm == 1 && a.son == 1) {
@@ -1040,18 +1070,16 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         constexpr int kRowsPerCta = (FMT == kSfPacked && GRAN == 128) ? 512 : 128;
         dim3 grid(static_cast<unsigned>((a.m + 32 * V - 1) / (32 * V)),
                   static_cast<unsigned>((a.n + kRowsPerCta - 1) / kRowsPerCta));
-        cast_cols_kernel<T, GRAN, FMT, RECIP><<<grid, 256, 0, st>>>(x, a.m, a.n, a.sxn, a.out, a.som, a.sf, a.ssm,
-                                                                     a.ssg, vec_in, vec_out);
-        return cudaGetLastError();
+        return launch_pdl(cast_cols_kernel<T, GRAN, FMT, RECIP>, grid, dim3(256), 0, st, x, a.m, a.n, a.sxn, a.out,
+                          a.som, a.sf, a.ssm, a.ssg, vec_in, vec_out);
     }
     const int64_t G = (a.n + GRAN - 1) / GRAN;
     const int64_t total = a.m * ((G + 3) / 4);
     int64_t blocks = (total + 127) / 128;
     if (blocks > static_cast<int64_t>(num_sms) * 16) blocks = static_cast<int64_t>(num_sms) * 16;
     if (blocks < 1) blocks = 1;
-    cast_generic_kernel<T, GRAN, FMT, RECIP><<<static_cast<unsigned>(blocks), 128, 0, st>>>(
-        x, a.m, a.n, a.sxm, a.sxn, a.out, a.som, a.son, a.sf, a.ssm, a.ssg);
-    return cudaGetLastError();
+    return launch_pdl(cast_generic_kernel<T, GRAN, FMT, RECIP>, dim3(static_cast<unsigned>(blocks)), dim3(128), 0, st,
+                      x, a.m, a.n, a.sxm, a.sxn, a.out, a.som, a.son, a.sf, a.ssm, a.ssg);
 }
 
 template <typename T, int GRAN>
@@ -1075,9 +1103,8 @@ cudaError_t launch_block_t(const CastBlockArgs& a, cudaStream_t st) {
     if (a.son == 1 && aligned16(a.out) && a.som % 16 == 0) out_mode = 0;
     else if (a.som == 1 && aligned16(a.out) && a.son % 16 == 0) out_mode = 1;
     dim3 grid(static_cast<unsigned>((a.n + 127) / 128), static_cast<unsigned>((a.m + 127) / 128));
-    cast_block_kernel<T, FMT, RECIP><<<grid, 256, 0, st>>>(x, a.m, a.n, a.sxm, a.sxn, in_mode, a.out, a.som, a.son,
-                                                          out_mode, a.sf, a.ssr, a.ssc);
-    return cudaGetLastError();
+    return launch_pdl(cast_block_kernel<T, FMT, RECIP>, grid, dim3(256), 0, st, x, a.m, a.n, a.sxm, a.sxn, in_mode,
+                      a.out, a.som, a.son, out_mode, a.sf, a.ssr, a.ssc);
 }
 
 template <typename T>
