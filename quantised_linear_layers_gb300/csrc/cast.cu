@@ -563,20 +563,26 @@ __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restri
 // TMA-staged column-major per-token cast (x_stride_m == 1, out_stride_m == 1,
 // 16-byte-aligned physical rows): the same operation as cast_colmajor_kernel,
 // with one producer thread streaming boxes of 128 physical rows x 256 bytes
-// into a 4-stage shared-memory ring (128 KB in flight per SM) and 16 consumer
-// warps, each taking 8 rows x 8 bytes per lane of a box. Per box the consumers
-// combine their column amaxes through shared memory, one warp per group turns
-// them into scales and factors, and every lane quantises its 8 rows and
-// stores 8 x V bytes; the stage is released as soon as its bytes are in
-// registers. Persistent CTAs walk the boxes row band by row band. Every wait
-// is bounded; on a time-out the CTA records it and drains its copies.
+// into a 4-stage shared-memory ring (128 KB in flight per SM) and two
+// consumer groups of 8 warps that take alternate boxes, so one group's
+// barriers and scale step overlap the other's loads and stores. In a group,
+// warp w takes rows 16w .. 16w+16 of the box and each lane 8 bytes of
+// columns; the group combines its column amaxes through shared memory, one
+// warp per 1 x GRAN group turns them into scales and factors, and every lane
+// quantises its 16 rows and stores them. The stage is released as soon as its
+// bytes are in registers. Persistent CTAs walk the boxes row band by row
+// band. Every wait is bounded; a group leaves its loop only by a vote of all
+// its warps (bar.red.or), so a time-out cannot strand a barrier.
 // ---------------------------------------------------------------------------
 namespace colmajor_tma {
 constexpr int kStages = 4;
 constexpr int kRows = 128;                   // physical rows (j) per box
 constexpr int kBoxBytes = kRows * 256;       // 32 KB
-constexpr int kConsumerWarps = 16;
+constexpr int kGroups = 2;                   // consumer groups, alternate boxes
+constexpr int kGroupWarps = 8;
+constexpr int kConsumerWarps = kGroups * kGroupWarps;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kRowsPerWarp = kRows / kGroupWarps;   // 16
 }  // namespace colmajor_tma
 
 template <typename T, int GRAN, int FMT, bool RECIP>
@@ -588,15 +594,17 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
     using namespace colmajor_tma;
     constexpr int V = 8 / sizeof(T);                 // columns per lane (4 bf16 or 2 fp32)
     constexpr int BI = 256 / sizeof(T);              // columns (logical rows i) per box
-    constexpr int R = 8;                             // rows per consumer warp
-    constexpr int WPG = GRAN / R;                    // consumer warps per group (16 or 4)
-    constexpr int NG = kConsumerWarps / WPG;         // groups per box (1 or 4)
+    constexpr int R = kRowsPerWarp;
+    constexpr int WPG = GRAN / R;                    // warps per 1 x GRAN group (8 or 2)
+    constexpr int NG = kGroupWarps / WPG;            // 1 x GRAN groups per box (1 or 4)
+    constexpr int kRed = kGroupWarps * 32 * (V + 1); // floats of one consumer group's partial amaxes
+    constexpr int kF = NG * 32 * V;                  // floats (or words) of its factors / exponents
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* red = reinterpret_cast<float*>(ring + kStages * kBoxBytes);            // [16][32][V+1]
-    float* fbuf = red + kConsumerWarps * 32 * (V + 1);                            // [NG][32][V]
-    uint32_t* ebuf = reinterpret_cast<uint32_t*>(fbuf + NG * 32 * V);             // [NG][32][V]
-    uint64_t* full = reinterpret_cast<uint64_t*>(ebuf + NG * 32 * V);
+    float* red_all = reinterpret_cast<float*>(ring + kStages * kBoxBytes);        // [kGroups][8][32][V+1]
+    float* fbuf_all = red_all + kGroups * kRed;                                   // [kGroups][NG][32][V]
+    uint32_t* ebuf_all = reinterpret_cast<uint32_t*>(fbuf_all + kGroups * kF);    // [kGroups][NG][32][V]
+    uint64_t* full = reinterpret_cast<uint64_t*>(ebuf_all + kGroups * kF);
     uint64_t* empty = full + kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
 
@@ -606,7 +614,7 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
     const int64_t units = strips * bands;
     const int64_t G = (n + GRAN - 1) / GRAN;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kConsumerWarps); }
+        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kGroupWarps); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -633,12 +641,20 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
         }
         __syncwarp();
     } else {
-        const int cw = warp - 1;                       // consumer warp: rows 8cw .. 8cw+8 of a box
-        const int w0 = (cw / WPG) * WPG;
-        const int grp = cw / WPG;
-        const bool group_lead = cw == w0;
-        uint32_t it = 0;
-        for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+        const int cw = warp - 1;
+        const int cg = cw / kGroupWarps;               // consumer group: boxes it = cg, cg + kGroups, ...
+        const int gw = cw % kGroupWarps;               // warp within the group: rows 16gw .. 16gw+16
+        const uint32_t bar_id = 1 + cg;
+        const uint32_t bar_n = 32 * kGroupWarps;
+        float* red = red_all + cg * kRed;
+        float* fbuf = fbuf_all + cg * kF;
+        uint32_t* ebuf = ebuf_all + cg * kF;
+        const int w0 = (gw / WPG) * WPG;               // first warp of this warp's 1 x GRAN group
+        const int grp = gw / WPG;
+        const bool group_lead = gw == w0;
+        uint32_t it = cg;
+        for (int64_t u = blockIdx.x + cg * static_cast<int64_t>(gridDim.x); u < units;
+             u += kGroups * static_cast<int64_t>(gridDim.x), it += kGroups) {
             const int64_t band = u / strips, strip = u % strips;
             const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], ph, ctl)) != 0;
@@ -647,7 +663,7 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
                 const uint8_t* box = ring + s * kBoxBytes;
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    raw[r] = *reinterpret_cast<const uint2*>(box + (cw * R + r) * 256 + lane * 8);
+                    raw[r] = *reinterpret_cast<const uint2*>(box + (gw * R + r) * 256 + lane * 8);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 float amax[V];
@@ -660,13 +676,13 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
                     for (int c = 0; c < V; ++c) amax[c] = fmaxf(amax[c], fabsf(to_f32(t[c])));
                 }
 #pragma unroll
-                for (int c = 0; c < V; ++c) red[(cw * 32 + lane) * (V + 1) + c] = amax[c];
+                for (int c = 0; c < V; ++c) red[(gw * 32 + lane) * (V + 1) + c] = amax[c];
             }
-            // every consumer warp arrives here once per box whatever its wait
-            // gave; if any wait ran out, all of them leave together
-            if (named_bar_or(1, 32 * kConsumerWarps, !ok)) break;
+            // every warp of the group arrives here once per box whatever its
+            // wait gave; if any wait ran out, the whole group leaves together
+            if (named_bar_or(bar_id, bar_n, !ok)) break;
             const int64_t i0 = strip * BI + lane * V;        // first logical row of this lane
-            const int64_t j0 = band * kRows + cw * R;        // first physical row of this warp
+            const int64_t j0 = band * kRows + gw * R;        // first physical row of this warp
             const int64_t g = (band * kRows + w0 * R) / GRAN;
             if (group_lead) {
 #pragma unroll
@@ -694,21 +710,21 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
                     }
                 }
             }
-            named_bar_sync(1, 32 * kConsumerWarps);
+            named_bar_sync(bar_id, bar_n);
             float f[V];
 #pragma unroll
             for (int c = 0; c < V; ++c) f[c] = fbuf[(grp * 32 + lane) * V + c];
             if constexpr (FMT == kSfPacked && GRAN == 32) {
-                if (cw == 0) {
-                    const int64_t gw = band * kRows / 32;   // first group of the box (a multiple of 4)
+                if (gw == 0) {
+                    const int64_t gwd = band * kRows / 32;   // first group of the box (a multiple of 4)
 #pragma unroll
                     for (int c = 0; c < V; ++c) {
                         const int64_t i = i0 + c;
-                        if (i < m && gw < G) {
+                        if (i < m && gwd < G) {
                             const uint32_t word = ebuf[(0 * 32 + lane) * V + c] | (ebuf[(1 * 32 + lane) * V + c] << 8) |
                                                   (ebuf[(2 * 32 + lane) * V + c] << 16) |
                                                   (ebuf[(3 * 32 + lane) * V + c] << 24);
-                            static_cast<int32_t*>(sf)[i * ssm + (gw / 4) * ssg] = static_cast<int32_t>(word);
+                            static_cast<int32_t*>(sf)[i * ssm + (gwd / 4) * ssg] = static_cast<int32_t>(word);
                         }
                     }
                 }
@@ -731,9 +747,9 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
                         if (i0 + c < m) dst[c] = static_cast<uint8_t>(w >> (8 * c));
                 }
             }
-            // red, fbuf and ebuf are rewritten for the next box only after every
-            // consumer has passed this barrier
-            named_bar_sync(1, 32 * kConsumerWarps);
+            // red, fbuf and ebuf are rewritten for the group's next box only
+            // after every warp of the group has passed this barrier
+            named_bar_sync(bar_id, bar_n);
         }
     }
     __syncthreads();
@@ -1016,8 +1032,8 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         if (encode_2d_map(&tmap, x, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                           a.n, a.m, a.sxn * static_cast<int64_t>(sizeof(T)), kRows, BI)) {
             const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) % V) == 0) && (a.son % V == 0);
-            constexpr int NG = kConsumerWarps / (GRAN / 8);
-            const int smem = kStages * kBoxBytes + kConsumerWarps * 32 * (V + 1) * 4 + 2 * NG * 32 * V * 4 +
+            constexpr int NG = kGroupWarps / (GRAN / kRowsPerWarp);
+            const int smem = kStages * kBoxBytes + kGroups * (kGroupWarps * 32 * (V + 1) + 2 * NG * 32 * V) * 4 +
                              2 * kStages * 8 + 16 + 1024;
             auto kern = cast_colmajor_tma_kernel<T, GRAN, FMT, RECIP>;
             static bool attr = false;
