@@ -560,61 +560,68 @@ __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restri
 }
 
 // ---------------------------------------------------------------------------
-// TMA-staged column-major per-token cast (x_stride_m == 1, out_stride_m == 1,
-// 16-byte-aligned physical rows): the same operation as cast_colmajor_kernel,
-// with one producer thread streaming boxes of 128 physical rows x 256 bytes
-// into a 4-stage shared-memory ring (128 KB in flight per SM) and two
-// consumer groups of 8 warps that take alternate boxes, so one group's
-// barriers and scale step overlap the other's loads and stores. In a group,
-// warp w takes rows 16w .. 16w+16 of the box and each lane 8 bytes of
-// columns; the group combines its column amaxes through shared memory, one
-// warp per 1 x GRAN group turns them into scales and factors, and every lane
-// quantises its 16 rows and stores them. The stage is released as soon as its
-// bytes are in registers. Persistent CTAs walk the boxes row band by row
-// band. Every wait is bounded; a group leaves its loop only by a vote of all
-// its warps (bar.red.or), so a time-out cannot strand a barrier.
+// Column-major per-token cast, one warp per column chunk (x_stride_m == 1,
+// out_stride_m == 1, 16-byte-aligned physical rows): the same operation as
+// cast_colmajor_kernel. One producer thread streams stages of 128 physical
+// rows (j) x 256 bytes, each two 128-byte-wide boxes loaded with the 128-byte
+// swizzle, into a 4-stage shared-memory ring. Each of the 16 consumer warps
+// owns one 16-byte column chunk of a stage (8 bf16 or 4 fp32 logical rows i)
+// over all 128 physical rows: lane l holds rows l, l+32, l+64 and l+96, which
+// the swizzle spreads over all banks. A 1 x GRAN group along j is one quarter
+// (GRAN 32) or all four quarters (GRAN 128) of the lanes' rows, so its column
+// amax is one warp reduction: redux.sync max on the float bits, which order as
+// the values do because every partial amax is a non-negative, non-NaN float
+// (each starts at 0 and fmaxf drops NaN). A warp releases the stage once its
+// bytes are in registers and computes its scales without waiting for any
+// other warp. For bf16 input with a 16-byte-aligned output, the E4M3 rows go
+// through a double-buffered 128 x 128-byte output tile (128-byte swizzle) that
+// one store thread writes back with a TMA tile store, so every write is a
+// full line; otherwise each lane stores its 8 or 4 bytes per row directly.
+// Persistent CTAs walk the stages row band by row band; every wait is bounded.
 // ---------------------------------------------------------------------------
-namespace colmajor_tma {
+namespace colmajor_sw {
 constexpr int kStages = 4;
-constexpr int kRows = 128;                   // physical rows (j) per box
-constexpr int kBoxBytes = kRows * 256;       // 32 KB
-constexpr int kGroups = 2;                   // consumer groups, alternate boxes
-constexpr int kGroupWarps = 8;
-constexpr int kConsumerWarps = kGroups * kGroupWarps;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);
-constexpr int kRowsPerWarp = kRows / kGroupWarps;   // 16
-}  // namespace colmajor_tma
+constexpr int kRows = 128;                     // physical rows (j) per stage
+constexpr int kHalfBytes = kRows * 128;        // one 128-byte-wide box, 16 KB
+constexpr int kStageBytes = 2 * kHalfBytes;
+constexpr int kOutBytes = kRows * 128;         // E4M3 output tile of a bf16 stage
+constexpr int kConsumerWarps = 16;             // 2 boxes x 8 chunks of 16 bytes
+constexpr int kThreads = 32 * (2 + kConsumerWarps);   // producer, consumers, store warp
+constexpr int kSmemBytes = kStages * kStageBytes + 2 * kOutBytes + 1024 + (2 * kStages + 4) * 8 + 16;
+}  // namespace colmajor_sw
 
 template <typename T, int GRAN, int FMT, bool RECIP>
-__global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
-    cast_colmajor_tma_kernel(const __grid_constant__ CUtensorMap tmap, int64_t m, int64_t n, uint8_t* __restrict__ out,
-                             int64_t ldo, void* __restrict__ sf, int64_t ssm, int64_t ssg, int vec_out,
-                             uint32_t* dev_status, uint64_t limit_ns) {
+__global__ void __launch_bounds__(colmajor_sw::kThreads, 1)
+    cast_colmajor_sw_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap omap,
+                            int64_t m, int64_t n, uint8_t* __restrict__ out, int64_t ldo, void* __restrict__ sf,
+                            int64_t ssm, int64_t ssg, int vec_out, int tma_out, uint32_t* dev_status,
+                            uint64_t limit_ns) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
-    using namespace colmajor_tma;
-    constexpr int V = 8 / sizeof(T);                 // columns per lane (4 bf16 or 2 fp32)
-    constexpr int BI = 256 / sizeof(T);              // columns (logical rows i) per box
-    constexpr int R = kRowsPerWarp;
-    constexpr int WPG = GRAN / R;                    // warps per 1 x GRAN group (8 or 2)
-    constexpr int NG = kGroupWarps / WPG;            // 1 x GRAN groups per box (1 or 4)
-    constexpr int kRed = kGroupWarps * 32 * (V + 1); // floats of one consumer group's partial amaxes
-    constexpr int kF = NG * 32 * V;                  // floats (or words) of its factors / exponents
+    using namespace colmajor_sw;
+    static_assert(GRAN == 32 || GRAN == 128, "groups of 32 or 128 rows");
+    constexpr int E = 16 / sizeof(T);              // columns (logical rows i) per warp
+    constexpr int BH = 128 / sizeof(T);            // columns per box
+    constexpr int BI = 2 * BH;                     // columns per stage
+    constexpr int QPG = GRAN / 32;                 // row quarters per 1 x GRAN group
+    constexpr int NGS = 4 / QPG;                   // groups per stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* red_all = reinterpret_cast<float*>(ring + kStages * kBoxBytes);        // [kGroups][8][32][V+1]
-    float* fbuf_all = red_all + kGroups * kRed;                                   // [kGroups][NG][32][V]
-    uint32_t* ebuf_all = reinterpret_cast<uint32_t*>(fbuf_all + kGroups * kF);    // [kGroups][NG][32][V]
-    uint64_t* full = reinterpret_cast<uint64_t*>(ebuf_all + kGroups * kF);
+    uint8_t* obuf = ring + kStages * kStageBytes;                  // [2][128 rows x 128 bytes], swizzled
+    uint64_t* full = reinterpret_cast<uint64_t*>(obuf + 2 * kOutBytes);
     uint64_t* empty = full + kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+    uint64_t* ofull = empty + kStages;                               // output tile written by all warps
+    uint64_t* oempty = ofull + 2;                                    // output tile read by its TMA store
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(oempty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t strips = (m + BI - 1) / BI;
     const int64_t bands = (n + kRows - 1) / kRows;
     const int64_t units = strips * bands;
     const int64_t G = (n + GRAN - 1) / GRAN;
+    const bool tile_out = sizeof(T) == 2 && tma_out != 0;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kGroupWarps); }
+        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kConsumerWarps); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&ofull[b], kConsumerWarps); mbar_init(&oempty[b], 1); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -626,13 +633,14 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
             tma_prefetch_desc(&tmap);
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+            for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++it) {
                 const int64_t band = u / strips, strip = u % strips;
                 const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
                 if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
-                mbar_arrive_expect_tx(&full[s], kBoxBytes);
-                tma_load_2d(ring + s * kBoxBytes, &tmap, &full[s], static_cast<int32_t>(strip * BI),
-                            static_cast<int32_t>(band * kRows));
+                mbar_arrive_expect_tx(&full[s], kStageBytes);
+                const int32_t x0 = static_cast<int32_t>(strip * BI), y0 = static_cast<int32_t>(band * kRows);
+                tma_load_2d(ring + s * kStageBytes, &tmap, &full[s], x0, y0);
+                tma_load_2d(ring + s * kStageBytes + kHalfBytes, &tmap, &full[s], x0 + BH, y0);
             }
             if (!ok) {
                 const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
@@ -640,116 +648,157 @@ __global__ void __launch_bounds__(colmajor_tma::kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (warp == kConsumerWarps + 1) {
+        if (tile_out && lane == 0) {
+            uint32_t it = 0;
+            for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+                const int64_t band = u / strips, strip = u % strips;
+                const uint32_t b = it & 1u;
+                if (!mbar_wait(&ofull[b], (it >> 1) & 1u, ctl)) break;
+                tma_store_2d(&omap, obuf + b * kOutBytes, static_cast<int32_t>(strip * BI),
+                             static_cast<int32_t>(band * kRows));
+                bulk_commit_group();
+                bulk_wait_read_but_one();                    // the previous tile has been read
+                if (it > 0) mbar_arrive(&oempty[b ^ 1u]);
+            }
+            bulk_wait_all();
+        }
+        __syncwarp();
     } else {
         const int cw = warp - 1;
-        const int cg = cw / kGroupWarps;               // consumer group: boxes it = cg, cg + kGroups, ...
-        const int gw = cw % kGroupWarps;               // warp within the group: rows 16gw .. 16gw+16
-        const uint32_t bar_id = 1 + cg;
-        const uint32_t bar_n = 32 * kGroupWarps;
-        float* red = red_all + cg * kRed;
-        float* fbuf = fbuf_all + cg * kF;
-        uint32_t* ebuf = ebuf_all + cg * kF;
-        const int w0 = (gw / WPG) * WPG;               // first warp of this warp's 1 x GRAN group
-        const int grp = gw / WPG;
-        const bool group_lead = gw == w0;
-        uint32_t it = cg;
-        for (int64_t u = blockIdx.x + cg * static_cast<int64_t>(gridDim.x); u < units;
-             u += kGroups * static_cast<int64_t>(gridDim.x), it += kGroups) {
-            const int64_t band = u / strips, strip = u % strips;
+        const int half = cw >> 3, chunk = cw & 7;
+        // byte offset of this lane's 16-byte chunk within a 128-byte swizzled row
+        // (rows l + 32q share l & 7, so one offset serves all four quarters)
+        const uint32_t col_off = static_cast<uint32_t>((chunk ^ (lane & 7)) << 4);
+        // (group, column) pairs of one stage; lane l turns pair l % NP into its scale
+        constexpr int NP = NGS * E;
+        static_assert(32 % NP == 0, "pairs divide the warp");
+        const int pl = lane % NP, p_gi = pl / E, p_e = pl % E;
+        int64_t band = blockIdx.x / strips, strip = blockIdx.x % strips;
+        uint32_t it = 0;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+            if (it > 0) {
+                strip += gridDim.x;
+                while (strip >= strips) { strip -= strips; ++band; }
+            }
             const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], ph, ctl)) != 0;
-            uint2 raw[R];
-            if (ok) {
-                const uint8_t* box = ring + s * kBoxBytes;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, ctl))) break;
+            const uint8_t* box = ring + s * kStageBytes + half * kHalfBytes;
+            uint4 raw[4];
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-                    raw[r] = *reinterpret_cast<const uint2*>(box + (gw * R + r) * 256 + lane * 8);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                float amax[V];
+            for (int q = 0; q < 4; ++q)
+                raw[q] = *reinterpret_cast<const uint4*>(box + (lane + 32 * q) * 128 + col_off);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+
+            const int64_t i0 = strip * BI + half * BH + chunk * E;   // first logical row of this warp
+            // this lane's |x| maxima per (group, column) as non-negative float bits
+            uint32_t am[NGS][E];
 #pragma unroll
-                for (int c = 0; c < V; ++c) amax[c] = 0.0f;
+            for (int gi = 0; gi < NGS; ++gi) {
+                if constexpr (sizeof(T) == 2) {
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const T* t = reinterpret_cast<const T*>(&raw[r]);
+                    for (int wd = 0; wd < 4; ++wd) {
+                        uint32_t mx = 0u;                    // bf16 pair max of |x| (sign bits cleared)
 #pragma unroll
-                    for (int c = 0; c < V; ++c) amax[c] = fmaxf(amax[c], fabsf(to_f32(t[c])));
-                }
-#pragma unroll
-                for (int c = 0; c < V; ++c) red[(gw * 32 + lane) * (V + 1) + c] = amax[c];
-            }
-            // every warp of the group arrives here once per box whatever its
-            // wait gave; if any wait ran out, the whole group leaves together
-            if (named_bar_or(bar_id, bar_n, !ok)) break;
-            const int64_t i0 = strip * BI + lane * V;        // first logical row of this lane
-            const int64_t j0 = band * kRows + gw * R;        // first physical row of this warp
-            const int64_t g = (band * kRows + w0 * R) / GRAN;
-            if (group_lead) {
-#pragma unroll
-                for (int c = 0; c < V; ++c) {
-                    float a = red[(w0 * 32 + lane) * (V + 1) + c];
-#pragma unroll
-                    for (int w = 1; w < WPG; ++w) a = fmaxf(a, red[((w0 + w) * 32 + lane) * (V + 1) + c]);
-                    float sc, f;
-                    uint32_t eb;
-                    group_scale<FMT, RECIP>(a, sc, f, eb);
-                    fbuf[(grp * 32 + lane) * V + c] = f;
-                    const int64_t i = i0 + c;
-                    if constexpr (FMT != kSfPacked) {
-                        if (i < m && g < G) static_cast<float*>(sf)[i * ssm + g * ssg] = sc;
-                    } else if constexpr (GRAN == 128) {
-                        if (i < m && g < G) {
-                            uint8_t* word =
-                                reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + i * ssm + (g / 4) * ssg);
-                            word[g % 4] = static_cast<uint8_t>(eb);
-                            if (g == G - 1)
-                                for (int z = static_cast<int>(g % 4) + 1; z < 4; ++z) word[z] = 0;
-                        }
-                    } else {
-                        ebuf[(grp * 32 + lane) * V + c] = (g < G) ? eb : 0u;
+                        for (int q = gi * QPG; q < (gi + 1) * QPG; ++q)
+                            mx = bf16x2_max(mx, reinterpret_cast<const uint32_t*>(&raw[q])[wd] & 0x7FFF7FFFu);
+                        am[gi][2 * wd] = mx << 16;
+                        am[gi][2 * wd + 1] = mx & 0xFFFF0000u;
                     }
-                }
-            }
-            named_bar_sync(bar_id, bar_n);
-            float f[V];
-#pragma unroll
-            for (int c = 0; c < V; ++c) f[c] = fbuf[(grp * 32 + lane) * V + c];
-            if constexpr (FMT == kSfPacked && GRAN == 32) {
-                if (gw == 0) {
-                    const int64_t gwd = band * kRows / 32;   // first group of the box (a multiple of 4)
-#pragma unroll
-                    for (int c = 0; c < V; ++c) {
-                        const int64_t i = i0 + c;
-                        if (i < m && gwd < G) {
-                            const uint32_t word = ebuf[(0 * 32 + lane) * V + c] | (ebuf[(1 * 32 + lane) * V + c] << 8) |
-                                                  (ebuf[(2 * 32 + lane) * V + c] << 16) |
-                                                  (ebuf[(3 * 32 + lane) * V + c] << 24);
-                            static_cast<int32_t*>(sf)[i * ssm + (gwd / 4) * ssg] = static_cast<int32_t>(word);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int64_t j = j0 + r;
-                if (j >= n) break;
-                const T* t = reinterpret_cast<const T*>(&raw[r]);
-                uint8_t* dst = out + j * ldo + i0;
-                uint32_t w = e4m3x2(__fmul_rn(to_f32(t[0]), f[0]), __fmul_rn(to_f32(t[1]), f[1]));
-                if constexpr (V == 4)
-                    w |= e4m3x2(__fmul_rn(to_f32(t[2]), f[2]), __fmul_rn(to_f32(t[3]), f[3])) << 16;
-                if (vec_out && i0 + V <= m) {
-                    if constexpr (V == 4) *reinterpret_cast<uint32_t*>(dst) = w;
-                    else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < V; ++c)
-                        if (i0 + c < m) dst[c] = static_cast<uint8_t>(w >> (8 * c));
+                    for (int e = 0; e < E; ++e) {
+                        float a = 0.0f;
+#pragma unroll
+                        for (int q = gi * QPG; q < (gi + 1) * QPG; ++q)
+                            a = fmaxf(a, fabsf(to_f32(reinterpret_cast<const T*>(&raw[q])[e])));
+                        am[gi][e] = __float_as_uint(a);
+                    }
                 }
             }
-            // red, fbuf and ebuf are rewritten for the group's next box only
-            // after every warp of the group has passed this barrier
-            named_bar_sync(bar_id, bar_n);
+            uint32_t mine = 0u;
+#pragma unroll
+            for (int gi = 0; gi < NGS; ++gi)
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const uint32_t v = __reduce_max_sync(0xffffffffu, am[gi][e]);
+                    if (pl == gi * E + e) mine = v;
+                }
+            float sc, fmine;
+            uint32_t eb;
+            group_scale<FMT, RECIP>(__uint_as_float(mine), sc, fmine, eb);
+            {
+                const int64_t i = i0 + p_e;
+                const int64_t g = band * NGS + p_gi;
+                if constexpr (FMT != kSfPacked) {
+                    if (lane < NP && i < m && g < G) static_cast<float*>(sf)[i * ssm + g * ssg] = sc;
+                } else if constexpr (GRAN == 128) {
+                    if (lane < NP && i < m && g < G) {
+                        uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + i * ssm + (g / 4) * ssg);
+                        word[g % 4] = static_cast<uint8_t>(eb);
+                        if (g == G - 1)
+                            for (int z = static_cast<int>(g % 4) + 1; z < 4; ++z) word[z] = 0;
+                    }
+                } else {
+                    // the stage's four 1 x 32 groups are the four bytes of word `band`
+                    const uint32_t b0 = (g < G) ? eb : 0u;
+                    const uint32_t b1 = __shfl_sync(0xffffffffu, b0, (lane + E) & 31);
+                    const uint32_t b2 = __shfl_sync(0xffffffffu, b0, (lane + 2 * E) & 31);
+                    const uint32_t b3 = __shfl_sync(0xffffffffu, b0, (lane + 3 * E) & 31);
+                    if (lane < E && i < m && band * 4 < G)
+                        static_cast<int32_t*>(sf)[i * ssm + band * ssg] =
+                            static_cast<int32_t>(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
+                }
+            }
+            float f[NGS][E];
+#pragma unroll
+            for (int gi = 0; gi < NGS; ++gi)
+#pragma unroll
+                for (int e = 0; e < E; ++e) f[gi][e] = __shfl_sync(0xffffffffu, fmine, gi * E + e);
+            uint8_t* otile = nullptr;
+            if (tile_out) {
+                const uint32_t b = it & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(&oempty[b], ((it >> 1) & 1u) ^ 1u, ctl))) break;
+                otile = obuf + b * kOutBytes;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = lane + 32 * q;
+                const int64_t j = band * kRows + r;
+                const T* t = reinterpret_cast<const T*>(&raw[q]);
+                const float* fq = f[q / QPG];
+                uint32_t w[E / 4];
+#pragma unroll
+                for (int b = 0; b < E / 4; ++b)
+                    w[b] = e4m3x2(__fmul_rn(to_f32(t[4 * b]), fq[4 * b]), __fmul_rn(to_f32(t[4 * b + 1]), fq[4 * b + 1])) |
+                           (e4m3x2(__fmul_rn(to_f32(t[4 * b + 2]), fq[4 * b + 2]),
+                                   __fmul_rn(to_f32(t[4 * b + 3]), fq[4 * b + 3])) << 16);
+                if constexpr (E == 8) {
+                    if (tile_out) {
+                        // bytes cw*8 .. cw*8+8 of tile row r, in the store map's 128-byte swizzle;
+                        // the TMA store drops rows past n and columns past m
+                        *reinterpret_cast<uint2*>(otile + r * 128 + ((((cw >> 1) ^ (r & 7)) << 4) | ((cw & 1) << 3))) =
+                            make_uint2(w[0], w[1]);
+                        continue;
+                    }
+                }
+                if (j >= n) break;
+                uint8_t* dst = out + j * ldo + i0;
+                if (vec_out && i0 + E <= m) {
+                    if constexpr (E == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                    else *reinterpret_cast<uint32_t*>(dst) = w[0];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e)
+                        if (i0 + e < m) dst[e] = static_cast<uint8_t>(w[e / 4] >> (8 * (e % 4)));
+                }
+            }
+            if (tile_out) {
+                fence_proxy_async_smem();                    // the tile's bytes are visible to the TMA store
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ofull[it & 1u]);
+            }
         }
     }
     __syncthreads();
@@ -1025,28 +1074,29 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
                           x, a.m, a.n, a.sxm, a.out, a.som, a.sf, a.ssm, a.ssg, chunks, vec_in, vec_out);
     }
     if (a.sxm == 1 && a.som == 1 && a.tma_ok) {
-        using namespace colmajor_tma;
-        constexpr int V = 8 / sizeof(T);
-        constexpr int BI = 256 / sizeof(T);
+        using namespace colmajor_sw;
+        constexpr int E = 16 / sizeof(T);
+        constexpr int BH = 128 / sizeof(T);
         CUtensorMap tmap;
         if (encode_2d_map(&tmap, x, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                          a.n, a.m, a.sxn * static_cast<int64_t>(sizeof(T)), kRows, BI)) {
-            const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) % V) == 0) && (a.son % V == 0);
-            constexpr int NG = kGroupWarps / (GRAN / kRowsPerWarp);
-            const int smem = kStages * kBoxBytes + kGroups * (kGroupWarps * 32 * (V + 1) + 2 * NG * 32 * V) * 4 +
-                             2 * kStages * 8 + 16 + 1024;
-            auto kern = cast_colmajor_tma_kernel<T, GRAN, FMT, RECIP>;
+                          a.n, a.m, a.sxn * static_cast<int64_t>(sizeof(T)), kRows, BH, /*swizzle128=*/true)) {
+            const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) % E) == 0) && (a.son % E == 0);
+            CUtensorMap omap = {};
+            const int tma_out = sizeof(T) == 2 && aligned16(a.out) && a.son > 0 && a.son % 16 == 0 &&
+                                encode_2d_map(&omap, a.out, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.n, a.m, a.son, kRows, 128,
+                                              /*swizzle128=*/true);
+            auto kern = cast_colmajor_sw_kernel<T, GRAN, FMT, RECIP>;
             static bool attr = false;
             if (!attr) {
-                cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
                 if (e != cudaSuccess) return e;
                 attr = true;
             }
-            const int64_t units = ((a.m + BI - 1) / BI) * ((a.n + kRows - 1) / kRows);
+            const int64_t units = ((a.m + 2 * BH - 1) / (2 * BH)) * ((a.n + kRows - 1) / kRows);
             int64_t grid = num_sms;
             if (grid > units) grid = units;
-            return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, st, tmap, a.m, a.n, a.out,
-                              a.son, a.sf, a.ssm, a.ssg, vec_out, a.dev_status, a.wait_limit_ns);
+            return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, st, tmap, omap, a.m,
+                              a.n, a.out, a.son, a.sf, a.ssm, a.ssg, vec_out, tma_out, a.dev_status, a.wait_limit_ns);
         }
     }
     if (a.sxm == 1 && a.som == 1) {

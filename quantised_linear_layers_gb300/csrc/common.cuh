@@ -207,6 +207,19 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster_addr, 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk copy of this thread has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until at most one committed bulk group of this thread is still reading its source.
+__device__ __forceinline__ void bulk_wait_read_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Waits until every committed bulk copy of this thread has completed (writes done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// TMA tile store shared::cta -> global with bulk-group completion; elements of
+// the box outside the tensor are not written. Coordinates must be >= 0.
+__device__ __forceinline__ void tma_store_2d(const void* desc, const void* src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(desc),
+                 "r"(smem_addr(src)), "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_nctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
@@ -489,23 +502,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Named barrier over `nthreads` threads that also ORs a predicate across
-// them: every participant gets the same answer.
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n"
-        ".reg .pred p, q;\n"
-        "setp.ne.u32 p, %1, 0;\n"
-        "bar.red.or.pred q, %2, %3, p;\n"
-        "selp.u32 %0, 1, 0, q;\n"
-        "}\n"
-        : "=r"(r)
-        : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

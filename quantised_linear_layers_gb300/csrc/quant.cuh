@@ -39,6 +39,14 @@ __device__ __forceinline__ void group_scale(float amax, float& s_store, float& f
     }
 }
 
+// Lane-wise max of two pairs of bf16 values (exact; a NaN operand yields the
+// other operand, as fmaxf does).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Two fp32 values to two E4M3 bytes (lo -> low byte), round to nearest even.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));

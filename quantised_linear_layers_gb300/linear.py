@@ -17,7 +17,7 @@ Essentials: High-Performance FP8 Matrix Multiplication" Part 18:
 ``mn_major=False`` selects the transposed form instead: dgrad always against
 W^T's cast, wgrad with dY^T and X^T cast from transposed views into K-major
 operands. On GB300 the MN-major weight gradient is the faster one (its casts
-take 19 + 25 us against 24 + 38 us at dY [4096, 4096], X [4096, 7168], the
+take 18 + 23 us against 25 + 38 us at dY [4096, 4096], X [4096, 7168], the
 GEMMs run at the same speed), so it is the default.
 
 W is cast once per weight update (``FP8Weight``), not every forward. Every

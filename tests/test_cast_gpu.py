@@ -224,7 +224,7 @@ def test_block_cast_packed(orc, ops, shape, transposed_input):
 @pytest.mark.parametrize("gran", GRANS)
 @pytest.mark.parametrize("fmt", FMTS, ids=["fp32", "ue8m0", "packed"])
 @pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
-@pytest.mark.parametrize("shape", [(4096, 1024), (300, 200), (7168, 640), (130, 36), (1, 24)],
+@pytest.mark.parametrize("shape", [(4096, 1024), (300, 200), (300, 336), (7168, 640), (130, 36), (1, 24)],
                          ids=lambda s: f"{s[0]}x{s[1]}")
 def test_cast_column_major_in_and_out(orc, ops, dtype, gran, fmt, shape):
     """Cast of x^T written as q^T (x_stride_m == out_stride_m == 1): groups run
@@ -243,3 +243,29 @@ def test_cast_column_major_in_and_out(orc, ops, dtype, gran, fmt, shape):
         assert np.array_equal(np.ascontiguousarray(gs), os_)
     else:
         assert np.array_equal(np.ascontiguousarray(gs).view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("gran", GRANS)
+@pytest.mark.parametrize("fmt", FMTS, ids=["fp32", "ue8m0", "packed"])
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
+def test_cast_column_major_subnormal_and_signed_zero(orc, ops, dtype, gran, fmt):
+    """Column-major cast over a group of subnormal inputs, a group of negative
+    zeros with one negative subnormal, and one value near the format's maximum:
+    the amax the kernel reduces (bf16 pairs, for bf16 input) must be the
+    maximum of |x| exactly as defined, so bytes and scales match the oracle."""
+    t_rows, feats = 384, 256
+    x = syn.randn((t_rows, feats), seed=77, dtype=torch.float32)
+    x[:128, :64] *= 1e-39
+    x[128:256, 64:128] = -0.0
+    x[130, 70] = -5.0e-39
+    x[300, 200] = -2.5e38
+    x = x.to(dtype)
+    q_phys = torch.empty((t_rows, feats), dtype=torch.float8_e4m3fn, device="cuda")
+    q, s = ops.fp8_cast_per_token(x.cuda().t(), gran, fmt, out=q_phys.t(), sf_mn_major=True)
+    oq, os_ = orc.cast_per_token(np_input(x).T, gran, fmt)
+    assert np.array_equal(np_bytes(q_phys).T, oq), "E4M3 bytes differ"
+    gs = np.ascontiguousarray(np_sf(s))
+    if fmt == 2:
+        assert np.array_equal(gs, os_)
+    else:
+        assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
