@@ -213,6 +213,15 @@ __device__ __forceinline__ void bulk_wait_read_but_one() {
 }
 // Waits until every committed bulk copy of this thread has completed (writes done).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// TMA tile reduction shared::cta -> global: each element of the box is added
+// to the tensor's element (fp32 adds at L2, the tensor map's type); elements
+// outside the tensor are left alone. Coordinates must be >= 0.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* desc, const void* src, int32_t x, int32_t y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     desc),
+                 "r"(smem_addr(src)), "r"(x), "r"(y)
+                 : "memory");
+}
 // TMA tile store shared::cta -> global with bulk-group completion; elements of
 // the box outside the tensor are not written. Coordinates must be >= 0.
 __device__ __forceinline__ void tma_store_2d(const void* desc, const void* src, int32_t x, int32_t y) {

@@ -38,6 +38,8 @@ struct GemmParams {
     int drecip;               // fp32 scales: factor 1 / s
     // operands stored K-outer ([K][M] / [K][N]) and read MN-major
     int a_mn, b_mn;
+    // fp32 output written (or added) through the kernel's D tensor map
+    int tma_d;
 };
 
 // Host-side description of one GEMM call.
@@ -111,14 +113,14 @@ __device__ __forceinline__ bool row_in_expert_quiet(const GemmParams& p, int64_t
 }
 #endif
 
-// Launch of a GEMM kernel (384 threads, two tensor maps and the parameters)
+// Launch of a GEMM kernel (384 threads; its tensor maps and the parameters)
 // with programmatic stream serialization, so its prologue and the L2
 // prefetch of its first weight tiles overlap the previous kernel's tail; the
 // kernel waits for the previous kernel before it reads any input. `cluster`
 // > 1 adds a cluster dimension.
-template <typename Kern>
+template <typename Kern, typename... Args>
 inline cudaError_t launch_gemm_kernel(Kern kern, unsigned grid, unsigned cluster, size_t smem, cudaStream_t st,
-                                      const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p) {
+                                      const Args&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(384, 1, 1);
@@ -138,7 +140,7 @@ inline cudaError_t launch_gemm_kernel(Kern kern, unsigned grid, unsigned cluster
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 int choose_block_n(int64_t m, int64_t n, int num_sms);

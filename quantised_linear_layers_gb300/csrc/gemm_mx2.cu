@@ -51,13 +51,16 @@ constexpr int BK = 128;
 constexpr int kSfSlots = 8;
 
 // BN: columns of D per pair (256 or 224); each CTA holds BN / 2 rows of B.
-template <int BN>
+// STAGE_OUT: fp32 output leaves through shared memory and TMA tile stores
+// (one 32-row x 32-column buffer per epilogue warp, 32 KB), paid for with one
+// operand stage less.
+template <int BN, bool STAGE_OUT = false>
 struct Mx2Cfg {
     static constexpr int BNH = BN / 2;
     static constexpr int kStageA = BM * BK;
     static constexpr int kStageB = BNH * BK;
     static constexpr int kStageBytes = kStageA + kStageB;
-    static constexpr int kStages = 6;
+    static constexpr int kStages = STAGE_OUT ? 5 : 6;
     static constexpr int kSfbChunks = 2;         // all B rows of the tile (up to 256) in each CTA
     static constexpr int kSfCols = 4 + 4 * kSfbChunks;
     static constexpr int kTmemCols = 512;
@@ -71,8 +74,11 @@ struct Mx2Cfg {
     static constexpr int kOffBar = kOffSf + kSfSlots * kSlotWords * 4;
     static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 2 * kSfSlots + 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static constexpr int kOutWarpBytes = 32 * 128;          // 32 rows x 32 fp32 columns, 128-byte swizzle
+    static constexpr int kOffStage = STAGE_OUT ? ((kOffMisc + 16 + 1023) / 1024) * 1024 : kOffMisc + 16;
+    static constexpr int kSmemBytes = kOffStage + (STAGE_OUT ? 8 * kOutWarpBytes : 0) + 1024;
     static_assert(BN % 32 == 0 && BN <= 256, "pair tile width");
+    static_assert(!STAGE_OUT || (BN / 2) % 32 == 0, "staged output takes 32-column chunks");
     static_assert(kStageB % 1024 == 0, "B stages stay 1024-byte aligned for the 128-byte swizzle");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kSfColBase + 2 * kSfCols <= kTmemCols, "tensor memory budget");
@@ -122,8 +128,8 @@ __device__ __forceinline__ void exp_words(const void* base, int fmt, const int64
 template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const GemmParams p) {
-    using C = Mx2Cfg<BN>;
+                    const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
+    using C = Mx2Cfg<BN, OUT_F32>;
     constexpr int BNH = C::BNH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -403,6 +409,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             else mbar_arrive_remote(leader_tempty0 + as * 8u);
             const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + r_local;
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
+            if constexpr (OUT_F32) {
+                if (p.tma_d) {
+                    // fp32 rows through this warp's staging buffer, 32 columns at a
+                    // time: lane l writes row l (16-byte chunks in the 128-byte
+                    // swizzle), then one TMA store (or add) covers the warp's 32 rows;
+                    // rows past m and columns past n are dropped by the copy
+                    uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kOutWarpBytes;
+                    const int32_t y = static_cast<int32_t>(static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32);
+#pragma unroll
+                    for (int c = 0; c < CPT; c += 32) {
+                        if (lane == 0) bulk_wait_read_all();     // the previous copy has read the buffer
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            *reinterpret_cast<float4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                                make_float4(acc[c + 4 * k], acc[c + 4 * k + 1], acc[c + 4 * k + 2], acc[c + 4 * k + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int32_t x = static_cast<int32_t>(col0 + c);
+                            if (p.accumulate) tma_reduce_add_2d(&tmap_d, stg, x, y);
+                            else tma_store_2d(&tmap_d, stg, x, y);
+                            bulk_commit_group();
+                        }
+                    }
+                    continue;
+                }
+            }
             if (row < p.m) {
                 if constexpr (OUT_FP8) {
                     store_row_e4m3_any(acc, row, col0, p);
@@ -449,6 +483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if constexpr (OUT_F32) {
+            // the staged tiles' copies are complete before the buffers go away
+            if (p.tma_d && lane == 0) bulk_wait_all();
+            __syncwarp();
+        }
     }
 
     tc_fence_before_sync();
@@ -478,13 +517,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
-    using Cf = Mx2Cfg<BN>;
+    using Cf = Mx2Cfg<BN, OUT_F32>;
     constexpr int BNH = Cf::BNH;
     CUtensorMap ta, tb;
     if (!(L.a_mn ? encode_kmajor_map(&ta, L.a, L.k, L.m, L.lda, BK) : encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)))
         return cudaErrorInvalidValue;
     if (!(L.b_mn ? encode_kmajor_map(&tb, L.b, L.k, L.n, L.ldb, BK) : encode_kmajor_map(&tb, L.b, L.n, L.k, L.ldb, BNH)))
         return cudaErrorInvalidValue;
+    // fp32 output through TMA tile stores when D's rows are 16-byte aligned
+    CUtensorMap td = {};
+    p.tma_d = 0;
+    if constexpr (OUT_F32) {
+        if ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && L.ldd > 0 && (L.ldd * 4) % 16 == 0 &&
+            encode_2d_map(&td, L.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, L.m, L.n, L.ldd * 4, 32, 32, /*swizzle128=*/true))
+            p.tma_d = 1;
+    }
     p.tiles_m = static_cast<int>((L.m + 2 * BM - 1) / (2 * BM));
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
     const int tiles = p.tiles_m * p.tiles_n;
@@ -521,7 +568,7 @@ cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int
         pairs = max_pairs;
         cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     }
-    return launch_gemm_kernel(kern, cfg.gridDim.x, 2, Cf::kSmemBytes, st, ta, tb, p);
+    return launch_gemm_kernel(kern, cfg.gridDim.x, 2, Cf::kSmemBytes, st, ta, tb, td, p);
 }
 
 }  // namespace
@@ -532,7 +579,7 @@ cudaError_t launch_gemm_mx2(const GemmLaunch& L, const GemmParams& p, cudaStream
         if (L.out_f32) return launch_mx2_t<256, true, true>(L, p, st, num_sms);
         return launch_mx2_t<256, false, false>(L, p, st, num_sms);
     }
-    if (L.out_f32) return launch_mx2_t<224, true, true>(L, p, st, num_sms);
+    if (L.out_f32) return launch_mx2_t<256, true, true>(L, p, st, num_sms);
     return launch_mx2_t<224, false, false>(L, p, st, num_sms);
 }
 
