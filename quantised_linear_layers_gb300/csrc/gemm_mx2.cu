@@ -51,17 +51,32 @@ constexpr int BK = 128;
 constexpr int kSfSlots = 8;
 
 // BN: columns of D per pair (256 or 224); each CTA holds BN / 2 rows of B.
-// STAGE_OUT: fp32 output leaves through shared memory and TMA tile stores
-// (one 32-row x 32-column buffer per epilogue warp, 32 KB), paid for with one
-// operand stage less.
-template <int BN, bool STAGE_OUT = false>
+// OUT_BYTES: element size of a D that leaves through shared memory and TMA
+// tile stores (2: bf16, 4: fp32; 0: stored directly). Each epilogue warp owns
+// one buffer of 32 rows x kCW columns (rows of 128 bytes with the 128-byte
+// swizzle, or 112 bytes unswizzled, whose pitch already spreads 8 consecutive
+// rows over all banks); the operand ring gives up a stage when the buffers do
+// not fit beside six.
+template <int BN, int OUT_BYTES = 0>
 struct Mx2Cfg {
     static constexpr int BNH = BN / 2;
     static constexpr int kStageA = BM * BK;
     static constexpr int kStageB = BNH * BK;
     static constexpr int kStageBytes = kStageA + kStageB;
-    static constexpr int kStages = STAGE_OUT ? 5 : 6;
+    static constexpr bool kStageOut = OUT_BYTES != 0;
+    static constexpr int kCW = OUT_BYTES == 4 ? 32 : ((BN / 2) % 64 == 0 ? 64 : 56);   // columns per copy
+    static constexpr int kRB = kCW * (OUT_BYTES == 0 ? 2 : OUT_BYTES);               // bytes per staged row
+    static constexpr bool kOutSwizzle = kRB == 128;
+    static constexpr int kOutWarpBytes = 32 * kRB;
     static constexpr int kSfbChunks = 2;         // all B rows of the tile (up to 256) in each CTA
+    // six operand stages unless the output buffers leave room for five only:
+    // bytes besides the ring (exponent slots, barriers for two accumulators, misc)
+    static constexpr int kFixedBytes = kSfSlots * (BM + 128 * kSfbChunks) * 4 + (2 * 2 + 2 * kSfSlots + 3) * 8 + 16;
+    static constexpr int kStages =
+        ((6 * (kStageBytes + 16) + kFixedBytes + 1023) / 1024) * 1024 + (kStageOut ? 8 * kOutWarpBytes : 0) + 1024 <=
+                232448
+            ? 6
+            : 5;
     static constexpr int kSfCols = 4 + 4 * kSfbChunks;
     static constexpr int kTmemCols = 512;
     static constexpr int kAccStride = 256;       // accumulator stages start on 256-column boundaries
@@ -74,11 +89,11 @@ struct Mx2Cfg {
     static constexpr int kOffBar = kOffSf + kSfSlots * kSlotWords * 4;
     static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 2 * kSfSlots + 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kOutWarpBytes = 32 * 128;          // 32 rows x 32 fp32 columns, 128-byte swizzle
-    static constexpr int kOffStage = STAGE_OUT ? ((kOffMisc + 16 + 1023) / 1024) * 1024 : kOffMisc + 16;
-    static constexpr int kSmemBytes = kOffStage + (STAGE_OUT ? 8 * kOutWarpBytes : 0) + 1024;
+    static constexpr int kOffStage = kStageOut ? ((kOffMisc + 16 + 1023) / 1024) * 1024 : kOffMisc + 16;
+    static constexpr int kSmemBytes = kOffStage + (kStageOut ? 8 * kOutWarpBytes : 0) + 1024;
     static_assert(BN % 32 == 0 && BN <= 256, "pair tile width");
-    static_assert(!STAGE_OUT || (BN / 2) % 32 == 0, "staged output takes 32-column chunks");
+    static_assert(!kStageOut || (BN / 2) % kCW == 0, "staged output takes whole chunks");
+    static_assert(kRB % 16 == 0 && (!kOutSwizzle || kRB == 128), "16-byte chunks per staged row");
     static_assert(kStageB % 1024 == 0, "B stages stay 1024-byte aligned for the 128-byte swizzle");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kSfColBase + 2 * kSfCols <= kTmemCols, "tensor memory budget");
@@ -129,7 +144,7 @@ template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
-    using C = Mx2Cfg<BN, OUT_F32>;
+    using C = Mx2Cfg<BN, OUT_FP8 ? 0 : (OUT_F32 ? 4 : 2)>;
     constexpr int BNH = C::BNH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -409,27 +424,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             else mbar_arrive_remote(leader_tempty0 + as * 8u);
             const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + r_local;
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
-            if constexpr (OUT_F32) {
+            if constexpr (C::kStageOut) {
                 if (p.tma_d) {
-                    // fp32 rows through this warp's staging buffer, 32 columns at a
-                    // time: lane l writes row l (16-byte chunks in the 128-byte
-                    // swizzle), then one TMA store (or add) covers the warp's 32 rows;
-                    // rows past m and columns past n are dropped by the copy
+                    // D rows through this warp's staging buffer, kCW columns at a
+                    // time: lane l writes row l in 16-byte chunks, then one TMA
+                    // store (or add) covers the warp's 32 rows; rows past m and
+                    // columns past n are dropped by the copy
                     uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kOutWarpBytes;
                     const int32_t y = static_cast<int32_t>(static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32);
 #pragma unroll
-                    for (int c = 0; c < CPT; c += 32) {
+                    for (int c = 0; c < CPT; c += C::kCW) {
                         if (lane == 0) bulk_wait_read_all();     // the previous copy has read the buffer
                         __syncwarp();
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            *reinterpret_cast<float4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
-                                make_float4(acc[c + 4 * k], acc[c + 4 * k + 1], acc[c + 4 * k + 2], acc[c + 4 * k + 3]);
+                        for (int k = 0; k < C::kRB / 16; ++k) {
+                            uint4 v;
+                            if constexpr (OUT_F32) {
+                                v = make_uint4(__float_as_uint(acc[c + 4 * k]), __float_as_uint(acc[c + 4 * k + 1]),
+                                               __float_as_uint(acc[c + 4 * k + 2]), __float_as_uint(acc[c + 4 * k + 3]));
+                            } else {
+                                const float* a8 = acc + c + 8 * k;
+                                __nv_bfloat162 h0 = __floats2bfloat162_rn(a8[0], a8[1]);
+                                __nv_bfloat162 h1 = __floats2bfloat162_rn(a8[2], a8[3]);
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(a8[4], a8[5]);
+                                __nv_bfloat162 h3 = __floats2bfloat162_rn(a8[6], a8[7]);
+                                v = make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
+                                               *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
+                            }
+                            const uint32_t pos = C::kOutSwizzle ? ((k ^ (lane & 7)) << 4) : (k << 4);
+                            *reinterpret_cast<uint4*>(stg + lane * C::kRB + pos) = v;
+                        }
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
                             const int32_t x = static_cast<int32_t>(col0 + c);
-                            if (p.accumulate) tma_reduce_add_2d(&tmap_d, stg, x, y);
+                            if (OUT_F32 && p.accumulate) tma_reduce_add_2d(&tmap_d, stg, x, y);
                             else tma_store_2d(&tmap_d, stg, x, y);
                             bulk_commit_group();
                         }
@@ -483,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if constexpr (OUT_F32) {
+        if constexpr (C::kStageOut) {
             // the staged tiles' copies are complete before the buffers go away
             if (p.tma_d && lane == 0) bulk_wait_all();
             __syncwarp();
@@ -517,19 +546,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
-    using Cf = Mx2Cfg<BN, OUT_F32>;
+    using Cf = Mx2Cfg<BN, OUT_FP8 ? 0 : (OUT_F32 ? 4 : 2)>;
     constexpr int BNH = Cf::BNH;
     CUtensorMap ta, tb;
     if (!(L.a_mn ? encode_kmajor_map(&ta, L.a, L.k, L.m, L.lda, BK) : encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)))
         return cudaErrorInvalidValue;
     if (!(L.b_mn ? encode_kmajor_map(&tb, L.b, L.k, L.n, L.ldb, BK) : encode_kmajor_map(&tb, L.b, L.n, L.k, L.ldb, BNH)))
         return cudaErrorInvalidValue;
-    // fp32 output through TMA tile stores when D's rows are 16-byte aligned
+    // bf16 / fp32 output through TMA tile stores when D's rows are 16-byte aligned
     CUtensorMap td = {};
     p.tma_d = 0;
-    if constexpr (OUT_F32) {
-        if ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && L.ldd > 0 && (L.ldd * 4) % 16 == 0 &&
-            encode_2d_map(&td, L.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, L.m, L.n, L.ldd * 4, 32, 32, /*swizzle128=*/true))
+    if constexpr (Cf::kStageOut) {
+        constexpr int es = OUT_F32 ? 4 : 2;
+        if ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && L.ldd > 0 && (L.ldd * es) % 16 == 0 &&
+            encode_2d_map(&td, L.d, OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L.m,
+                          L.n, L.ldd * es, 32, Cf::kCW, Cf::kOutSwizzle))
             p.tma_d = 1;
     }
     p.tiles_m = static_cast<int>((L.m + 2 * BM - 1) / (2 * BM));
