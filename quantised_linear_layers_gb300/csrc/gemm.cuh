@@ -157,9 +157,10 @@ cudaError_t launch_gemm_mx_sk(const GemmLaunch& L, GemmParams p, int split, cuda
 bool encode_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows);
 
 // 2-D tensor map of `rows` rows of `cols` elements (row stride in bytes), box
-// [box_rows x box_cols] elements, zero fill out of bounds; no swizzle, or with
-// `swizzle128` the 128-byte swizzle (box_cols x element size must be 128).
+// [box_rows x box_cols] elements, zero fill out of bounds; `swizzle` 0 (none),
+// 64 or 128 selects the 64- or 128-byte swizzle (box_cols x element size must
+// then equal it).
 bool encode_2d_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int64_t rows, int64_t cols,
-                   int64_t row_stride_bytes, int box_rows, int box_cols, bool swizzle128 = false);
+                   int64_t row_stride_bytes, int box_rows, int box_cols, int swizzle = 0);
 
 }  // namespace ql

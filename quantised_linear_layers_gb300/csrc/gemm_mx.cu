@@ -46,7 +46,11 @@ constexpr int BM = 128;
 constexpr int BK = 128;
 constexpr int kSfSlots = 8;          // shared-memory scale ring (K groups)
 
-template <int BN>
+// OUT_BYTES: element size of a D that leaves through shared memory and TMA
+// tile stores (2: bf16, 4: fp32; 0: stored directly). Each epilogue warp owns a
+// 2 KB buffer of 32 rows x 64 bytes in the 64-byte swizzle (32 bf16 or 16 fp32
+// columns per copy), which fits beside every tile width's operand ring.
+template <int BN, int OUT_BYTES = 0>
 struct MxCfg {
     static constexpr int kStageA = BM * BK;
     static constexpr int kStageB = BN * BK;
@@ -66,7 +70,11 @@ struct MxCfg {
     static constexpr int kOffBar = kOffSf + kSfSlots * kSlotWords * 4;
     static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 2 * kSfSlots + 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static constexpr int kCW = OUT_BYTES == 0 ? 1 : 64 / OUT_BYTES;          // columns per copy
+    static constexpr bool kStageOut = OUT_BYTES != 0 && (BN / 2) % kCW == 0;
+    static constexpr int kOutWarpBytes = 32 * 64;
+    static constexpr int kOffStage = kStageOut ? ((kOffMisc + 16 + 1023) / 1024) * 1024 : kOffMisc + 16;
+    static constexpr int kSmemBytes = kOffStage + (kStageOut ? 8 * kOutWarpBytes : 0) + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kTmemColsUsed <= 512, "tensor memory budget");
 };
@@ -119,8 +127,8 @@ __device__ __forceinline__ void exp_words(const void* base, int fmt, const int64
 template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                   const GemmParams p) {
-    using C = MxCfg<BN>;
+                   const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
+    using C = MxCfg<BN, OUT_FP8 ? 0 : (OUT_F32 ? 4 : 2)>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + C::kOffA;
@@ -380,6 +388,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before_sync();
             mbar_arrive(&tempty[as]);
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
+            if constexpr (C::kStageOut) {
+                if (p.tma_d && __all_sync(0xffffffffu, store_row)) {
+                    // all 32 rows of this warp are written: through the staging
+                    // buffer, kCW columns per TMA tile store (or add); lane l
+                    // writes row l, 16-byte chunk k at k ^ ((l >> 1) & 3), the
+                    // 64-byte swizzle; columns past n are dropped by the copy
+                    uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kOutWarpBytes;
+                    const int32_t y = static_cast<int32_t>(static_cast<int64_t>(mb) * BM + q * 32);
+#pragma unroll
+                    for (int c = 0; c < CPT; c += C::kCW) {
+                        if (lane == 0) bulk_wait_read_all();     // the previous copy has read the buffer
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint4 v;
+                            if constexpr (OUT_F32) {
+                                v = make_uint4(__float_as_uint(acc[c + 4 * k]), __float_as_uint(acc[c + 4 * k + 1]),
+                                               __float_as_uint(acc[c + 4 * k + 2]), __float_as_uint(acc[c + 4 * k + 3]));
+                            } else {
+                                const float* a8 = acc + c + 8 * k;
+                                __nv_bfloat162 h0 = __floats2bfloat162_rn(a8[0], a8[1]);
+                                __nv_bfloat162 h1 = __floats2bfloat162_rn(a8[2], a8[3]);
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(a8[4], a8[5]);
+                                __nv_bfloat162 h3 = __floats2bfloat162_rn(a8[6], a8[7]);
+                                v = make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
+                                               *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
+                            }
+                            *reinterpret_cast<uint4*>(stg + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) = v;
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int32_t x = static_cast<int32_t>(col0 + c);
+                            if (OUT_F32 && p.accumulate) tma_reduce_add_2d(&tmap_d, stg, x, y);
+                            else tma_store_2d(&tmap_d, stg, x, y);
+                            bulk_commit_group();
+                        }
+                    }
+                    continue;
+                }
+            }
             if (store_row) {
                 if constexpr (OUT_FP8) {
                     static_assert(CPT == 128, "E4M3 output needs 128 columns per thread");
@@ -427,6 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if constexpr (C::kStageOut) {
+            // the staged tiles' copies are complete before the buffers go away
+            if (p.tma_d && lane == 0) bulk_wait_all();
+            __syncwarp();
+        }
     }
 
     tc_fence_before_sync();
@@ -439,13 +493,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_mx_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
-    using Cf = MxCfg<BN>;
+    using Cf = MxCfg<BN, OUT_FP8 ? 0 : (OUT_F32 ? 4 : 2)>;
     CUtensorMap ta, tb;
     if (!(L.a_mn ? encode_kmajor_map(&ta, L.a, L.k, L.m, L.lda, BK) : encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)))
         return cudaErrorInvalidValue;
     if (!(L.b_mn ? encode_kmajor_map(&tb, L.b, L.k, L.n, L.ldb, BK)
                  : encode_kmajor_map(&tb, L.b, L.n * (L.m_indices ? L.num_groups : 1), L.k, L.ldb, BN)))
         return cudaErrorInvalidValue;
+    // bf16 / fp32 output through TMA tile stores when D's rows are 16-byte aligned
+    CUtensorMap td = {};
+    p.tma_d = 0;
+    if constexpr (Cf::kStageOut) {
+        constexpr int es = OUT_F32 ? 4 : 2;
+        if ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && L.ldd > 0 && (L.ldd * es) % 16 == 0 &&
+            encode_2d_map(&td, L.d, OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L.m,
+                          L.n, L.ldd * es, 32, Cf::kCW, /*swizzle=*/64))
+            p.tma_d = 1;
+    }
     p.tiles_m = static_cast<int>((L.m + BM - 1) / BM);
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
     const int tiles = p.tiles_m * p.tiles_n;
@@ -457,7 +521,7 @@ cudaError_t launch_mx_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int 
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    return launch_gemm_kernel(kern, static_cast<unsigned>(grid), 1, Cf::kSmemBytes, st, ta, tb, p);
+    return launch_gemm_kernel(kern, static_cast<unsigned>(grid), 1, Cf::kSmemBytes, st, ta, tb, td, p);
 }
 
 template <bool PER_ROW_B, bool OUT_F32>

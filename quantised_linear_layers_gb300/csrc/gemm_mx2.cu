@@ -560,7 +560,7 @@ cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int
         constexpr int es = OUT_F32 ? 4 : 2;
         if ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && L.ldd > 0 && (L.ldd * es) % 16 == 0 &&
             encode_2d_map(&td, L.d, OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L.m,
-                          L.n, L.ldd * es, 32, Cf::kCW, Cf::kOutSwizzle))
+                          L.n, L.ldd * es, 32, Cf::kCW, Cf::kOutSwizzle ? 128 : 0))
             p.tma_d = 1;
     }
     p.tiles_m = static_cast<int>((L.m + 2 * BM - 1) / (2 * BM));
