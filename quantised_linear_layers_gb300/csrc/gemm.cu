@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "epilogue_fp8.cuh"
+#include "epilogue_tma.cuh"
 #include "gemm.cuh"
 
 namespace ql {
@@ -100,7 +101,10 @@ constexpr int BM = 128;
 constexpr int BK = 128;         // K block = scale granularity
 constexpr int kScaleSlots = 8;
 
-template <int BN, bool PER_ROW_B>
+// OUT_BYTES: element size of a D that leaves through shared memory and TMA
+// tile stores (2: bf16, 4: fp32; 0: stored directly), one 2 KB buffer of 32
+// rows x 64 bytes (64-byte swizzle) per epilogue warp.
+template <int BN, bool PER_ROW_B, int OUT_BYTES = 0>
 struct Cfg {
     static constexpr int kStageA = BM * BK;                  // bytes
     static constexpr int kStageB = BN * BK;
@@ -119,7 +123,10 @@ struct Cfg {
     static constexpr int kOffBar = kOffScale + kScaleSlots * kSlotFloats * 4;
     static constexpr int kNumBars = 2 * kStages + 2 * kTmemStages + 2 * kScaleSlots + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+    static constexpr bool kStageOut = OUT_BYTES != 0 && (BN / 2) % (64 / (OUT_BYTES == 0 ? 1 : OUT_BYTES)) == 0;
+    static constexpr int kOutWarpBytes = 32 * 64;
+    static constexpr int kOffStage = kStageOut ? ((kOffMisc + 16 + 1023) / 1024) * 1024 : kOffMisc + 16;
+    static constexpr int kSmemBytes = kOffStage + (kStageOut ? 8 * kOutWarpBytes : 0) + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kColsPerThread % 16 == 0, "columns per thread");
 };
@@ -181,8 +188,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const GemmParams p) {
-    using C = Cfg<BN, PER_ROW_B>;
+                    const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
+    using C = Cfg<BN, PER_ROW_B, OUT_FP8 ? 0 : (OUT_F32 ? 4 : 2)>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + C::kOffA;
@@ -441,6 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             // ---------------- epilogue ----------------
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
+            if constexpr (C::kStageOut) {
+                if (p.tma_d && __all_sync(0xffffffffu, store_row)) {
+                    // all 32 rows of this warp are written: through its staging buffer
+                    uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kOutWarpBytes;
+                    const int32_t y = static_cast<int32_t>(static_cast<int64_t>(mb) * BM + q * 32);
+                    tma_store_warp_rows<CPT, 64, OUT_F32>(acc, stg, &tmap_d, col0, y, p.accumulate != 0);
+                    continue;
+                }
+            }
             if (store_row) {
                 if constexpr (OUT_FP8) {
                     static_assert(CPT == 128, "E4M3 output needs 128 columns per thread");
@@ -488,6 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if constexpr (C::kStageOut) {
+            // the staged tiles' copies are complete before the buffers go away
+            if (p.tma_d && lane == 0) bulk_wait_all();
+            __syncwarp();
+        }
     }
 
     tc_fence_before_sync();
@@ -500,13 +521,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
-    using Cf = Cfg<BN, PER_ROW_B>;
+    using Cf = Cfg<BN, PER_ROW_B, OUT_FP8 ? 0 : (OUT_F32 ? 4 : 2)>;
     CUtensorMap ta, tb;
     if (!(L.a_mn ? encode_kmajor_map(&ta, L.a, L.k, L.m, L.lda, BK) : encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)))
         return cudaErrorInvalidValue;
     if (!(L.b_mn ? encode_kmajor_map(&tb, L.b, L.k, L.n, L.ldb, BK)
                  : encode_kmajor_map(&tb, L.b, L.n * (L.m_indices ? L.num_groups : 1), L.k, L.ldb, BN)))
         return cudaErrorInvalidValue;
+    // bf16 / fp32 output through TMA tile stores when D's rows are 16-byte aligned
+    CUtensorMap td = {};
+    p.tma_d = 0;
+    if constexpr (Cf::kStageOut) {
+        constexpr int es = OUT_F32 ? 4 : 2;
+        if ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && L.ldd > 0 && (L.ldd * es) % 16 == 0 &&
+            encode_2d_map(&td, L.d, OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L.m,
+                          L.n, L.ldd * es, 32, 64 / es, /*swizzle=*/64))
+            p.tma_d = 1;
+    }
     p.tiles_m = static_cast<int>((L.m + BM - 1) / BM);
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
     const int tiles = p.tiles_m * p.tiles_n;
@@ -518,7 +549,7 @@ cudaError_t launch_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    return launch_gemm_kernel(kern, static_cast<unsigned>(grid), 1, Cf::kSmemBytes, st, ta, tb, p);
+    return launch_gemm_kernel(kern, static_cast<unsigned>(grid), 1, Cf::kSmemBytes, st, ta, tb, td, p);
 }
 
 template <bool PER_ROW_B, bool OUT_F32>

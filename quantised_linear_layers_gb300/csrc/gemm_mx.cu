@@ -35,6 +35,7 @@
 
 #include "common.cuh"
 #include "epilogue_fp8.cuh"
+#include "epilogue_tma.cuh"
 #include "gemm.cuh"
 
 namespace ql {
@@ -390,42 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
             if constexpr (C::kStageOut) {
                 if (p.tma_d && __all_sync(0xffffffffu, store_row)) {
-                    // all 32 rows of this warp are written: through the staging
-                    // buffer, kCW columns per TMA tile store (or add); lane l
-                    // writes row l, 16-byte chunk k at k ^ ((l >> 1) & 3), the
-                    // 64-byte swizzle; columns past n are dropped by the copy
+                    // all 32 rows of this warp are written: through its staging buffer
                     uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kOutWarpBytes;
                     const int32_t y = static_cast<int32_t>(static_cast<int64_t>(mb) * BM + q * 32);
-#pragma unroll
-                    for (int c = 0; c < CPT; c += C::kCW) {
-                        if (lane == 0) bulk_wait_read_all();     // the previous copy has read the buffer
-                        __syncwarp();
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            uint4 v;
-                            if constexpr (OUT_F32) {
-                                v = make_uint4(__float_as_uint(acc[c + 4 * k]), __float_as_uint(acc[c + 4 * k + 1]),
-                                               __float_as_uint(acc[c + 4 * k + 2]), __float_as_uint(acc[c + 4 * k + 3]));
-                            } else {
-                                const float* a8 = acc + c + 8 * k;
-                                __nv_bfloat162 h0 = __floats2bfloat162_rn(a8[0], a8[1]);
-                                __nv_bfloat162 h1 = __floats2bfloat162_rn(a8[2], a8[3]);
-                                __nv_bfloat162 h2 = __floats2bfloat162_rn(a8[4], a8[5]);
-                                __nv_bfloat162 h3 = __floats2bfloat162_rn(a8[6], a8[7]);
-                                v = make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
-                                               *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
-                            }
-                            *reinterpret_cast<uint4*>(stg + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) = v;
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const int32_t x = static_cast<int32_t>(col0 + c);
-                            if (OUT_F32 && p.accumulate) tma_reduce_add_2d(&tmap_d, stg, x, y);
-                            else tma_store_2d(&tmap_d, stg, x, y);
-                            bulk_commit_group();
-                        }
-                    }
+                    tma_store_warp_rows<CPT, 64, OUT_F32>(acc, stg, &tmap_d, col0, y, p.accumulate != 0);
                     continue;
                 }
             }

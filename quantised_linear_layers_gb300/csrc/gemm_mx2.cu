@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "epilogue_fp8.cuh"
+#include "epilogue_tma.cuh"
 #include "gemm.cuh"
 
 namespace ql {
@@ -426,43 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t col0 = static_cast<int64_t>(nb) * BN + wg * CPT;
             if constexpr (C::kStageOut) {
                 if (p.tma_d) {
-                    // D rows through this warp's staging buffer, kCW columns at a
-                    // time: lane l writes row l in 16-byte chunks, then one TMA
-                    // store (or add) covers the warp's 32 rows; rows past m and
-                    // columns past n are dropped by the copy
+                    // D rows through this warp's staging buffer and TMA tile stores
                     uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kOutWarpBytes;
                     const int32_t y = static_cast<int32_t>(static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32);
-#pragma unroll
-                    for (int c = 0; c < CPT; c += C::kCW) {
-                        if (lane == 0) bulk_wait_read_all();     // the previous copy has read the buffer
-                        __syncwarp();
-#pragma unroll
-                        for (int k = 0; k < C::kRB / 16; ++k) {
-                            uint4 v;
-                            if constexpr (OUT_F32) {
-                                v = make_uint4(__float_as_uint(acc[c + 4 * k]), __float_as_uint(acc[c + 4 * k + 1]),
-                                               __float_as_uint(acc[c + 4 * k + 2]), __float_as_uint(acc[c + 4 * k + 3]));
-                            } else {
-                                const float* a8 = acc + c + 8 * k;
-                                __nv_bfloat162 h0 = __floats2bfloat162_rn(a8[0], a8[1]);
-                                __nv_bfloat162 h1 = __floats2bfloat162_rn(a8[2], a8[3]);
-                                __nv_bfloat162 h2 = __floats2bfloat162_rn(a8[4], a8[5]);
-                                __nv_bfloat162 h3 = __floats2bfloat162_rn(a8[6], a8[7]);
-                                v = make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
-                                               *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
-                            }
-                            const uint32_t pos = C::kOutSwizzle ? ((k ^ (lane & 7)) << 4) : (k << 4);
-                            *reinterpret_cast<uint4*>(stg + lane * C::kRB + pos) = v;
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const int32_t x = static_cast<int32_t>(col0 + c);
-                            if (OUT_F32 && p.accumulate) tma_reduce_add_2d(&tmap_d, stg, x, y);
-                            else tma_store_2d(&tmap_d, stg, x, y);
-                            bulk_commit_group();
-                        }
-                    }
+                    tma_store_warp_rows<CPT, C::kRB, OUT_F32>(acc, stg, &tmap_d, col0, y, p.accumulate != 0);
                     continue;
                 }
             }

@@ -333,3 +333,50 @@ def test_split_k_cluster(orc, ops, case, fmt):
     # the default path picks the same kernel for these shapes and agrees
     d2 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt) if sms == 0 else d
     assert torch.equal(d, d2)
+
+
+@pytest.mark.parametrize("offset", [64, 4], ids=["tile_store", "direct"])
+@pytest.mark.parametrize("out", ["bf16", "f32", "f32_acc"])
+@pytest.mark.parametrize("path", [1, 2, 3], ids=["promotion", "block_scaled", "pair"])
+def test_output_view_leaves_rest_untouched(orc, ops, path, out, offset):
+    """D written into a view of a taller, wider buffer (row pitch 1024, view at
+    column `offset`: 64 keeps its rows 16-byte aligned, so the kernels write
+    through TMA tile stores, 4 does not): every element outside the view keeps
+    its canary, ragged last row and column tiles included, and the view holds
+    exactly what a contiguous output gets (the accumulate form adds to the
+    view's previous contents)."""
+    m, n, k = 300, 520, 384
+    if out == "bf16":
+        _, _, aq, sa, bq, sb = fwd_operands(ops, m, n, k, 1)
+        dt = torch.bfloat16
+    else:
+        aq, sa = ops.fp8_cast_per_token(syn.randn((m, k), seed=syn.SEED_DY).cuda(), 128, 1)
+        bq, sb = ops.fp8_cast_per_token(syn.randn((n, k), seed=syn.SEED_X).cuda(), 128, 1)
+        dt = torch.float32
+    canary = -3072.0
+    parent = torch.full((m + 40, 1024), canary, dtype=dt, device="cuda")
+    view = parent[:m, offset:offset + n]
+    acc = out == "f32_acc"
+    d0 = syn.randn((m, n), seed=5, dtype=torch.float32, mul=0.1).cuda()
+    if acc:
+        view.copy_(d0)
+    ops.set_gemm_path(path)
+    try:
+        if out == "bf16":
+            ops.gemm_fp8_nt_bf16(aq, sa, bq, sb, 1, out=view)
+            ref = ops.gemm_fp8_nt_bf16(aq, sa, bq, sb, 1)
+        else:
+            ops.gemm_fp8_wgrad_fp32(aq, sa, bq, sb, out=view, accumulate=acc, fmt=1)
+            ref = d0.clone() if acc else torch.empty((m, n), dtype=dt, device="cuda")
+            ops.gemm_fp8_wgrad_fp32(aq, sa, bq, sb, out=ref, accumulate=acc, fmt=1)
+    finally:
+        ops.set_gemm_path(0)
+    assert ops.device_status() == 0
+    outside = torch.ones(parent.shape, dtype=torch.bool, device="cuda")
+    outside[:m, offset:offset + n] = False
+    assert torch.all(parent[outside] == canary)
+    assert torch.equal(view, ref)
+    if not acc:
+        refo = orc.gemm(np_bytes(aq), np_sf(sa), np_bytes(bq), np_sf(sb), 1, b_per_row=(out != "bf16"),
+                        rows=np.array([0, 129, 256, m - 1]), out="bf16" if out == "bf16" else "f32")
+        check_gemm(view[[0, 129, 256, m - 1]].double().cpu().numpy(), refo)
