@@ -1082,7 +1082,9 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
                           a.n, a.m, a.sxn * static_cast<int64_t>(sizeof(T)), kRows, BH, /*swizzle=*/128)) {
             const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) % E) == 0) && (a.son % E == 0);
             CUtensorMap omap = {};
+            // a TMA store may write a row's last 16-byte chunk whole: rows must start and end aligned
             const int tma_out = sizeof(T) == 2 && aligned16(a.out) && a.son > 0 && a.son % 16 == 0 &&
+                                a.m % 16 == 0 &&
                                 encode_2d_map(&omap, a.out, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.n, a.m, a.son, kRows, 128,
                                               /*swizzle=*/128);
             auto kern = cast_colmajor_sw_kernel<T, GRAN, FMT, RECIP>;

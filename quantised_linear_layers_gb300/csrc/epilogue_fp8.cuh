@@ -25,9 +25,13 @@ __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(_
 // p.ldd bytes) and one scale per GRAN-wide group into p.dsf (fp32 at
 // [row*dsm + g*dsg], or for packed UE8M0 byte g%4 of int32 word
 // [row*dsm + (g/4)*dsg]; the owner of the last group zeroes the word's pad
-// bytes). Columns at or past n are not stored.
-template <int GRAN>
-__device__ __forceinline__ void store_row_e4m3(const float* acc, int64_t row, int64_t col0, const GemmParams& p) {
+// bytes). Columns at or past n are not stored. With STAGED the bytes go to
+// the 128-byte shared-memory row `srow` instead, 16-byte chunk k at
+// k ^ swz (the 128-byte swizzle of a TMA tile store that the caller issues),
+// and the scales are stored only when `row_ok`.
+template <int GRAN, bool STAGED = false>
+__device__ __forceinline__ void store_row_e4m3(const float* acc, int64_t row, int64_t col0, const GemmParams& p,
+                                               uint8_t* srow = nullptr, int swz = 0, bool row_ok = true) {
     constexpr int NG = 128 / GRAN;
     uint8_t* drow = static_cast<uint8_t*>(p.d) + row * p.ldd;
     const int64_t G = (p.n + GRAN - 1) / GRAN;
@@ -57,7 +61,10 @@ __device__ __forceinline__ void store_row_e4m3(const float* acc, int64_t row, in
                     w[q] = quant4(bf16_round(a[0]), bf16_round(a[1]), bf16_round(a[2]), bf16_round(a[3]), f);
                 }
                 const int64_t c = c0 + j;
-                if (p.vec_store && c + 16 <= p.n) {
+                if constexpr (STAGED) {
+                    *reinterpret_cast<uint4*>(srow + ((((gi * GRAN + j) >> 4) ^ swz) << 4)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                } else if (p.vec_store && c + 16 <= p.n) {
                     *reinterpret_cast<uint4*>(drow + c) = make_uint4(w[0], w[1], w[2], w[3]);
                 } else {
 #pragma unroll
@@ -66,6 +73,7 @@ __device__ __forceinline__ void store_row_e4m3(const float* acc, int64_t row, in
                 }
             }
             const int64_t g = c0 / GRAN;
+            if (!row_ok) continue;
             if (p.dfmt != kSfPacked) {
                 static_cast<float*>(p.dsf)[row * p.dsm + g * p.dsg] = s;
             } else {
@@ -83,6 +91,13 @@ __device__ __forceinline__ void store_row_e4m3_any(const float* acc, int64_t row
                                                    const GemmParams& p) {
     if (p.dgran == 32) store_row_e4m3<32>(acc, row, col0, p);
     else store_row_e4m3<128>(acc, row, col0, p);
+}
+
+// The same into a staged 128-byte row (see store_row_e4m3).
+__device__ __forceinline__ void stage_row_e4m3_any(const float* acc, int64_t row, int64_t col0, const GemmParams& p,
+                                                   uint8_t* srow, int swz, bool row_ok) {
+    if (p.dgran == 32) store_row_e4m3<32, true>(acc, row, col0, p, srow, swz, row_ok);
+    else store_row_e4m3<128, true>(acc, row, col0, p, srow, swz, row_ok);
 }
 
 }  // namespace ql

@@ -469,12 +469,14 @@ cudaError_t launch_mx_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int 
     if (!(L.b_mn ? encode_kmajor_map(&tb, L.b, L.k, L.n, L.ldb, BK)
                  : encode_kmajor_map(&tb, L.b, L.n * (L.m_indices ? L.num_groups : 1), L.k, L.ldb, BN)))
         return cudaErrorInvalidValue;
-    // bf16 / fp32 output through TMA tile stores when D's rows are 16-byte aligned
+    // bf16 / fp32 output through TMA tile stores when D's rows start and end 16-byte aligned
     CUtensorMap td = {};
     p.tma_d = 0;
     if constexpr (Cf::kStageOut) {
         constexpr int es = OUT_F32 ? 4 : 2;
+        // a TMA store may write a row's last 16-byte chunk whole, so D's rows must end on one
         if ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && L.ldd > 0 && (L.ldd * es) % 16 == 0 &&
+            (L.n * es) % 16 == 0 &&
             encode_2d_map(&td, L.d, OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L.m,
                           L.n, L.ldd * es, 32, Cf::kCW, /*swizzle=*/64))
             p.tma_d = 1;

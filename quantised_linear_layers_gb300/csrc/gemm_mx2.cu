@@ -53,7 +53,7 @@ constexpr int kSfSlots = 8;
 
 // BN: columns of D per pair (256 or 224); each CTA holds BN / 2 rows of B.
 // OUT_BYTES: element size of a D that leaves through shared memory and TMA
-// tile stores (2: bf16, 4: fp32; 0: stored directly). Each epilogue warp owns
+// tile stores (1: E4M3, 2: bf16, 4: fp32; 0: stored directly). Each epilogue warp owns
 // one buffer of 32 rows x kCW columns (rows of 128 bytes with the 128-byte
 // swizzle, or 112 bytes unswizzled, whose pitch already spreads 8 consecutive
 // rows over all banks); the operand ring gives up a stage when the buffers do
@@ -65,7 +65,7 @@ struct Mx2Cfg {
     static constexpr int kStageB = BNH * BK;
     static constexpr int kStageBytes = kStageA + kStageB;
     static constexpr bool kStageOut = OUT_BYTES != 0;
-    static constexpr int kCW = OUT_BYTES == 4 ? 32 : ((BN / 2) % 64 == 0 ? 64 : 56);   // columns per copy
+    static constexpr int kCW = OUT_BYTES == 4 ? 32 : (OUT_BYTES == 1 ? 128 : ((BN / 2) % 64 == 0 ? 64 : 56));
     static constexpr int kRB = kCW * (OUT_BYTES == 0 ? 2 : OUT_BYTES);               // bytes per staged row
     static constexpr bool kOutSwizzle = kRB == 128;
     static constexpr int kOutWarpBytes = 32 * kRB;
@@ -145,7 +145,7 @@ template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
-    using C = Mx2Cfg<BN, OUT_FP8 ? 0 : (OUT_F32 ? 4 : 2)>;
+    using C = Mx2Cfg<BN, OUT_FP8 ? 1 : (OUT_F32 ? 4 : 2)>;
     constexpr int BNH = C::BNH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -430,7 +430,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // D rows through this warp's staging buffer and TMA tile stores
                     uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kOutWarpBytes;
                     const int32_t y = static_cast<int32_t>(static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32);
-                    tma_store_warp_rows<CPT, C::kRB, OUT_F32>(acc, stg, &tmap_d, col0, y, p.accumulate != 0);
+                    if constexpr (OUT_FP8) {
+                        // E4M3 bytes staged (one 128-byte row per lane), scales stored directly
+                        static_assert(CPT == 128, "E4M3 output needs 128 columns per thread");
+                        if (lane == 0) bulk_wait_read_all();     // the previous copy has read the buffer
+                        __syncwarp();
+                        stage_row_e4m3_any(acc, row, col0, p, stg + lane * 128, lane & 7, row < p.m);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmap_d, stg, static_cast<int32_t>(col0), y);
+                            bulk_commit_group();
+                        }
+                    } else {
+                        tma_store_warp_rows<CPT, C::kRB, OUT_F32>(acc, stg, &tmap_d, col0, y, p.accumulate != 0);
+                    }
                     continue;
                 }
             }
@@ -514,21 +528,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
 cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num_sms) {
-    using Cf = Mx2Cfg<BN, OUT_FP8 ? 0 : (OUT_F32 ? 4 : 2)>;
+    using Cf = Mx2Cfg<BN, OUT_FP8 ? 1 : (OUT_F32 ? 4 : 2)>;
     constexpr int BNH = Cf::BNH;
     CUtensorMap ta, tb;
     if (!(L.a_mn ? encode_kmajor_map(&ta, L.a, L.k, L.m, L.lda, BK) : encode_kmajor_map(&ta, L.a, L.m, L.k, L.lda, BM)))
         return cudaErrorInvalidValue;
     if (!(L.b_mn ? encode_kmajor_map(&tb, L.b, L.k, L.n, L.ldb, BK) : encode_kmajor_map(&tb, L.b, L.n, L.k, L.ldb, BNH)))
         return cudaErrorInvalidValue;
-    // bf16 / fp32 output through TMA tile stores when D's rows are 16-byte aligned
+    // E4M3 / bf16 / fp32 output through TMA tile stores when D's rows start and end 16-byte aligned
     CUtensorMap td = {};
     p.tma_d = 0;
     if constexpr (Cf::kStageOut) {
-        constexpr int es = OUT_F32 ? 4 : 2;
+        constexpr int es = OUT_FP8 ? 1 : (OUT_F32 ? 4 : 2);
+        const CUtensorMapDataType dt = OUT_FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                               : (OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+        // a TMA store may write a row's last 16-byte chunk whole, so D's rows must end on one
         if ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && L.ldd > 0 && (L.ldd * es) % 16 == 0 &&
-            encode_2d_map(&td, L.d, OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L.m,
-                          L.n, L.ldd * es, 32, Cf::kCW, Cf::kOutSwizzle ? 128 : 0))
+            (L.n * es) % 16 == 0 &&
+            encode_2d_map(&td, L.d, dt, L.m, L.n, L.ldd * es, 32, Cf::kCW, Cf::kOutSwizzle ? 128 : 0))
             p.tma_d = 1;
     }
     p.tiles_m = static_cast<int>((L.m + 2 * BM - 1) / (2 * BM));

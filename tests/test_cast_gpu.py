@@ -269,3 +269,27 @@ def test_cast_column_major_subnormal_and_signed_zero(orc, ops, dtype, gran, fmt)
         assert np.array_equal(gs, os_)
     else:
         assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("feats", [208, 200])
+@pytest.mark.parametrize("fmt", [0, 2], ids=["fp32", "packed"])
+def test_cast_column_major_into_view(orc, ops, fmt, feats):
+    """Column-major cast written into a view of a wider buffer (row pitch 256
+    bytes): with 208 features the view's rows start and end on 16-byte
+    boundaries and the E4M3 rows leave through TMA tile stores, with 200 they
+    end mid-chunk and are stored directly. The bytes outside the view keep
+    their canary and the view matches the oracle."""
+    t_rows = 300
+    x = make_x(t_rows, feats, torch.bfloat16, 128, huge=False)
+    parent = torch.full((t_rows + 8, 256), 0x5A, dtype=torch.uint8, device="cuda")
+    view = parent[:t_rows, :feats].view(torch.float8_e4m3fn)
+    _, s = ops.fp8_cast_per_token(x.cuda().t(), 128, fmt, out=view.t(), sf_mn_major=True)
+    oq, os_ = orc.cast_per_token(np_input(x).T, 128, fmt)
+    p = parent.cpu().numpy()
+    assert np.all(p[:, feats:] == 0x5A) and np.all(p[t_rows:] == 0x5A)
+    assert np.array_equal(p[:t_rows, :feats].T, oq)
+    gs = np.ascontiguousarray(np_sf(s))
+    if fmt == 2:
+        assert np.array_equal(gs, os_)
+    else:
+        assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))

@@ -51,8 +51,8 @@ def dequant(q, sf, gran, out_fmt, n):
 
 # (m, n, k, path, input scale format): the CTA-pair kernel, the single-SM
 # block-scaled kernel and the CUDA-core promotion kernel, ragged n
-KERNELS = [(2048, 2560, 1024, 3, 2), (2048, 2560, 1024, 3, 1), (300, 520, 640, 2, 2), (300, 520, 640, 2, 1),
-           (300, 520, 640, 1, 0), (129, 7168, 512, 0, 0)]
+KERNELS = [(2048, 2560, 1024, 3, 2), (2048, 2560, 1024, 3, 1), (300, 520, 640, 3, 2), (300, 520, 640, 2, 2),
+           (300, 520, 640, 2, 1), (300, 520, 640, 1, 0), (129, 7168, 512, 0, 0)]
 
 
 @pytest.mark.parametrize("kcase", KERNELS, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}_path{c[3]}_fmt{c[4]}")
@@ -106,13 +106,25 @@ def test_worked_shape_default_path(orc, ops):
     check_gemm(d2.float().cpu().numpy(), ref2, "next layer")
 
 
-def test_output_views_untouched_outside(ops):
-    """E4M3 output written into a column view of a wider buffer: the bytes
-    outside the view stay as they were."""
-    m, n, k = 256, 300, 256
+@pytest.mark.parametrize("n", [300, 336])
+@pytest.mark.parametrize("path", [0, 3], ids=["default", "pair"])
+def test_output_views_untouched_outside(ops, path, n):
+    """E4M3 output written into a column view of a taller, wider buffer: the
+    bytes outside the view stay as they were, and the view holds the same bytes
+    as a contiguous output. With n = 336 the view's rows start and end on
+    16-byte boundaries, so the pair kernel writes through TMA tile stores (a
+    ragged last tile); with n = 300 they do not end on one and it stores
+    directly."""
+    m, k = 300, 256
     xq, xs, wq, ws = operands(ops, m, n, k, 2, seed=11)
-    parent = torch.full((m, 400), 0x5A, dtype=torch.uint8, device="cuda")
-    view = parent[:, 48:48 + n].view(torch.float8_e4m3fn)
-    ops.gemm_fp8_nt_fp8out(xq, xs, wq, ws, 2, 128, 2, out=view)
+    parent = torch.full((m + 20, 400), 0x5A, dtype=torch.uint8, device="cuda")
+    view = parent[:m, 48:48 + n].view(torch.float8_e4m3fn)
+    ops.set_gemm_path(path)
+    try:
+        _, sf_v = ops.gemm_fp8_nt_fp8out(xq, xs, wq, ws, 2, 128, 2, out=view)
+        q_c, sf_c = ops.gemm_fp8_nt_fp8out(xq, xs, wq, ws, 2, 128, 2)
+    finally:
+        ops.set_gemm_path(0)
     p = parent.cpu().numpy()
-    assert np.all(p[:, :48] == 0x5A) and np.all(p[:, 48 + n:] == 0x5A)
+    assert np.all(p[:, :48] == 0x5A) and np.all(p[:, 48 + n:] == 0x5A) and np.all(p[m:] == 0x5A)
+    assert np.array_equal(np_bytes(view), np_bytes(q_c)) and torch.equal(sf_v, sf_c)

@@ -335,17 +335,19 @@ def test_split_k_cluster(orc, ops, case, fmt):
     assert torch.equal(d, d2)
 
 
-@pytest.mark.parametrize("offset", [64, 4], ids=["tile_store", "direct"])
+@pytest.mark.parametrize("n", [520, 300])
+@pytest.mark.parametrize("offset", [64, 4], ids=["aligned", "unaligned"])
 @pytest.mark.parametrize("out", ["bf16", "f32", "f32_acc"])
 @pytest.mark.parametrize("path", [1, 2, 3], ids=["promotion", "block_scaled", "pair"])
-def test_output_view_leaves_rest_untouched(orc, ops, path, out, offset):
+def test_output_view_leaves_rest_untouched(orc, ops, path, out, offset, n):
     """D written into a view of a taller, wider buffer (row pitch 1024, view at
-    column `offset`: 64 keeps its rows 16-byte aligned, so the kernels write
-    through TMA tile stores, 4 does not): every element outside the view keeps
-    its canary, ragged last row and column tiles included, and the view holds
-    exactly what a contiguous output gets (the accumulate form adds to the
-    view's previous contents)."""
-    m, n, k = 300, 520, 384
+    column `offset`). The kernels write through TMA tile stores only when the
+    view's rows start and end on 16-byte boundaries (offset 64 with n = 520);
+    otherwise they store directly. Either way every element outside the view
+    keeps its canary, ragged last row and column tiles included, and the view
+    holds exactly what a contiguous output gets (the accumulate form adds to
+    the view's previous contents)."""
+    m, k = 300, 384
     if out == "bf16":
         _, _, aq, sa, bq, sb = fwd_operands(ops, m, n, k, 1)
         dt = torch.bfloat16
