@@ -16,8 +16,9 @@
 // summed through distributed shared memory with no global scratch: each CTA
 // owns a slice of 128/S columns; every CTA writes its fp32 partial of slice j
 // into a staging buffer and the TMA engine copies it (one bulk copy per
-// slice) into CTA j's receive area, completing on CTA j's mbarrier; CTA j adds
-// the S partials and writes bf16. Staging and receive areas reuse the operand
+// slice, of the tile's rows inside A only: half the bytes at M = 64) into CTA
+// j's receive area, completing on CTA j's mbarrier; CTA j adds the S partials
+// and writes bf16. Staging and receive areas reuse the operand
 // ring, idle once every CTA of the cluster has passed the cluster barrier that
 // follows its last MMA.
 //
@@ -145,6 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g0 = kb0 / 4, g1 = (kb1 + 3) / 4;      // K groups touching [kb0, kb1)
     const int sw = BN / split;                       // columns of the slice each CTA finishes
     const uint32_t slice_bytes = static_cast<uint32_t>(BM * sw * 4);
+    // only the tile's rows inside A travel: rows are contiguous in a slice block
+    const int64_t rows_left = p.m - static_cast<int64_t>(mb) * BM;
+    const uint32_t copy_bytes = static_cast<uint32_t>((rows_left < BM ? rows_left : BM) * sw * 4);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
         // armed before the cluster barrier that precedes any copy into this CTA
-        mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(split - 1) * slice_bytes);
+        mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(split - 1) * copy_bytes);
     }
     pdl_launch_dependents();
     if (warp == 0 && lane == 0) {
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = first_slice + i;
                 if (j == rank) continue;
                 bulk_copy_to_cluster(mapa_shared(recv + rank * slice_bytes, static_cast<uint32_t>(j)),
-                                     stage + i * slice_bytes, slice_bytes,
+                                     stage + i * slice_bytes, copy_bytes,
                                      mapa_shared(rbar, static_cast<uint32_t>(j)));
             }
             bulk_commit_group();
