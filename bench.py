@@ -435,8 +435,9 @@ def run_workloads(dev, pk, reps):
       dominate) and 4096 (tensor-bound), L2 flushed before each repetition,
       and at M = 64, 128 as 32 GEMMs back to back over 8 distinct weights;
     - the Linear layer's step, X [4096, 7168], dY [4096, 4096], W [4096, 7168]:
-      weight casts (W and W^T, 128x128), forward (cast X + GEMM), dgrad (cast dY
-      + GEMM against W^T), wgrad (transposed casts of dY and X + fp32 GEMM),
+      weight cast (W's 128x128 block cast, which also writes W^T's scale
+      grid), forward (cast X + GEMM), dgrad (cast dY + GEMM reading W's cast
+      MN-major), wgrad (column-major casts of dY and X + fp32 GEMM),
       L2 flushed before each step; and its weight gradient with the operands
       cast from transposed views against cast in place and read MN-major;
     - the low-latency per-token cast (hidden 4096, group 32, packed UE8M0) at

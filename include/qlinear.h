@@ -126,6 +126,29 @@ ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t
                              ql_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * fp8_cast_per_block_dual
+ * fp8_cast_per_block that also writes, in the same pass, the scale grid of
+ * the transposed cast: block (r, c) of x into out_sf_t at
+ * [c*sf_t_stride_c + r*sf_t_stride_r] (fp32 / UE8M0), or for
+ * QL_SF_PACKED_UE8M0 as byte r % 4 of int32 word [c*sf_t_stride_c +
+ * (r/4)*sf_t_stride_r] (words packed along the row-block axis, pad bytes 0);
+ * out_sf_t is [ceil(n/128), ceil(m/128)] (fp32) or [ceil(n/128),
+ * ceil(ceil(m/128)/4)] (words). A block's amax does not depend on orientation
+ * ("DeepGEMM Essentials" Part 4; the W^T requantisation of "[Help] Starter
+ * script for nn.Linear for fwd,bwd"), so out_sf_t equals the scales of
+ * fp8_cast_per_block(x^T) byte for byte, and out read MN-major with out_sf_t
+ * is the data-gradient operand of gemm_fp8_nn_bf16 in every scale format: no
+ * cast of W^T is needed. Other arguments, requirements and errors as
+ * fp8_cast_per_block; out_sf_t == NULL with m*n > 0 is QL_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------- */
+ql_status fp8_cast_per_block_dual(const void* x, ql_dtype x_dtype, int64_t m, int64_t n,
+                                  int64_t x_stride_m, int64_t x_stride_n, int fmt,
+                                  uint8_t* out, int64_t out_stride_m, int64_t out_stride_n,
+                                  void* out_sf, int64_t sf_stride_r, int64_t sf_stride_c,
+                                  void* out_sf_t, int64_t sf_t_stride_c, int64_t sf_t_stride_r,
+                                  ql_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gemm_fp8_nt_bf16
  * D = A * B^T of "DeepGEMM Essentials" Parts 1 and 6 (gemm_fp8_fp8_bf16_nt),
  * with the scale semantics of "[Help] Starter script for nn.Linear for fwd,bwd"

@@ -247,9 +247,12 @@ ql_status fp8_cast_per_token(const void* x, ql_dtype x_dtype, int64_t m, int64_t
     return from_cuda(ql::launch_cast_per_token(a, reinterpret_cast<cudaStream_t>(stream), di.num_sms));
 }
 
-ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t n, int64_t x_stride_m,
-                             int64_t x_stride_n, int fmt, uint8_t* out, int64_t out_stride_m, int64_t out_stride_n,
-                             void* out_sf, int64_t sf_stride_r, int64_t sf_stride_c, ql_stream_t stream) {
+static ql_status cast_per_block_common(const void* x, ql_dtype x_dtype, int64_t m, int64_t n,
+                                       int64_t x_stride_m, int64_t x_stride_n, int fmt, uint8_t* out,
+                                       int64_t out_stride_m, int64_t out_stride_n, void* out_sf,
+                                       int64_t sf_stride_r, int64_t sf_stride_c, void* out_sf_t,
+                                       int64_t sf_t_stride_c, int64_t sf_t_stride_r, bool dual,
+                                       ql_stream_t stream) {
     if (m < 0 || n < 0) return QL_ERR_INVALID_ARG;
     if (x_dtype != QL_BF16 && x_dtype != QL_F32) return QL_ERR_INVALID_ARG;
     const bool recip = (fmt & QL_CAST_RECIP_OF_SCALE) != 0;
@@ -258,6 +261,7 @@ ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t
     if (recip && base != QL_SF_FP32) return QL_ERR_INVALID_ARG;
     if (m == 0 || n == 0) return QL_OK;
     if (x == nullptr || out == nullptr || out_sf == nullptr) return QL_ERR_INVALID_ARG;
+    if (dual && out_sf_t == nullptr) return QL_ERR_INVALID_ARG;
     if ((m + 127) / 128 > 65535) return QL_ERR_UNSUPPORTED;
     ql::CastBlockArgs a{};
     a.x = x;
@@ -274,7 +278,26 @@ ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t
     a.sf = out_sf;
     a.ssr = sf_stride_r;
     a.ssc = sf_stride_c;
+    a.sf_t = dual ? out_sf_t : nullptr;
+    a.sst_c = sf_t_stride_c;
+    a.sst_r = sf_t_stride_r;
     return from_cuda(ql::launch_cast_per_block(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t n, int64_t x_stride_m,
+                             int64_t x_stride_n, int fmt, uint8_t* out, int64_t out_stride_m, int64_t out_stride_n,
+                             void* out_sf, int64_t sf_stride_r, int64_t sf_stride_c, ql_stream_t stream) {
+    return cast_per_block_common(x, x_dtype, m, n, x_stride_m, x_stride_n, fmt, out, out_stride_m, out_stride_n,
+                                 out_sf, sf_stride_r, sf_stride_c, nullptr, 0, 0, false, stream);
+}
+
+ql_status fp8_cast_per_block_dual(const void* x, ql_dtype x_dtype, int64_t m, int64_t n, int64_t x_stride_m,
+                                  int64_t x_stride_n, int fmt, uint8_t* out, int64_t out_stride_m,
+                                  int64_t out_stride_n, void* out_sf, int64_t sf_stride_r, int64_t sf_stride_c,
+                                  void* out_sf_t, int64_t sf_t_stride_c, int64_t sf_t_stride_r, ql_stream_t stream) {
+    return cast_per_block_common(x, x_dtype, m, n, x_stride_m, x_stride_n, fmt, out, out_stride_m, out_stride_n,
+                                 out_sf, sf_stride_r, sf_stride_c, out_sf_t, sf_t_stride_c, sf_t_stride_r, true,
+                                 stream);
 }
 
 ql_status gemm_fp8_nt_bf16(const uint8_t* a, int64_t lda, const void* sfa, int64_t sfa_stride_m,

@@ -848,7 +848,12 @@ __global__ void __launch_bounds__(128) cast_generic_kernel(const T* __restrict__
 // 128x128 block cast. One CTA (256 threads) per block; each thread holds 64
 // elements in registers. Loads follow whichever input axis is contiguous; the
 // E4M3 bytes are staged in shared memory and written along whichever output
-// axis is contiguous, so W and W^T are produced by the same kernel.
+// axis is contiguous, so W and W^T are produced by the same kernel. With
+// `sf_t` the block's scale is also written into the scale grid of the
+// transposed cast (block (r, c) at [c][r], packed along r): a block's amax
+// does not depend on orientation, so that grid is exactly the one
+// cast_per_block(W^T) makes, and W's own E4M3 bytes read MN-major with it
+// give the data-gradient operand without a second cast.
 // in_mode: 0 rows contiguous (vector), 1 columns contiguous (vector), 2 generic
 // out_mode: 0 rows contiguous, 1 columns contiguous, 2 generic
 // ---------------------------------------------------------------------------
@@ -857,7 +862,8 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
                                                          int64_t sxm, int64_t sxn, int in_mode,
                                                          uint8_t* __restrict__ out, int64_t som, int64_t son,
                                                          int out_mode, void* __restrict__ sf, int64_t ssr,
-                                                         int64_t ssc) {
+                                                         int64_t ssc, void* __restrict__ sf_t, int64_t sst_c,
+                                                         int64_t sst_r) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int B = 128;
     // E4M3 bytes of the block, [row][col] with a row pitch of 144 bytes (16-byte
@@ -954,6 +960,17 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
             word[bc % 4] = static_cast<uint8_t>(ebyte);
             if (bc == static_cast<int64_t>(gridDim.x) - 1)
                 for (int64_t z = bc % 4 + 1; z < 4; ++z) word[z] = 0;
+        }
+        if (sf_t != nullptr) {
+            if constexpr (FMT != kSfPacked) {
+                static_cast<float*>(sf_t)[bc * sst_c + br * sst_r] = s;
+            } else {
+                // packed along the row-block axis: block br is byte br % 4 of word br / 4
+                uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf_t) + bc * sst_c + (br / 4) * sst_r);
+                word[br % 4] = static_cast<uint8_t>(ebyte);
+                if (br == static_cast<int64_t>(gridDim.y) - 1)
+                    for (int64_t z = br % 4 + 1; z < 4; ++z) word[z] = 0;
+            }
         }
     }
 
@@ -1172,7 +1189,7 @@ cudaError_t launch_block_t(const CastBlockArgs& a, cudaStream_t st) {
     else if (a.som == 1 && aligned16(a.out) && a.son % 16 == 0) out_mode = 1;
     dim3 grid(static_cast<unsigned>((a.n + 127) / 128), static_cast<unsigned>((a.m + 127) / 128));
     return launch_pdl(cast_block_kernel<T, FMT, RECIP>, grid, dim3(256), 0, st, x, a.m, a.n, a.sxm, a.sxn, in_mode,
-                      a.out, a.som, a.son, out_mode, a.sf, a.ssr, a.ssc);
+                      a.out, a.som, a.son, out_mode, a.sf, a.ssr, a.ssc, a.sf_t, a.sst_c, a.sst_r);
 }
 
 template <typename T>

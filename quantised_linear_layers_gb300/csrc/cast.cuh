@@ -31,6 +31,10 @@ struct CastBlockArgs {
     int64_t som, son;
     void* sf;
     int64_t ssr, ssc;
+    // optional second scale grid, of the transposed block layout (nullptr: none):
+    // block (r, c) at [c*sst_c + r*sst_r], packed along r for packed UE8M0
+    void* sf_t;
+    int64_t sst_c, sst_r;
 };
 
 cudaError_t launch_cast_per_token(const CastTokenArgs& a, cudaStream_t st, int num_sms);

@@ -5,10 +5,10 @@ fwd,bwd" (maintainer's pseudo-code) and the integration of "DeepGEMM
 Essentials: High-Performance FP8 Matrix Multiplication" Part 18:
 
   fwd    Y  = X  W^T  : cast X per token; GEMM against W's 128x128 block cast
-  dgrad  dX = dY W    : cast dY per token; GEMM reading W's own cast MN-major
-                        with its block grid transposed (packed UE8M0 scales,
-                        whose words run along the forward K: GEMM against the
-                        block cast of W^T, read from W column-wise)
+  dgrad  dX = dY W    : cast dY per token; GEMM reading W's own E4M3 cast
+                        MN-major with the scale grid of W^T's cast, which W's
+                        block cast writes in the same pass (a block's amax
+                        does not depend on orientation)
   wgrad  dW = dY^T X  : cast dY and X with 1x128 groups along the token axis
                         into their own [T, features] layout; wgrad GEMM with
                         both operands MN-major and fp32 output, optionally
@@ -31,10 +31,11 @@ from . import ops
 
 
 class FP8Weight:
-    """A weight W [out, in] and its E4M3 casts with 128x128 block scales: W
-    (the forward operand) and W^T (the dgrad operand ``wtq`` / ``wts``, read
-    from W column-wise). With ``mn_major`` and fp32 or UE8M0 scales the dgrad
-    GEMM reads W's own cast MN-major instead and ``wtq`` / ``wts`` are None."""
+    """A weight W [out, in] and its E4M3 cast with 128x128 block scales (the
+    forward operand ``wq`` / ``ws``). With ``mn_major`` the same pass also
+    writes ``ws_t``, the scale grid of W^T's cast, and the dgrad GEMM reads
+    ``wq`` MN-major with it (``wtq`` / ``wts`` are None); otherwise W^T is cast
+    on its own (``wtq`` / ``wts``, read from W column-wise)."""
 
     def __init__(self, w: torch.Tensor, fmt: int = ops.SF_PACKED_UE8M0, mn_major: bool = True):
         self.fmt = fmt
@@ -45,10 +46,12 @@ class FP8Weight:
         if w.dim() != 2:
             raise ValueError("weight must be 2-D [out_features, in_features]")
         self.shape = tuple(w.shape)
-        self.wq, self.ws = ops.fp8_cast_per_block(w, self.fmt)
-        if self.mn_major and self.fmt != ops.SF_PACKED_UE8M0:
+        if self.mn_major:
+            self.wq, self.ws, self.ws_t = ops.fp8_cast_per_block_dual(w, self.fmt)
             self.wtq = self.wts = None
         else:
+            self.wq, self.ws = ops.fp8_cast_per_block(w, self.fmt)
+            self.ws_t = None
             self.wtq, self.wts = ops.fp8_cast_per_block(w.t(), self.fmt)
 
 
@@ -82,7 +85,7 @@ def dgrad(dy: torch.Tensor, w: FP8Weight, out: torch.Tensor | None = None) -> to
     """dX [T, in] = dY [T, out] W (bf16)."""
     dq, ds = _cast_rows(dy, w.fmt)
     if w.wtq is None:
-        return ops.gemm_fp8_nn_bf16(dq, ds, w.wq, w.ws.t(), w.fmt, out=out)
+        return ops.gemm_fp8_nn_bf16(dq, ds, w.wq, w.ws_t, w.fmt, out=out)
     return ops.gemm_fp8_nt_bf16(dq, ds, w.wtq, w.wts, w.fmt, out=out)
 
 

@@ -28,6 +28,8 @@ _i64, _vp, _int, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_s
 _SIGS = {
     "fp8_cast_per_token": [_vp, _int, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp],
     "fp8_cast_per_block": [_vp, _int, _i64, _i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp],
+    "fp8_cast_per_block_dual": [_vp, _int, _i64, _i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64,
+                                _vp, _i64, _i64, _vp],
     "gemm_fp8_nt_bf16": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
                          _i64, _i64, _i64, _vp, _sz, _vp],
     "gemm_fp8_wgrad_fp32": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
@@ -176,6 +178,34 @@ def fp8_cast_per_block(x: torch.Tensor, fmt: int = SF_FP32, recip: bool = False,
         _stream(x))
     _check("fp8_cast_per_block", st)
     return out, out_sf
+
+
+def fp8_cast_per_block_dual(x: torch.Tensor, fmt: int = SF_FP32, recip: bool = False):
+    """fp8_cast_per_block plus, from the same pass, the scale grid of the
+    transposed cast (equal to fp8_cast_per_block(x.t())'s scales): returns
+    (data [m, n], scales of x, scales of x^T). With the data read MN-major,
+    the second grid is the data-gradient operand of gemm_fp8_nn_bf16. The
+    data's rows start on 16-byte boundaries (the GEMMs' operand rows must),
+    whatever n is; the padding bytes are never written or read."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D")
+    m, n = x.shape
+    ld = _ceil(max(n, 1), 16) * 16
+    out = torch.empty((m, ld), dtype=torch.float8_e4m3fn, device=x.device)[:, :n]
+    rb, cb = _ceil(m, 128), _ceil(n, 128)
+    if fmt == SF_PACKED_UE8M0:
+        out_sf = torch.empty((rb, _ceil(cb, 4)), dtype=torch.int32, device=x.device)
+        out_sf_t = torch.empty((cb, _ceil(rb, 4)), dtype=torch.int32, device=x.device)
+    else:
+        out_sf = torch.empty((rb, cb), dtype=torch.float32, device=x.device)
+        out_sf_t = torch.empty((cb, rb), dtype=torch.float32, device=x.device)
+    code = fmt | (CAST_RECIP_OF_SCALE if recip else 0)
+    st = load_library().fp8_cast_per_block_dual(
+        x.data_ptr(), _dtype_code(x), m, n, x.stride(0), x.stride(1), code,
+        out.data_ptr(), out.stride(0), out.stride(1), out_sf.data_ptr(), out_sf.stride(0), out_sf.stride(1),
+        out_sf_t.data_ptr(), out_sf_t.stride(0), out_sf_t.stride(1), _stream(x))
+    _check("fp8_cast_per_block_dual", st)
+    return out, out_sf, out_sf_t
 
 
 def _gemm_args(a, sfa, b, sfb):

@@ -78,6 +78,11 @@ def test_host_validation_rejects_before_cuda(lib):
     # block cast: unknown format; recip with a UE8M0 format
     assert L.fp8_cast_per_block(p, 0, 4, 256, 256, 1, 3, p, 256, 1, p, 2, 1, None) == 1
     assert L.fp8_cast_per_block(p, 0, 4, 256, 256, 1, 0x102, p, 256, 1, p, 2, 1, None) == 1
+    # dual block cast: missing second scale grid; unknown format; empty problem is a no-op
+    D = L.fp8_cast_per_block_dual
+    assert D(p, 0, 4, 256, 256, 1, 2, p, 256, 1, p, 2, 1, None, 1, 1, None) == 1
+    assert D(p, 0, 4, 256, 256, 1, 3, p, 256, 1, p, 2, 1, p, 1, 1, None) == 1
+    assert D(None, 0, 0, 256, 256, 1, 2, None, 256, 1, None, 2, 1, None, 1, 1, None) == 0
     # empty problems are no-ops (no CUDA call)
     assert L.fp8_cast_per_token(None, 0, 0, 256, 256, 1, 128, 0, None, 256, 1, None, 2, 1, None) == 0
     assert L.gemm_fp8_nt_bf16(None, 16, None, 1, 1, None, 16, None, 1, 1, 0, None, 16, 0, 16, 16, None, 0,

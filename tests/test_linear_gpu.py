@@ -48,11 +48,14 @@ def test_linear_fwd_dgrad_wgrad(orc, lin, fmt, shape, mn_major):
     oq, os_ = orc.cast_per_block(np_input(w), bfmt)
     assert np.array_equal(np_bytes(w8.wq), oq) and np.array_equal(np_sf(w8.ws).view(np.uint32), os_.view(np.uint32))
     otq, ots = orc.cast_per_block(np_input(w).T, bfmt)
-    if w8.wtq is not None:                    # packed words: dgrad's own W^T cast
+    if w8.wtq is not None:                    # dgrad's own W^T cast
+        assert not mn_major
         assert np.array_equal(np_bytes(w8.wtq), otq)
         assert np.array_equal(np_sf(w8.wts).view(np.uint32), ots.view(np.uint32))
-    else:                                     # dgrad reads W's cast MN-major
-        assert mn_major and fmt != 2
+    else:                                     # dgrad reads W's cast MN-major with W^T's scale grid
+        assert mn_major
+        assert np.array_equal(np_bytes(w8.wq).T, otq)
+        assert np.array_equal(np_sf(w8.ws_t).view(np.uint32), ots.view(np.uint32))
 
     rng = np.random.default_rng(11)
     rows_t = np.sort(rng.choice(T, min(T, 24), replace=False))

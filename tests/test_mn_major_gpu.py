@@ -145,3 +145,33 @@ def test_dgrad_nn_with_w_own_cast(orc, ops, fmt):
     ref = orc.gemm(np_bytes(dq), np_sf(ds), np.ascontiguousarray(np_bytes(wq).T), np.ascontiguousarray(np_sf(ws).T),
                    fmt, out="bf16")
     check_gemm(d_nn.float().cpu().numpy(), ref, "dgrad nn")
+
+
+@pytest.mark.parametrize("path", [0, 1, 2, 3], ids=["default", "promotion", "block_scaled", "pair"])
+@pytest.mark.parametrize("fmt", [0, 1, 2], ids=["fp32", "ue8m0", "packed"])
+@pytest.mark.parametrize("shape", [(512, 1024, 768), (300, 640, 520)], ids=["512x1024x768", "ragged"])
+def test_dgrad_from_dual_block_cast(orc, ops, fmt, path, shape):
+    """dX = dY W from W's one block cast: the dual cast's second scale grid is
+    the scale grid of cast_per_block(W^T) byte for byte (a block's amax does
+    not depend on orientation; packed words run along W^T's column blocks),
+    W's E4M3 bytes are W^T's cast transposed, and the NN GEMM over them meets
+    the GEMM tolerance against the oracle on W^T's cast, in every format and
+    on every kernel."""
+    T, OUT, IN = shape
+    dy = syn.randn((T, OUT), seed=syn.SEED_DY).cuda()
+    w = syn.randn((OUT, IN), seed=syn.SEED_W, mul=0.02)
+    wq, ws, ws_t = ops.fp8_cast_per_block_dual(w.cuda(), fmt)
+    otq, ots = orc.cast_per_block(np_input(w).T, fmt)
+    oq, os_ = orc.cast_per_block(np_input(w), fmt)
+    assert np.array_equal(np_bytes(wq), oq) and np.array_equal(np_sf(ws).view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(np_bytes(wq).T, otq)
+    assert np.array_equal(np_sf(ws_t).view(np.uint32), ots.view(np.uint32))
+    dq, ds = ops.fp8_cast_per_token(dy, 128, fmt, sf_mn_major=True)
+    ops.set_gemm_path(path)
+    try:
+        dx = ops.gemm_fp8_nn_bf16(dq, ds, wq, ws_t, fmt)
+    finally:
+        ops.set_gemm_path(0)
+    assert ops.device_status() == 0
+    ref = orc.gemm(np_bytes(dq), np_sf(ds), otq, ots, fmt, out="bf16")
+    check_gemm(dx.float().cpu().numpy(), ref, "dgrad from the dual cast")
