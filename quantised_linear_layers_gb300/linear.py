@@ -155,4 +155,13 @@ class FP8Linear(torch.nn.Module):
         return self._w8
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
-        return _FP8LinearFn.apply(x, self.weight, self.fp8_weight(), self)
+        """x [..., in_features] -> [..., out_features]: leading dimensions are
+        flattened into tokens, as nn.Linear accepts them."""
+        if x.shape[-1] != self.weight.shape[1]:
+            raise ValueError(f"expected {self.weight.shape[1]} input features, got {x.shape[-1]}")
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, x.shape[-1])
+        if x2.stride(1) != 1:
+            x2 = x2.contiguous()
+        y = _FP8LinearFn.apply(x2, self.weight, self.fp8_weight(), self)
+        return y.reshape(*lead, y.shape[-1])

@@ -120,3 +120,24 @@ def test_fp8_linear_main_grad_accumulates(lin):
     m(x).backward(dy)
     assert m.weight.grad is None
     assert torch.allclose(m.main_grad, 2 * g1, rtol=1e-5, atol=1e-5)
+
+
+def test_fp8_linear_batched_input(lin):
+    """A [batch, seq, features] input is flattened into tokens like nn.Linear:
+    the output and both gradients equal those of the 2-D call."""
+    B, S, IN, OUT = 3, 100, 512, 384
+    m = lin.FP8Linear(IN, OUT, device="cuda")
+    x = syn.randn((B * S, IN), seed=syn.SEED_X).cuda()
+    dy = syn.randn((B * S, OUT), seed=syn.SEED_DY).cuda()
+    x3 = x.reshape(B, S, IN).clone().requires_grad_(True)
+    y3 = m(x3)
+    assert y3.shape == (B, S, OUT)
+    y3.backward(dy.reshape(B, S, OUT))
+    g3, gw3 = x3.grad.clone(), m.weight.grad.clone()
+    m.weight.grad = None
+    x2 = x.clone().requires_grad_(True)
+    y2 = m(x2)
+    y2.backward(dy)
+    assert torch.equal(y3.reshape(B * S, OUT), y2)
+    assert torch.equal(g3.reshape(B * S, IN), x2.grad)
+    assert torch.equal(gw3, m.weight.grad)
