@@ -102,6 +102,35 @@ ql_status fp8_cast_per_token(const void* x, ql_dtype x_dtype, int64_t m, int64_t
                              ql_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * fp8_cast_per_token_dual
+ * Both per-token casts the Linear layer takes of one activation, from a single
+ * read of it: fp8_cast_per_token(x, 128, fmt) and fp8_cast_per_token(x^T,
+ * 128, fmt). In "[Help] Starter script for nn.Linear for fwd,bwd" X is cast
+ * along its features for the forward GEMM and along the tokens for the weight
+ * gradient, and dY likewise for the data and weight gradients. The results are
+ * bit-identical to the two separate calls.
+ *   x          [m, n] bf16 or fp32, rows contiguous, row stride x_stride_m >= n.
+ *   out_rows   [m, n] E4M3, the cast of x (1x128 groups along n), row stride
+ *              out_rows_stride_m >= n; sf_rows [m, ceil(n/128)] at
+ *              sf_rows[i*sf_rows_stride_m + g*sf_rows_stride_g] (packed UE8M0:
+ *              int32 words along g, as fp8_cast_per_token).
+ *   out_cols   [m, n] E4M3, the cast of x^T (1x128 groups along m) kept in x's
+ *              own layout: element (i, j) of x at out_cols[i*out_cols_stride_m + j]
+ *              (the K-outer operand of gemm_fp8_wgrad_fp32_mn); sf_cols
+ *              [n, ceil(m/128)] at sf_cols[j*sf_cols_stride_n + g*sf_cols_stride_g].
+ *   fmt        ql_sf_format, optionally | QL_CAST_RECIP_OF_SCALE with QL_SF_FP32.
+ * m == 0 or n == 0 is a no-op. QL_ERR_INVALID_ARG for null pointers with
+ * m*n > 0, negative sizes, a row stride below n, or an unknown format.
+ * ------------------------------------------------------------------------- */
+ql_status fp8_cast_per_token_dual(const void* x, ql_dtype x_dtype, int64_t m, int64_t n,
+                                  int64_t x_stride_m, int fmt,
+                                  uint8_t* out_rows, int64_t out_rows_stride_m, void* sf_rows,
+                                  int64_t sf_rows_stride_m, int64_t sf_rows_stride_g,
+                                  uint8_t* out_cols, int64_t out_cols_stride_m, void* sf_cols,
+                                  int64_t sf_cols_stride_n, int64_t sf_cols_stride_g,
+                                  ql_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * fp8_cast_per_block
  * 128x128 block cast of "DeepGEMM Essentials" Part 4 (the RHS / weight cast).
  * Same arithmetic as fp8_cast_per_token with the group being a 128x128 block

@@ -284,6 +284,43 @@ static ql_status cast_per_block_common(const void* x, ql_dtype x_dtype, int64_t 
     return from_cuda(ql::launch_cast_per_block(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ql_status fp8_cast_per_token_dual(const void* x, ql_dtype x_dtype, int64_t m, int64_t n, int64_t x_stride_m,
+                                  int fmt, uint8_t* out_rows, int64_t out_rows_stride_m, void* sf_rows,
+                                  int64_t sf_rows_stride_m, int64_t sf_rows_stride_g, uint8_t* out_cols,
+                                  int64_t out_cols_stride_m, void* sf_cols, int64_t sf_cols_stride_n,
+                                  int64_t sf_cols_stride_g, ql_stream_t stream) {
+    if (m < 0 || n < 0) return QL_ERR_INVALID_ARG;
+    if (x_dtype != QL_BF16 && x_dtype != QL_F32) return QL_ERR_INVALID_ARG;
+    const bool recip = (fmt & QL_CAST_RECIP_OF_SCALE) != 0;
+    const int base = fmt & ~QL_CAST_RECIP_OF_SCALE;
+    if (base < QL_SF_FP32 || base > QL_SF_PACKED_UE8M0) return QL_ERR_INVALID_ARG;
+    if (recip && base != QL_SF_FP32) return QL_ERR_INVALID_ARG;
+    if (m == 0 || n == 0) return QL_OK;
+    if (x == nullptr || out_rows == nullptr || sf_rows == nullptr || out_cols == nullptr || sf_cols == nullptr)
+        return QL_ERR_INVALID_ARG;
+    if (x_stride_m < n || out_rows_stride_m < n || out_cols_stride_m < n) return QL_ERR_INVALID_ARG;
+    if ((m + 127) / 128 > 65535) return QL_ERR_UNSUPPORTED;
+    ql::CastDualArgs a{};
+    a.x = x;
+    a.is_bf16 = x_dtype == QL_BF16;
+    a.m = m;
+    a.n = n;
+    a.sxm = x_stride_m;
+    a.fmt = base;
+    a.recip = recip;
+    a.qr = out_rows;
+    a.ldr = out_rows_stride_m;
+    a.sfr = sf_rows;
+    a.srm = sf_rows_stride_m;
+    a.srg = sf_rows_stride_g;
+    a.qc = out_cols;
+    a.ldc = out_cols_stride_m;
+    a.sfc = sf_cols;
+    a.scn = sf_cols_stride_n;
+    a.scg = sf_cols_stride_g;
+    return from_cuda(ql::launch_cast_dual(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 ql_status fp8_cast_per_block(const void* x, ql_dtype x_dtype, int64_t m, int64_t n, int64_t x_stride_m,
                              int64_t x_stride_n, int fmt, uint8_t* out, int64_t out_stride_m, int64_t out_stride_n,
                              void* out_sf, int64_t sf_stride_r, int64_t sf_stride_c, ql_stream_t stream) {

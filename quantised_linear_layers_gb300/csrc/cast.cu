@@ -1056,6 +1056,168 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
     pdl_launch_dependents();
 }
 
+// ---------------------------------------------------------------------------
+// Dual per-token cast: from one read of a row-contiguous x [m, n], both the
+// per-token cast of x (1 x 128 groups along n: the forward / data-gradient
+// operand) and the per-token cast of x^T (1 x 128 groups along m: the
+// weight-gradient operand, kept in x's own [m, n] layout for the MN-major
+// GEMM). A 128 x 128 tile of x holds exactly 128 groups of each cast: its rows
+// and its columns. One CTA per tile: thread t holds rows 16i + t/16 (i < 8) at
+// columns 8(t%16) .. +8 as raw input words, so a row's amax is a 16-lane
+// reduction and a column's a reduction over the thread's 8 rows, the lane 16
+// apart and the 8 warps (through shared memory). Each row's and column's
+// scale is made by one thread; the E4M3 bytes of both casts leave with one
+// 8-byte store per row per cast (16 threads cover 128 contiguous bytes).
+// ---------------------------------------------------------------------------
+template <typename T, int FMT, bool RECIP>
+__global__ void __launch_bounds__(256, 2)
+    cast_dual_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx, uint8_t* __restrict__ qr,
+                     int64_t ldr, void* __restrict__ sfr, int64_t srm, int64_t srg, uint8_t* __restrict__ qc,
+                     int64_t ldc, void* __restrict__ sfc, int64_t scn, int64_t scg, int vec_in, int vec_out) {
+    pdl_wait_prior();           // the previous kernel's writes are complete and visible
+    constexpr int WPG = (8 * static_cast<int>(sizeof(T))) / 4;      // words per 8 elements
+    __shared__ float red[8][128];       // per-warp column maxima
+    __shared__ float fcol[128];         // column factors
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t br = blockIdx.y, bc = blockIdx.x;
+    const int64_t r0 = br * 128, c0 = bc * 128;
+    const int a0 = (tid % 16) * 8;
+    const int64_t gc = c0 + a0;
+
+    uint32_t raw[8 * WPG];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int64_t gr = r0 + it * 16 + tid / 16;
+        const T* p = x + gr * ldx + gc;
+        if (vec_in && gr < m && gc + 8 <= n) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+            raw[it * WPG + 0] = u.x; raw[it * WPG + 1] = u.y; raw[it * WPG + 2] = u.z; raw[it * WPG + 3] = u.w;
+            if constexpr (sizeof(T) == 4) {
+                const uint4 u2 = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+                raw[it * WPG + 4] = u2.x; raw[it * WPG + 5] = u2.y; raw[it * WPG + 6] = u2.z; raw[it * WPG + 7] = u2.w;
+            }
+        } else {
+            union { uint32_t w[WPG]; T t[8]; } tmp;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tmp.t[e] = (gr < m && gc + e < n) ? p[e] : T(0.0f);
+#pragma unroll
+            for (int w = 0; w < WPG; ++w) raw[it * WPG + w] = tmp.w[w];
+        }
+    }
+    auto val = [&](int it, int e) -> float {
+        if constexpr (sizeof(T) == 2) {
+            const uint32_t w = raw[it * WPG + e / 2];
+            return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+        } else {
+            return __uint_as_float(raw[it * WPG + e]);
+        }
+    };
+
+    // column maxima: over this thread's 8 rows, the lane 16 apart, the 8 warps
+    float cmax[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        float a = 0.0f;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) a = fmaxf(a, fabsf(val(it, e)));
+        cmax[e] = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+    }
+    if (lane < 16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) red[warp][a0 + e] = cmax[e];
+    }
+    // row maxima: a row's 16 chunks are one half-warp (non-negative floats
+    // order as their bits)
+    const uint32_t half = 0xFFFFu << (lane & 16);
+    uint32_t rmax[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        float a = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(val(it, e)));
+        rmax[it] = __reduce_max_sync(half, __float_as_uint(a));
+    }
+    // this thread's row (lane % 16 < 8: row 16*(lane%16) + tid/16) gets its scale
+    const int my_it = lane & 15;
+    uint32_t mine = rmax[0];
+#pragma unroll
+    for (int it = 1; it < 8; ++it)
+        if (my_it == it) mine = rmax[it];
+    float s_r, f_r;
+    uint32_t e_r;
+    group_scale<FMT, RECIP>(__uint_as_float(mine), s_r, f_r, e_r);
+    if (my_it < 8) {
+        const int64_t gr = r0 + my_it * 16 + tid / 16;
+        if (gr < m) {
+            if constexpr (FMT != kSfPacked) {
+                static_cast<float*>(sfr)[gr * srm + bc * srg] = s_r;
+            } else {
+                uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sfr) + gr * srm + (bc / 4) * srg);
+                word[bc % 4] = static_cast<uint8_t>(e_r);
+                if (bc == static_cast<int64_t>(gridDim.x) - 1)
+                    for (int64_t z = bc % 4 + 1; z < 4; ++z) word[z] = 0;
+            }
+        }
+    }
+    float frow[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) frow[it] = __shfl_sync(0xffffffffu, f_r, (lane & 16) + it);
+    __syncthreads();
+    if (tid < 128) {
+        float a = red[0][tid];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][tid]);
+        float s_c, f_c;
+        uint32_t e_c;
+        group_scale<FMT, RECIP>(a, s_c, f_c, e_c);
+        fcol[tid] = f_c;
+        const int64_t col = c0 + tid;
+        if (col < n) {
+            if constexpr (FMT != kSfPacked) {
+                static_cast<float*>(sfc)[col * scn + br * scg] = s_c;
+            } else {
+                uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sfc) + col * scn + (br / 4) * scg);
+                word[br % 4] = static_cast<uint8_t>(e_c);
+                if (br == static_cast<int64_t>(gridDim.y) - 1)
+                    for (int64_t z = br % 4 + 1; z < 4; ++z) word[z] = 0;
+            }
+        }
+    }
+    __syncthreads();
+    float fc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fc[e] = fcol[a0 + e];
+
+    // E4M3 bytes of both casts, 8 per row per cast
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int64_t gr = r0 + it * 16 + tid / 16;
+        if (gr >= m) continue;
+        const uint32_t r_lo = quant4(val(it, 0), val(it, 1), val(it, 2), val(it, 3), frow[it]);
+        const uint32_t r_hi = quant4(val(it, 4), val(it, 5), val(it, 6), val(it, 7), frow[it]);
+        const uint32_t c_lo = e4m3x2(__fmul_rn(val(it, 0), fc[0]), __fmul_rn(val(it, 1), fc[1])) |
+                              (e4m3x2(__fmul_rn(val(it, 2), fc[2]), __fmul_rn(val(it, 3), fc[3])) << 16);
+        const uint32_t c_hi = e4m3x2(__fmul_rn(val(it, 4), fc[4]), __fmul_rn(val(it, 5), fc[5])) |
+                              (e4m3x2(__fmul_rn(val(it, 6), fc[6]), __fmul_rn(val(it, 7), fc[7])) << 16);
+        uint8_t* dr = qr + gr * ldr + gc;
+        uint8_t* dc = qc + gr * ldc + gc;
+        if (vec_out && gc + 8 <= n) {
+            *reinterpret_cast<uint2*>(dr) = make_uint2(r_lo, r_hi);
+            *reinterpret_cast<uint2*>(dc) = make_uint2(c_lo, c_hi);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (gc + e < n) {
+                    dr[e] = static_cast<uint8_t>((e < 4 ? r_lo : r_hi) >> (8 * (e & 3)));
+                    dc[e] = static_cast<uint8_t>((e < 4 ? c_lo : c_hi) >> (8 * (e & 3)));
+                }
+            }
+        }
+    }
+    // this CTA's work is done: the next kernel of the stream may be scheduled
+    pdl_launch_dependents();
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
@@ -1211,6 +1373,32 @@ cudaError_t launch_cast_per_token(const CastTokenArgs& a, cudaStream_t st, int n
 
 cudaError_t launch_cast_per_block(const CastBlockArgs& a, cudaStream_t st) {
     return a.is_bf16 ? launch_block_fmt<__nv_bfloat16>(a, st) : launch_block_fmt<float>(a, st);
+}
+
+namespace {
+
+template <typename T, int FMT, bool RECIP>
+cudaError_t launch_dual_t(const CastDualArgs& a, cudaStream_t st) {
+    const T* x = static_cast<const T*>(a.x);
+    const int vec_in = aligned16(x) && (a.sxm * static_cast<int64_t>(sizeof(T))) % 16 == 0;
+    const int vec_out = (reinterpret_cast<uintptr_t>(a.qr) % 8 == 0) && (reinterpret_cast<uintptr_t>(a.qc) % 8 == 0) &&
+                        a.ldr % 8 == 0 && a.ldc % 8 == 0;
+    dim3 grid(static_cast<unsigned>((a.n + 127) / 128), static_cast<unsigned>((a.m + 127) / 128));
+    return launch_pdl(cast_dual_kernel<T, FMT, RECIP>, grid, dim3(256), 0, st, x, a.m, a.n, a.sxm, a.qr, a.ldr, a.sfr,
+                      a.srm, a.srg, a.qc, a.ldc, a.sfc, a.scn, a.scg, vec_in, vec_out);
+}
+
+template <typename T>
+cudaError_t launch_dual_fmt(const CastDualArgs& a, cudaStream_t st) {
+    if (a.fmt == kSfUe8m0) return launch_dual_t<T, kSfUe8m0, false>(a, st);
+    if (a.fmt == kSfPacked) return launch_dual_t<T, kSfPacked, false>(a, st);
+    return a.recip ? launch_dual_t<T, kSfFp32, true>(a, st) : launch_dual_t<T, kSfFp32, false>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_cast_dual(const CastDualArgs& a, cudaStream_t st) {
+    return a.is_bf16 ? launch_dual_fmt<__nv_bfloat16>(a, st) : launch_dual_fmt<float>(a, st);
 }
 
 }  // namespace ql

@@ -37,7 +37,25 @@ struct CastBlockArgs {
     int64_t sst_c, sst_r;
 };
 
+// Per-token cast of x and of x^T from one read (1 x 128 groups both ways).
+struct CastDualArgs {
+    const void* x;
+    bool is_bf16;
+    int64_t m, n, sxm;          // x [m, n], rows contiguous
+    int fmt;
+    bool recip;
+    uint8_t* qr;                // cast of x: [m, n], row stride ldr
+    int64_t ldr;
+    void* sfr;                  // its scales [m, ceil(n/128)] at (srm, srg)
+    int64_t srm, srg;
+    uint8_t* qc;                // cast of x^T, in x's layout: [m, n], row stride ldc
+    int64_t ldc;
+    void* sfc;                  // its scales [n, ceil(m/128)] at (scn, scg)
+    int64_t scn, scg;
+};
+
 cudaError_t launch_cast_per_token(const CastTokenArgs& a, cudaStream_t st, int num_sms);
+cudaError_t launch_cast_dual(const CastDualArgs& a, cudaStream_t st);
 cudaError_t launch_cast_per_block(const CastBlockArgs& a, cudaStream_t st);
 
 }  // namespace ql

@@ -20,8 +20,12 @@ operands. On GB300 the MN-major weight gradient is the faster one (its casts
 take 18 + 23 us against 25 + 38 us at dY [4096, 4096], X [4096, 7168], the
 GEMMs run at the same speed), so it is the default.
 
-W is cast once per weight update (``FP8Weight``), not every forward. Every
-step runs in the CUDA library; torch only allocates outputs.
+W is cast once per weight update (``FP8Weight``), not every forward. With
+``mn_major`` each activation is read once for both of its casts: the forward
+casts X along its features and along the tokens in one pass and keeps the
+latter (E4M3, half the bytes of X) for the weight gradient, and the backward
+casts dY both ways in one pass (``forward_saving`` / ``backward``). Every step
+runs in the CUDA library; torch only allocates outputs.
 """
 from __future__ import annotations
 
@@ -81,6 +85,27 @@ def forward(x: torch.Tensor, w: FP8Weight, out: torch.Tensor | None = None) -> t
     return ops.gemm_fp8_nt_bf16(xq, xs, w.wq, w.ws, w.fmt, out=out)
 
 
+def forward_saving(x: torch.Tensor, w: FP8Weight):
+    """Y = X W^T plus X's cast along the tokens for the weight gradient, both
+    from one read of X: returns (Y, (x_cols, x_cols_scales))."""
+    xq, xs, xcq, xcs = ops.fp8_cast_per_token_dual(x, w.fmt)
+    return ops.gemm_fp8_nt_bf16(xq, xs, w.wq, w.ws, w.fmt), (xcq, xcs)
+
+
+def backward(dy: torch.Tensor, w: FP8Weight, x_cols, need_dx: bool = True, dw_out: torch.Tensor | None = None,
+             accumulate: bool = False):
+    """dX = dY W and dW (+)= dY^T X for an MN-major weight (``w.mn_major``),
+    with dY cast along its features and along the tokens from one read and
+    x_cols from ``forward_saving``. Returns (dX or None, dW)."""
+    if not w.mn_major:
+        raise ValueError("backward() takes an MN-major FP8Weight")
+    dq, ds, dcq, dcs = ops.fp8_cast_per_token_dual(dy, w.fmt)
+    dx = ops.gemm_fp8_nn_bf16(dq, ds, w.wq, w.ws_t, w.fmt) if need_dx else None
+    xcq, xcs = x_cols
+    dw = ops.gemm_fp8_wgrad_fp32_mn(dcq, dcs, xcq, xcs, out=dw_out, accumulate=accumulate, fmt=w.fmt)
+    return dx, dw
+
+
 def dgrad(dy: torch.Tensor, w: FP8Weight, out: torch.Tensor | None = None) -> torch.Tensor:
     """dX [T, in] = dY [T, out] W (bf16)."""
     dq, ds = _cast_rows(dy, w.fmt)
@@ -106,23 +131,37 @@ def wgrad(dy: torch.Tensor, x: torch.Tensor, fmt: int = ops.SF_PACKED_UE8M0,
 class _FP8LinearFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, x, weight, w8, module):
-        ctx.save_for_backward(x)
         ctx.w8 = w8
         ctx.module = module
+        ctx.x_dtype = x.dtype
+        if w8.mn_major:
+            # keep X's token-axis cast (E4M3) for the weight gradient, not X
+            y, (xcq, xcs) = forward_saving(x, w8)
+            ctx.save_for_backward(xcq, xcs)
+            return y
+        ctx.save_for_backward(x)
         return forward(x, w8)
 
     @staticmethod
     def backward(ctx, dy):
-        (x,) = ctx.saved_tensors
         dy = dy.contiguous()
-        dx = dgrad(dy, ctx.w8) if ctx.needs_input_grad[0] else None
         module = ctx.module
-        mn = ctx.w8.mn_major
-        if module is not None and module.main_grad is not None:
-            wgrad(dy, x, ctx.w8.fmt, out=module.main_grad, accumulate=True, mn_major=mn)
+        to_main = module is not None and module.main_grad is not None
+        w8 = ctx.w8
+        if w8.mn_major:
+            xcq, xcs = ctx.saved_tensors
+            if not to_main and not ctx.needs_input_grad[1]:
+                return (dgrad(dy, w8) if ctx.needs_input_grad[0] else None), None, None, None
+            dx, dw = backward(dy, w8, (xcq, xcs), need_dx=ctx.needs_input_grad[0],
+                              dw_out=module.main_grad if to_main else None, accumulate=to_main)
+            return dx, (None if to_main else dw.to(ctx.x_dtype)), None, None
+        (x,) = ctx.saved_tensors
+        dx = dgrad(dy, w8) if ctx.needs_input_grad[0] else None
+        if to_main:
+            wgrad(dy, x, w8.fmt, out=module.main_grad, accumulate=True, mn_major=False)
             dw = None
         else:
-            dw = wgrad(dy, x, ctx.w8.fmt, mn_major=mn).to(x.dtype) if ctx.needs_input_grad[1] else None
+            dw = wgrad(dy, x, w8.fmt, mn_major=False).to(x.dtype) if ctx.needs_input_grad[1] else None
         return dx, dw, None, None
 
 

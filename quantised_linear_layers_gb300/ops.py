@@ -28,6 +28,8 @@ _i64, _vp, _int, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_s
 _SIGS = {
     "fp8_cast_per_token": [_vp, _int, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp],
     "fp8_cast_per_block": [_vp, _int, _i64, _i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp],
+    "fp8_cast_per_token_dual": [_vp, _int, _i64, _i64, _i64, _int, _vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
+                                _i64, _i64, _vp],
     "fp8_cast_per_block_dual": [_vp, _int, _i64, _i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64,
                                 _vp, _i64, _i64, _vp],
     "gemm_fp8_nt_bf16": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
@@ -178,6 +180,29 @@ def fp8_cast_per_block(x: torch.Tensor, fmt: int = SF_FP32, recip: bool = False,
         _stream(x))
     _check("fp8_cast_per_block", st)
     return out, out_sf
+
+
+def fp8_cast_per_token_dual(x: torch.Tensor, fmt: int = SF_FP32, recip: bool = False):
+    """Both per-token casts of x [T, C] from one read (1x128 groups): returns
+    (q_rows [T, C], s_rows [T, ceil(C/128)] M-major) = fp8_cast_per_token(x)
+    and (q_cols [T, C], s_cols [C, ceil(T/128)] M-major), the cast of x^T kept
+    in x's layout (the MN-major weight-gradient operand). E4M3 rows start on
+    16-byte boundaries; their padding is never written or read."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with contiguous rows")
+    t, c = x.shape
+    ld = _ceil(max(c, 1), 16) * 16
+    q_rows = torch.empty((t, ld), dtype=torch.float8_e4m3fn, device=x.device)[:, :c]
+    q_cols = torch.empty((t, ld), dtype=torch.float8_e4m3fn, device=x.device)[:, :c]
+    s_rows = empty_sf(t, sf_shape(c, 128, fmt), fmt, x.device, mn_major=True)
+    s_cols = empty_sf(c, sf_shape(t, 128, fmt), fmt, x.device, mn_major=True)
+    code = fmt | (CAST_RECIP_OF_SCALE if recip else 0)
+    st = load_library().fp8_cast_per_token_dual(
+        x.data_ptr(), _dtype_code(x), t, c, x.stride(0), code,
+        q_rows.data_ptr(), q_rows.stride(0), s_rows.data_ptr(), s_rows.stride(0), s_rows.stride(1),
+        q_cols.data_ptr(), q_cols.stride(0), s_cols.data_ptr(), s_cols.stride(0), s_cols.stride(1), _stream(x))
+    _check("fp8_cast_per_token_dual", st)
+    return q_rows, s_rows, q_cols, s_cols
 
 
 def fp8_cast_per_block_dual(x: torch.Tensor, fmt: int = SF_FP32, recip: bool = False):

@@ -78,6 +78,12 @@ def test_host_validation_rejects_before_cuda(lib):
     # block cast: unknown format; recip with a UE8M0 format
     assert L.fp8_cast_per_block(p, 0, 4, 256, 256, 1, 3, p, 256, 1, p, 2, 1, None) == 1
     assert L.fp8_cast_per_block(p, 0, 4, 256, 256, 1, 0x102, p, 256, 1, p, 2, 1, None) == 1
+    # dual per-token cast: null column output; row stride below n; recip with UE8M0; empty is a no-op
+    T2 = L.fp8_cast_per_token_dual
+    assert T2(p, 0, 4, 256, 256, 0, p, 256, p, 1, 4, None, 256, p, 1, 4, None) == 1
+    assert T2(p, 0, 4, 256, 128, 0, p, 256, p, 1, 4, p, 256, p, 1, 4, None) == 1
+    assert T2(p, 0, 4, 256, 256, 0x101, p, 256, p, 1, 4, p, 256, p, 1, 4, None) == 1
+    assert T2(None, 0, 0, 256, 256, 0, None, 256, None, 1, 4, None, 256, None, 1, 4, None) == 0
     # dual block cast: missing second scale grid; unknown format; empty problem is a no-op
     D = L.fp8_cast_per_block_dual
     assert D(p, 0, 4, 256, 256, 1, 2, p, 256, 1, p, 2, 1, None, 1, 1, None) == 1

@@ -293,3 +293,28 @@ def test_cast_column_major_into_view(orc, ops, fmt, feats):
         assert np.array_equal(gs, os_)
     else:
         assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt,recip", [(0, False), (0, True), (1, False), (2, False)],
+                         ids=["fp32", "fp32-recip", "ue8m0", "packed"])
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(4096, 1024), (300, 200), (300, 336), (129, 7168), (1, 24), (640, 4096)],
+                         ids=lambda s: f"{s[0]}x{s[1]}")
+def test_cast_dual_per_token(orc, ops, dtype, fmt, recip, shape):
+    """fp8_cast_per_token_dual: from one read of x [T, C], the per-token cast of
+    x and that of x^T (kept in x's layout), each bit for bit the oracle's cast,
+    with partial tiles in both directions, an all-zero group and huge values."""
+    t_rows, feats = shape
+    x = make_x(t_rows, feats, dtype, 128, huge=t_rows > 1)
+    qr, sr, qc, sc = ops.fp8_cast_per_token_dual(x.cuda(), fmt, recip)
+    assert ops.device_status() == 0
+    oq, os_ = orc.cast_per_token(np_input(x), 128, fmt, recip=recip)
+    assert np.array_equal(np_bytes(qr), oq), "row-cast bytes differ"
+    oqt, ost = orc.cast_per_token(np_input(x).T, 128, fmt, recip=recip)
+    assert np.array_equal(np_bytes(qc).T, oqt), "column-cast bytes differ"
+    for got, want in ((sr, os_), (sc, ost)):
+        g = np.ascontiguousarray(np_sf(got))
+        if fmt == 2:
+            assert np.array_equal(g, want)
+        else:
+            assert np.array_equal(g.view(np.uint32), np.ascontiguousarray(want).view(np.uint32))

@@ -141,3 +141,24 @@ def test_fp8_linear_batched_input(lin):
     assert torch.equal(y3.reshape(B * S, OUT), y2)
     assert torch.equal(g3.reshape(B * S, IN), x2.grad)
     assert torch.equal(gw3, m.weight.grad)
+
+
+@pytest.mark.parametrize("fmt", [0, 2], ids=["fp32", "packed"])
+def test_one_pass_casts_equal_separate_calls(lin, fmt):
+    """forward_saving / backward (each activation cast both ways in one pass)
+    give exactly the outputs and gradients of forward / dgrad / wgrad, which
+    cast each orientation separately; the accumulate form adds into a main grad."""
+    T, IN, OUT = 640, 1024, 768
+    x = syn.randn((T, IN), seed=syn.SEED_X).cuda()
+    dy = syn.randn((T, OUT), seed=syn.SEED_DY).cuda()
+    w8 = lin.FP8Weight(syn.randn((OUT, IN), seed=syn.SEED_W, mul=0.02).cuda(), fmt)
+    y1, xc = lin.forward_saving(x, w8)
+    assert torch.equal(y1, lin.forward(x, w8))
+    dx1, dw1 = lin.backward(dy, w8, xc)
+    assert torch.equal(dx1, lin.dgrad(dy, w8))
+    assert torch.equal(dw1, lin.wgrad(dy, x, fmt, mn_major=True))
+    main = syn.randn((OUT, IN), seed=5, dtype=torch.float32, mul=0.1).cuda()
+    main2 = main.clone()
+    lin.backward(dy, w8, xc, need_dx=False, dw_out=main, accumulate=True)
+    lin.wgrad(dy, x, fmt, out=main2, accumulate=True, mn_major=True)
+    assert torch.equal(main, main2)
