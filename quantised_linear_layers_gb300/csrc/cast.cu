@@ -1247,7 +1247,9 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         const int64_t chunks = (a.n + 32 * (64 / sizeof(T)) - 1) / (32 * (64 / sizeof(T)));
         const int64_t warps = a.m * chunks;
         int64_t blocks = (warps + 7) / 8;
-        const int64_t cap = static_cast<int64_t>(num_sms) * 8 * 4;   // enough warps for full-rate HBM
+        // one resident wave (4 CTAs of 8 warps per SM) walks all tasks: no CTA
+        // launches after the first, and a shorter tail at sub-L2 sizes
+        const int64_t cap = static_cast<int64_t>(num_sms) * 4;
         if (blocks > cap) blocks = cap;
         return launch_pdl(cast_rows_kernel<T, GRAN, FMT, RECIP>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
                           x, a.m, a.n, a.sxm, a.out, a.som, a.sf, a.ssm, a.ssg, chunks, vec_in, vec_out);
