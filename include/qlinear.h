@@ -405,12 +405,15 @@ ql_status ql_set_gemm_block_n(int block_n);
 /* GEMM promotion path. With UE8M0 scale formats (QL_SF_UE8M0,
  * QL_SF_PACKED_UE8M0) the default (0) promotes inside the tensor core
  * (block-scaled MMA, one power-of-two scale per row and 32-wide K slice), on
- * CTA pairs (256 x 256 tiles over two SMs) when the problem has at least one
- * such tile per pair of SMs, else on single SMs; 1 forces the CUDA-core
- * promotion path used for fp32 scales; 2 forces the single-SM block-scaled
- * kernel and 3 the CTA-pair kernel (both ignored for QL_SF_FP32). All give
- * results within the GEMM tolerance of each other. Process-wide; for tuning
- * and tests. */
+ * CTA pairs (256 x 224 or 256 x 256 tiles over two SMs) when the problem has
+ * at least one such tile per pair of SMs; with fewer tiles, split over K
+ * across a thread-block cluster when that fills the SMs, else on CTA pairs
+ * while there is a tile for every other pair, else on single SMs. 1 forces
+ * the CUDA-core promotion path used for fp32 scales; 2 forces the single-SM
+ * block-scaled kernel, 3 the CTA-pair kernel and 4 the cluster split-K
+ * kernel where it applies (2-4 ignored for QL_SF_FP32). All give results
+ * within the GEMM tolerance of each other. Process-wide; for tuning and
+ * tests. */
 ql_status ql_set_gemm_path(int path);
 
 /* Time limit of every bounded wait inside the GEMM kernel, in milliseconds

@@ -639,12 +639,17 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     const int split = (ue8m0 && !grouped && !L.out_f32) ? choose_split_k(L.m, L.n, L.k, num_sms) : 1;
     if (L.path == 4 && split >= 2) return launch_gemm_mx_sk(L, p, split, st);
     if (ue8m0 && L.path == 0 && !grouped && L.block_n == 0) {
-        // CTA pairs on 256 x 256 tiles when there are enough tiles to give
-        // every pair of SMs one; split-K over a cluster when the 128 x 256
-        // tiles are too few to occupy the SMs; else single-SM tiles.
-        const int64_t pair_tiles = ((L.m + 255) / 256) * ((L.n + 255) / 256);
+        // CTA pairs (256 x 224 tiles for bf16 output, 256 x 256 for fp32)
+        // when there is a tile for every pair of SMs; split-K over a cluster
+        // when the 128 x 128 tiles are too few to occupy the SMs; CTA pairs
+        // again down to a tile for every other pair (mid-size M: their larger
+        // tiles read A and B fewer times than single-SM tiles narrow enough to
+        // fill the SMs); else single-SM tiles.
+        const int64_t bnp = L.out_f32 ? 256 : 224;
+        const int64_t pair_tiles = ((L.m + 255) / 256) * ((L.n + bnp - 1) / bnp);
         if (pair_tiles >= num_sms / 2) return launch_gemm_mx2(L, p, st, num_sms);
         if (split >= 2) return launch_gemm_mx_sk(L, p, split, st);
+        if (pair_tiles >= num_sms / 4) return launch_gemm_mx2(L, p, st, num_sms);
     }
     if (ue8m0 && L.path != 1) return launch_gemm_mx(L, p, bn, st, num_sms);
     if (L.out_f32) return dispatch_bn<true, true>(bn, L, p, st, num_sms);
