@@ -1062,21 +1062,29 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
 // operand) and the per-token cast of x^T (1 x 128 groups along m: the
 // weight-gradient operand, kept in x's own [m, n] layout for the MN-major
 // GEMM). A 128 x 128 tile of x holds exactly 128 groups of each cast: its rows
-// and its columns. One CTA per tile: thread t holds rows 16i + t/16 (i < 8) at
-// columns 8(t%16) .. +8 as raw input words, so a row's amax is a 16-lane
-// reduction and a column's a reduction over the thread's 8 rows, the lane 16
-// apart and the 8 warps (through shared memory). Each row's and column's
+// and its columns. One CTA of 512 threads per tile: thread t holds rows
+// 32i + t/16 (i < 4) at columns 8(t%16) .. +8 as raw input words, so a row's
+// amax is a 16-lane reduction and a column's a reduction over the thread's 4
+// rows, the lane 16 apart and the 16 warps (through shared memory). Each row's and column's
 // scale is made by one thread; the E4M3 bytes of both casts leave with one
 // 8-byte store per row per cast (16 threads cover 128 contiguous bytes).
 // ---------------------------------------------------------------------------
+namespace dual {
+constexpr int kRowsPerThread = 4;                         // of the tile's 128 rows
+constexpr int kThreads = 16 * (128 / kRowsPerThread);      // 16 threads per row: 512
+constexpr int kWarps = kThreads / 32;
+}  // namespace dual
+
 template <typename T, int FMT, bool RECIP>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(dual::kThreads, 2)
     cast_dual_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx, uint8_t* __restrict__ qr,
                      int64_t ldr, void* __restrict__ sfr, int64_t srm, int64_t srg, uint8_t* __restrict__ qc,
                      int64_t ldc, void* __restrict__ sfc, int64_t scn, int64_t scg, int vec_in, int vec_out) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int WPG = (8 * static_cast<int>(sizeof(T))) / 4;      // words per 8 elements
-    __shared__ float red[8][128];       // per-warp column maxima
+    constexpr int NIT = dual::kRowsPerThread;
+    constexpr int RS = 128 / NIT;       // rows between a thread's rows
+    __shared__ float red[dual::kWarps][128];   // per-warp column maxima
     __shared__ float fcol[128];         // column factors
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t br = blockIdx.y, bc = blockIdx.x;
@@ -1084,10 +1092,10 @@ __global__ void __launch_bounds__(256, 2)
     const int a0 = (tid % 16) * 8;
     const int64_t gc = c0 + a0;
 
-    uint32_t raw[8 * WPG];
+    uint32_t raw[NIT * WPG];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int64_t gr = r0 + it * 16 + tid / 16;
+    for (int it = 0; it < NIT; ++it) {
+        const int64_t gr = r0 + it * RS + tid / 16;
         const T* p = x + gr * ldx + gc;
         if (vec_in && gr < m && gc + 8 <= n) {
             const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
@@ -1113,13 +1121,13 @@ __global__ void __launch_bounds__(256, 2)
         }
     };
 
-    // column maxima: over this thread's 8 rows, the lane 16 apart, the 8 warps
+    // column maxima: over this thread's rows, the lane 16 apart, the warps
     float cmax[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         float a = 0.0f;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) a = fmaxf(a, fabsf(val(it, e)));
+        for (int it = 0; it < NIT; ++it) a = fmaxf(a, fabsf(val(it, e)));
         cmax[e] = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
     }
     if (lane < 16) {
@@ -1129,25 +1137,25 @@ __global__ void __launch_bounds__(256, 2)
     // row maxima: a row's 16 chunks are one half-warp (non-negative floats
     // order as their bits)
     const uint32_t half = 0xFFFFu << (lane & 16);
-    uint32_t rmax[8];
+    uint32_t rmax[NIT];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < NIT; ++it) {
         float a = 0.0f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(val(it, e)));
         rmax[it] = __reduce_max_sync(half, __float_as_uint(a));
     }
-    // this thread's row (lane % 16 < 8: row 16*(lane%16) + tid/16) gets its scale
+    // lane i (i < NIT) of each half-warp makes the scale of its i-th row
     const int my_it = lane & 15;
     uint32_t mine = rmax[0];
 #pragma unroll
-    for (int it = 1; it < 8; ++it)
+    for (int it = 1; it < NIT; ++it)
         if (my_it == it) mine = rmax[it];
     float s_r, f_r;
     uint32_t e_r;
     group_scale<FMT, RECIP>(__uint_as_float(mine), s_r, f_r, e_r);
-    if (my_it < 8) {
-        const int64_t gr = r0 + my_it * 16 + tid / 16;
+    if (my_it < NIT) {
+        const int64_t gr = r0 + my_it * RS + tid / 16;
         if (gr < m) {
             if constexpr (FMT != kSfPacked) {
                 static_cast<float*>(sfr)[gr * srm + bc * srg] = s_r;
@@ -1159,14 +1167,14 @@ __global__ void __launch_bounds__(256, 2)
             }
         }
     }
-    float frow[8];
+    float frow[NIT];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) frow[it] = __shfl_sync(0xffffffffu, f_r, (lane & 16) + it);
+    for (int it = 0; it < NIT; ++it) frow[it] = __shfl_sync(0xffffffffu, f_r, (lane & 16) + it);
     __syncthreads();
     if (tid < 128) {
         float a = red[0][tid];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][tid]);
+        for (int w = 1; w < dual::kWarps; ++w) a = fmaxf(a, red[w][tid]);
         float s_c, f_c;
         uint32_t e_c;
         group_scale<FMT, RECIP>(a, s_c, f_c, e_c);
@@ -1190,8 +1198,8 @@ __global__ void __launch_bounds__(256, 2)
 
     // E4M3 bytes of both casts, 8 per row per cast
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int64_t gr = r0 + it * 16 + tid / 16;
+    for (int it = 0; it < NIT; ++it) {
+        const int64_t gr = r0 + it * RS + tid / 16;
         if (gr >= m) continue;
         const uint32_t r_lo = quant4(val(it, 0), val(it, 1), val(it, 2), val(it, 3), frow[it]);
         const uint32_t r_hi = quant4(val(it, 4), val(it, 5), val(it, 6), val(it, 7), frow[it]);
@@ -1386,8 +1394,8 @@ cudaError_t launch_dual_t(const CastDualArgs& a, cudaStream_t st) {
     const int vec_out = (reinterpret_cast<uintptr_t>(a.qr) % 8 == 0) && (reinterpret_cast<uintptr_t>(a.qc) % 8 == 0) &&
                         a.ldr % 8 == 0 && a.ldc % 8 == 0;
     dim3 grid(static_cast<unsigned>((a.n + 127) / 128), static_cast<unsigned>((a.m + 127) / 128));
-    return launch_pdl(cast_dual_kernel<T, FMT, RECIP>, grid, dim3(256), 0, st, x, a.m, a.n, a.sxm, a.qr, a.ldr, a.sfr,
-                      a.srm, a.srg, a.qc, a.ldc, a.sfc, a.scn, a.scg, vec_in, vec_out);
+    return launch_pdl(cast_dual_kernel<T, FMT, RECIP>, grid, dim3(dual::kThreads), 0, st, x, a.m, a.n, a.sxm, a.qr,
+                      a.ldr, a.sfr, a.srm, a.srg, a.qc, a.ldc, a.sfc, a.scn, a.scg, vec_in, vec_out);
 }
 
 template <typename T>
