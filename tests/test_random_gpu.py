@@ -37,7 +37,7 @@ def _scales_equal(got, want, fmt):
     return np.array_equal(g.view(np.uint32), w.view(np.uint32))
 
 
-@pytest.mark.parametrize("case", range(24))
+@pytest.mark.parametrize("case", range(64))
 def test_random_cast(orc, ops, case):
     rng = np.random.default_rng(1000 + case)
     m = int(rng.integers(1, 700))
@@ -82,7 +82,7 @@ def test_random_cast(orc, ops, case):
     assert _scales_equal(s, os_, fmt), f"{layout} m={m} n={n}: scales differ"
 
 
-@pytest.mark.parametrize("case", range(16))
+@pytest.mark.parametrize("case", range(32))
 def test_random_gemm(orc, ops, case):
     rng = np.random.default_rng(3000 + case)
     m = int(rng.integers(1, 600))
