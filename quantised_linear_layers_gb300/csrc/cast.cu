@@ -1277,12 +1277,8 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
                                 encode_2d_map(&omap, a.out, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.n, a.m, a.son, kRows, 128,
                                               /*swizzle=*/128);
             auto kern = cast_colmajor_sw_kernel<T, GRAN, FMT, RECIP>;
-            static bool attr = false;
-            if (!attr) {
-                cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-                if (e != cudaSuccess) return e;
-                attr = true;
-            }
+            if (cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), kSmemBytes); e != cudaSuccess)
+                return e;
             const int64_t units = ((a.m + 2 * BH - 1) / (2 * BH)) * ((a.n + kRows - 1) / kRows);
             int64_t grid = num_sms;
             if (grid > units) grid = units;
@@ -1307,12 +1303,8 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
             const int vec_out = aligned16(a.out) && (a.som % 16 == 0);
             const int smem = kStages * kBoxBytes + 2 * kStages * 8 + 16 + 1024;
             auto kern = cast_cols_tma_kernel<T, GRAN, FMT, RECIP>;
-            static bool attr = false;
-            if (!attr) {
-                cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                if (e != cudaSuccess) return e;
-                attr = true;
-            }
+            if (cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem); e != cudaSuccess)
+                return e;
             const int64_t units = ((a.m + BI - 1) / BI) * ((a.n + kUnit * kRows - 1) / (kUnit * kRows));
             int64_t grid = static_cast<int64_t>(num_sms) * 3;
             if (grid > units) grid = units;

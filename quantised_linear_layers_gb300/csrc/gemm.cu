@@ -34,6 +34,11 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "common.cuh"
 #include "epilogue_fp8.cuh"
 #include "epilogue_tma.cuh"
@@ -62,6 +67,33 @@ static EncodeTiledFn get_encode_fn() {
         return nullptr;
     }();
     return fn;
+}
+
+cudaError_t ensure_smem_attr(const void* kern, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::set<std::pair<const void*, int>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({kern, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert({kern, dev});
+    return e;
+}
+
+int max_active_clusters(const void* kern, const cudaLaunchConfig_t& cfg) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({kern, dev});
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = 1;
+    cache[{kern, dev}] = n;
+    return n;
 }
 
 bool encode_2d_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int64_t rows, int64_t cols,
@@ -545,12 +577,7 @@ cudaError_t launch_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int num
     const int tiles = p.tiles_m * p.tiles_n;
     int grid = tiles < num_sms ? tiles : num_sms;
     auto kern = gemm_fp8_kernel<BN, PER_ROW_B, OUT_F32, OUT_FP8>;
-    static bool attr_done = false;   // per instantiation
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    if (cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), Cf::kSmemBytes); e != cudaSuccess) return e;
     return launch_gemm_kernel(kern, static_cast<unsigned>(grid), 1, Cf::kSmemBytes, st, ta, tb, td, p);
 }
 

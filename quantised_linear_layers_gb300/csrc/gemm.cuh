@@ -152,6 +152,14 @@ cudaError_t launch_gemm_mx2(const GemmLaunch& L, const GemmParams& p, cudaStream
 int choose_split_k(int64_t m, int64_t n, int64_t k, int num_sms);
 cudaError_t launch_gemm_mx_sk(const GemmLaunch& L, GemmParams p, int split, cudaStream_t st);
 
+// Raises `kern`'s dynamic shared-memory limit to `bytes` on the current device,
+// once per (kernel, device): the attribute is per device. Thread-safe.
+cudaError_t ensure_smem_attr(const void* kern, int bytes);
+// The number of clusters of `cfg`'s shape that can be resident at once for
+// `kern` on the current device (at least 1), computed once per (kernel,
+// device). Thread-safe.
+int max_active_clusters(const void* kern, const cudaLaunchConfig_t& cfg);
+
 // 2-D uint8 tensor map [rows, cols] (cols contiguous, row stride ld bytes),
 // box [box_rows x 128 bytes], 128-byte swizzle, zero fill out of bounds.
 bool encode_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows);

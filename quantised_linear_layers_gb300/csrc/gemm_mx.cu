@@ -486,12 +486,7 @@ cudaError_t launch_mx_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int 
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = tiles < num_sms ? tiles : num_sms;
     auto kern = gemm_mx_kernel<BN, PER_ROW_B, OUT_F32, OUT_FP8>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    if (cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), Cf::kSmemBytes); e != cudaSuccess) return e;
     return launch_gemm_kernel(kern, static_cast<unsigned>(grid), 1, Cf::kSmemBytes, st, ta, tb, td, p);
 }
 

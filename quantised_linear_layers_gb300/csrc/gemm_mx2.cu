@@ -555,12 +555,7 @@ cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int
     if (pairs < 1) pairs = 1;
     if (tiles < pairs) pairs = tiles;
     auto kern = gemm_mx2_kernel<BN, PER_ROW_B, OUT_F32, OUT_FP8>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    if (cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), Cf::kSmemBytes); e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -574,12 +569,7 @@ cudaError_t launch_mx2_t(const GemmLaunch& L, GemmParams p, cudaStream_t st, int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // a persistent grid of no more pairs than can be resident at once
-    static int max_pairs = 0;
-    if (max_pairs == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = 1;
-        max_pairs = n;
-    }
+    const int max_pairs = max_active_clusters(reinterpret_cast<const void*>(kern), cfg);
     if (pairs > max_pairs) {
         pairs = max_pairs;
         cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);

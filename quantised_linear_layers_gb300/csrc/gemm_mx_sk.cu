@@ -421,12 +421,7 @@ cudaError_t launch_gemm_mx_sk(const GemmLaunch& L, GemmParams p, int split, cuda
     p.tiles_n = static_cast<int>((L.n + BN - 1) / BN);
     const int tiles = p.tiles_m * p.tiles_n;
     auto kern = gemm_mx_sk_kernel;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    if (cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), Cf::kSmemBytes); e != cudaSuccess) return e;
     return launch_gemm_kernel(kern, static_cast<unsigned>(tiles * split), static_cast<unsigned>(split), Cf::kSmemBytes,
                               st, ta, tb, p);
 }
