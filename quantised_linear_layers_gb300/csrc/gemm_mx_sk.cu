@@ -167,8 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmap_a);
         tma_prefetch_desc(&tmap_b);
-        // this CTA's first weight tiles into L2 while the previous kernel finishes
-        for (int kb = kb0; kb < kb1 && kb < kb0 + C::kStages; ++kb) tma_prefetch_l2_2d(&tmap_b, kb * BK, nb * BN);
+        // This CTA's weight tiles into L2 while the previous kernel finishes
+        // (B does not depend on it): all of its K range, so the whole weight
+        // streams from HBM at once instead of a smem ring's depth at a time;
+        // at most 64 MB over the grid, well inside L2.
+        const int pf_cap = static_cast<int>((64u << 20) / (gridDim.x * static_cast<unsigned>(BN * BK)));
+        const int pf = pf_cap > C::kStages ? pf_cap : C::kStages;
+        for (int kb = kb0; kb < kb1 && kb < kb0 + pf; ++kb) tma_prefetch_l2_2d(&tmap_b, kb * BK, nb * BN);
     }
     if (warp == 1) { tmem_alloc(tmem_base_sm, C::kTmemCols); tmem_relinquish(); }
     tc_fence_before_sync();

@@ -123,8 +123,10 @@ def wgrad(dy: torch.Tensor, x: torch.Tensor, fmt: int = ops.SF_PACKED_UE8M0,
         aq, sa = _cast_cols(dy, fmt)
         bq, sb = _cast_cols(x, fmt)
         return ops.gemm_fp8_wgrad_fp32_mn(aq, sa, bq, sb, out=out, accumulate=accumulate, fmt=fmt)
+    # both scale grids M-major: the scale loaders read 32 consecutive rows'
+    # scales per load (K-major per-row B scales do not coalesce)
     aq, sa = _cast_rows(dy.t(), fmt)
-    bq, sb = _cast_rows(x.t(), fmt, mn_major=False)
+    bq, sb = _cast_rows(x.t(), fmt)
     return ops.gemm_fp8_wgrad_fp32(aq, sa, bq, sb, out=out, accumulate=accumulate, fmt=fmt)
 
 
