@@ -8,7 +8,6 @@ return, and the context must stay usable (the next call is correct). Covered
 for the CUDA-core promotion kernel, the single-SM block-scaled kernel, the
 CTA-pair kernel and the split-K cluster kernel.
 """
-import numpy as np
 import pytest
 import torch
 

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import check_gemm, np_bytes, np_input, np_sf
+from helpers import check_gemm, np_bytes, np_sf
 from quantised_linear_layers_gb300 import synthetic as syn
 
 pytestmark = pytest.mark.gpu

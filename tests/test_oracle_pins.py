@@ -8,7 +8,6 @@ direction, transposed scale grid, wrong group boundary, lost sign) fails at
 least one of them.
 """
 import json
-import math
 import os
 
 import numpy as np

@@ -8,7 +8,6 @@ run the same kernels on the same row chunks. Called through the C ABI.
 
 This file is collected last on purpose: a run that stops at the first failure
 has already run every other test when it gets here."""
-import ctypes
 
 import pytest
 import torch
