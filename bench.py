@@ -637,9 +637,12 @@ def run_reference(args, world, rank):
         secs += s
         rows_total += rows
     value = statistics.median(vals)
+    # one whole step of the workload at the sampled rate (the GEMM's 2mnk flop)
+    ms_full = 2.0 * m * n * k / (value * 1e12) * 1e3 if value > 0 else None
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_full, "ms_per_step_note": "whole step extrapolated from the sample",
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn; W randn*0.02)",
         "config": {"workload": WORKLOAD, "m": m, "n": n, "k": k, "gran_k": 128, "scales": args.fmt},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
