@@ -385,6 +385,12 @@ ql_status ql_cast_gemm_host_noalloc(const void* x_host, int64_t ldx, const uint8
                                     uint16_t* d_host, int64_t ldd, int64_t m, int64_t n, int64_t k,
                                     int64_t chunk_rows, ql_stream_t stream);
 
+/* The binary version (major * 10 + minor, 103 for sm_103a) of the kernel
+ * image the CUDA runtime loaded for this library on the current device, from
+ * cudaFuncGetAttributes; 0 if the runtime reports an error (no device, or no
+ * image for it). A diagnostic: it launches nothing. */
+int ql_binary_version(void);
+
 /* Workspace bytes a GEMM of this shape needs (0 in this build). */
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k);
 

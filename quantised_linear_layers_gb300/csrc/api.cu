@@ -138,31 +138,55 @@ ql_status gemm_common(const uint8_t* a, int64_t lda, const void* sfa, int64_t sa
 constexpr int kPipeSlots = 2;
 
 struct Pipe {
-    bool ready = false;
+    std::atomic<bool> ready{false};   // published only after every stream and event exists
+    std::mutex init_mu;               // serialises the one-time set-up
     cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
     cudaEvent_t start = nullptr, end = nullptr;
     cudaEvent_t in_done[kPipeSlots] = {}, comp_done[kPipeSlots] = {}, out_done[kPipeSlots] = {};
-    std::mutex mu;
+    std::mutex mu;                    // one call at a time runs the pipeline
 };
 Pipe g_pipe[kMaxDevices];
 
+// Destroys whatever a failed set-up created, so that the next call retries.
+void pipe_destroy(Pipe& p) {
+    cudaEvent_t* evs[] = {&p.start, &p.end};
+    for (cudaEvent_t* e : evs)
+        if (*e) { cudaEventDestroy(*e); *e = nullptr; }
+    for (int i = 0; i < kPipeSlots; ++i) {
+        cudaEvent_t* slot[] = {&p.in_done[i], &p.comp_done[i], &p.out_done[i]};
+        for (cudaEvent_t* e : slot)
+            if (*e) { cudaEventDestroy(*e); *e = nullptr; }
+    }
+    cudaStream_t* sts[] = {&p.in, &p.comp, &p.out};
+    for (cudaStream_t* s : sts)
+        if (*s) { cudaStreamDestroy(*s); *s = nullptr; }
+}
+
+// The current device's pipeline; its streams and events are created by the
+// first call on the device, under a lock, and published once all exist.
 ql_status pipe_for_device(Pipe*& out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QL_ERR_CUDA;
     Pipe& p = g_pipe[dev];
-    if (!p.ready) {
-        const unsigned fl = cudaEventDisableTiming;
-        if (cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&p.start, fl) != cudaSuccess || cudaEventCreateWithFlags(&p.end, fl) != cudaSuccess)
-            return QL_ERR_CUDA;
-        for (int i = 0; i < kPipeSlots; ++i)
-            if (cudaEventCreateWithFlags(&p.in_done[i], fl) != cudaSuccess ||
-                cudaEventCreateWithFlags(&p.comp_done[i], fl) != cudaSuccess ||
-                cudaEventCreateWithFlags(&p.out_done[i], fl) != cudaSuccess)
+    if (!p.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(p.init_mu);
+        if (!p.ready.load(std::memory_order_relaxed)) {
+            const unsigned fl = cudaEventDisableTiming;
+            bool ok = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
+                      cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking) == cudaSuccess &&
+                      cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess &&
+                      cudaEventCreateWithFlags(&p.start, fl) == cudaSuccess &&
+                      cudaEventCreateWithFlags(&p.end, fl) == cudaSuccess;
+            for (int i = 0; ok && i < kPipeSlots; ++i)
+                ok = cudaEventCreateWithFlags(&p.in_done[i], fl) == cudaSuccess &&
+                     cudaEventCreateWithFlags(&p.comp_done[i], fl) == cudaSuccess &&
+                     cudaEventCreateWithFlags(&p.out_done[i], fl) == cudaSuccess;
+            if (!ok) {
+                pipe_destroy(p);
                 return QL_ERR_CUDA;
-        p.ready = true;
+            }
+            p.ready.store(true, std::memory_order_release);
+        }
     }
     out = &p;
     return QL_OK;
@@ -190,6 +214,10 @@ SlotLayout slot_layout(int64_t n, int64_t k, int64_t rows, int fmt) {
     L.total = L.x + L.q + L.s + L.d;
     return L;
 }
+
+// Never launched: its attributes tell which binary the runtime loaded for
+// this library's kernels.
+__global__ void ql_probe_kernel() {}
 
 }  // namespace
 
@@ -434,6 +462,11 @@ ql_status ql_cast_gemm_host(const void* x_host, int64_t ldx, const uint8_t* b, i
     if (x_host == nullptr || d_host == nullptr || b == nullptr || sfb == nullptr || workspace == nullptr)
         return QL_ERR_INVALID_ARG;
     if (ldx < k || ldd < n) return QL_ERR_INVALID_ARG;
+    // the GEMM's own checks of B, made here so that an error returns before
+    // anything is queued
+    if (n >= (int64_t(1) << 31) || k >= (int64_t(1) << 31)) return QL_ERR_UNSUPPORTED;
+    if (ldb < k) return QL_ERR_INVALID_ARG;
+    if (!aligned16(b) || ldb % 16 != 0) return QL_ERR_ALIGNMENT;
     const SlotLayout sl = slot_layout(n, k, chunk_rows, fmt);
     if (ws_bytes < kPipeSlots * sl.total) return QL_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QL_ERR_ALIGNMENT;
@@ -451,7 +484,7 @@ ql_status ql_cast_gemm_host(const void* x_host, int64_t ldx, const uint8_t* b, i
         return QL_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const int64_t chunks = (m + chunk_rows - 1) / chunk_rows;
-    for (int64_t c = 0; c < chunks; ++c) {
+    for (int64_t c = 0; c < chunks && st == QL_OK; ++c) {
         const int slot = static_cast<int>(c % kPipeSlots);
         const int64_t r0 = c * chunk_rows;
         const int64_t rc = (m - r0) < chunk_rows ? (m - r0) : chunk_rows;
@@ -461,33 +494,52 @@ ql_status ql_cast_gemm_host(const void* x_host, int64_t ldx, const uint8_t* b, i
         void* sb = base + sl.x + sl.q;
         uint16_t* db = reinterpret_cast<uint16_t*>(base + sl.x + sl.q + sl.s);
         // copy in: the slot's X buffer is free once chunk c - slots was cast
-        if (c >= kPipeSlots && !ck(cudaStreamWaitEvent(P.in, P.comp_done[slot], 0))) return QL_ERR_CUDA;
+        if (c >= kPipeSlots && !ck(cudaStreamWaitEvent(P.in, P.comp_done[slot], 0))) { st = QL_ERR_CUDA; break; }
         if (!ck(cudaMemcpy2DAsync(xb, static_cast<size_t>(k) * 2,
                                   static_cast<const uint8_t*>(x_host) + static_cast<size_t>(r0) * ldx * 2,
                                   static_cast<size_t>(ldx) * 2, static_cast<size_t>(k) * 2, static_cast<size_t>(rc),
                                   cudaMemcpyHostToDevice, P.in)) ||
-            !ck(cudaEventRecord(P.in_done[slot], P.in)))
-            return QL_ERR_CUDA;
+            !ck(cudaEventRecord(P.in_done[slot], P.in))) {
+            st = QL_ERR_CUDA;
+            break;
+        }
         // cast + GEMM: after the copy in, and after the slot's D went out
-        if (!ck(cudaStreamWaitEvent(P.comp, P.in_done[slot], 0))) return QL_ERR_CUDA;
-        if (c >= kPipeSlots && !ck(cudaStreamWaitEvent(P.comp, P.out_done[slot], 0))) return QL_ERR_CUDA;
+        if (!ck(cudaStreamWaitEvent(P.comp, P.in_done[slot], 0)) ||
+            (c >= kPipeSlots && !ck(cudaStreamWaitEvent(P.comp, P.out_done[slot], 0)))) {
+            st = QL_ERR_CUDA;
+            break;
+        }
         st = fp8_cast_per_token(xb, QL_BF16, rc, k, k, 1, 128, fmt, qb, sl.ldq, 1, sb, 1, sl.sld,
                                 reinterpret_cast<ql_stream_t>(P.comp));
-        if (st != QL_OK) return st;
-        st = gemm_fp8_nt_bf16(qb, sl.ldq, sb, 1, sl.sld, b, ldb, sfb, sfb_stride_n, sfb_stride_k, fmt, db, n, rc, n, k,
-                              nullptr, 0, reinterpret_cast<ql_stream_t>(P.comp));
-        if (st != QL_OK) return st;
-        if (!ck(cudaEventRecord(P.comp_done[slot], P.comp))) return QL_ERR_CUDA;
+        if (st == QL_OK)
+            st = gemm_fp8_nt_bf16(qb, sl.ldq, sb, 1, sl.sld, b, ldb, sfb, sfb_stride_n, sfb_stride_k, fmt, db, n, rc,
+                                  n, k, nullptr, 0, reinterpret_cast<ql_stream_t>(P.comp));
+        if (st != QL_OK) break;
+        if (!ck(cudaEventRecord(P.comp_done[slot], P.comp))) { st = QL_ERR_CUDA; break; }
         // copy out
         if (!ck(cudaStreamWaitEvent(P.out, P.comp_done[slot], 0)) ||
             !ck(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(d_host) + static_cast<size_t>(r0) * ldd * 2,
                                   static_cast<size_t>(ldd) * 2, db, static_cast<size_t>(n) * 2,
                                   static_cast<size_t>(n) * 2, static_cast<size_t>(rc), cudaMemcpyDeviceToHost, P.out)) ||
-            !ck(cudaEventRecord(P.out_done[slot], P.out)))
-            return QL_ERR_CUDA;
+            !ck(cudaEventRecord(P.out_done[slot], P.out))) {
+            st = QL_ERR_CUDA;
+            break;
+        }
     }
-    if (!ck(cudaEventRecord(P.end, P.out)) || !ck(cudaStreamWaitEvent(cs, P.end, 0))) return QL_ERR_CUDA;
-    return QL_OK;
+    // Whatever happened, the caller's stream resumes only after everything the
+    // call queued on the three streams (copies touching the caller's host
+    // buffers included), so an error return leaves nothing unordered.
+    if (!ck(cudaEventRecord(P.in_done[0], P.in)) || !ck(cudaStreamWaitEvent(P.out, P.in_done[0], 0)) ||
+        !ck(cudaEventRecord(P.comp_done[0], P.comp)) || !ck(cudaStreamWaitEvent(P.out, P.comp_done[0], 0)) ||
+        !ck(cudaEventRecord(P.end, P.out)) || !ck(cudaStreamWaitEvent(cs, P.end, 0)))
+        return QL_ERR_CUDA;
+    return st;
+}
+
+int ql_binary_version(void) {
+    cudaFuncAttributes attr{};
+    if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void*>(&ql_probe_kernel)) != cudaSuccess) return 0;
+    return attr.binaryVersion;
 }
 
 size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k) {

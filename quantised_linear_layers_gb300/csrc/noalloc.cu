@@ -47,10 +47,12 @@ extern "C" ql_status ql_cast_gemm_host_noalloc(const void* x_host, int64_t ldx, 
                                                const void* sfb, int64_t sfb_stride_n, int64_t sfb_stride_k, int fmt,
                                                uint16_t* d_host, int64_t ldd, int64_t m, int64_t n, int64_t k,
                                                int64_t chunk_rows, ql_stream_t stream) {
+    // the checks of ql_cast_gemm_host that come before any size, in its order
     if (m < 0 || n < 0 || k <= 0 || chunk_rows <= 0) return QL_ERR_INVALID_ARG;
+    if (fmt < QL_SF_FP32 || fmt > QL_SF_PACKED_UE8M0) return QL_ERR_INVALID_ARG;
+    if (m == 0 || n == 0) return QL_OK;
     const size_t need = ql_cast_gemm_host_workspace_size(n, k, chunk_rows, fmt);
     if (need == 0 || need > QL_NOALLOC_SCRATCH_BYTES) return QL_ERR_UNSUPPORTED;   // does not fit: fewer rows per chunk
-    if (m == 0 || n == 0) return QL_OK;
     void* ws = nullptr;
     const ql_status st = scratch_address(ws);
     if (st != QL_OK) return st;

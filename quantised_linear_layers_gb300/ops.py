@@ -53,6 +53,7 @@ _SIGS = {
     "ql_gemm_workspace_size": [_i64, _i64, _i64],
     "ql_set_num_sms": [_int],
     "ql_get_num_sms": [],
+    "ql_binary_version": [],
     "ql_set_wait_limit_ms": [_int],
     "ql_set_gemm_block_n": [_int],
     "ql_set_gemm_path": [_int],

@@ -196,6 +196,73 @@ def test_block_cast_writes_transpose(orc, ops, fmt, shape):
     assert torch.equal(s2, st_store)
 
 
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(300, 200), (1, 130), (129, 384), (4096, 7168)],
+                         ids=lambda s: f"{s[0]}x{s[1]}")
+def test_block_cast_recip_of_scale(orc, ops, dtype, shape):
+    """QL_CAST_RECIP_OF_SCALE on the block cast and its dual form (factor
+    fl32(1 / fl32(amax / 448))): bytes, W's scale grid and W^T's grid all equal
+    the oracle's recip branch, on ragged shapes and the 4096 x 7168 weight."""
+    w = syn.randn(shape, seed=syn.SEED_W, dtype=dtype, mul=0.02)
+    if shape[0] >= 256:
+        w[128:256, 0:128] = 0                             # an all-zero block
+    oq, os_ = orc.cast_per_block(np_input(w), 0, recip=True)
+    q, s = ops.fp8_cast_per_block(w.cuda(), 0, recip=True)
+    assert np.array_equal(np_bytes(q), oq)
+    assert np.array_equal(np_sf(s).view(np.uint32), os_.view(np.uint32))
+    qd, sd, sdt = ops.fp8_cast_per_block_dual(w.cuda(), 0, recip=True)
+    otq, ots = orc.cast_per_block(np_input(w).T, 0, recip=True)
+    assert np.array_equal(np_bytes(qd), oq)
+    assert np.array_equal(np_bytes(qd).T, otq)
+    assert np.array_equal(np_sf(sd).view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(np_sf(sdt).view(np.uint32), ots.view(np.uint32))
+
+
+@pytest.mark.parametrize("shape", [(256, 384), (300, 520)], ids=lambda s: f"{s[0]}x{s[1]}")
+def test_block_cast_recip_where_readings_differ(orc, ops, shape):
+    """fp32 blocks built so that the two readings of the factor give different
+    bytes: the kernel follows the oracle in each branch, so the option is not
+    ignored, and the transposed-view cast agrees too."""
+    import recip_inputs
+    x = recip_inputs.sensitive_blocks(*shape, seed=9)
+    xt = torch.from_numpy(x)
+    for recip in (False, True):
+        oq, os_ = orc.cast_per_block(x, 0, recip=recip)
+        q, s = ops.fp8_cast_per_block(xt.cuda(), 0, recip=recip)
+        assert np.array_equal(np_bytes(q), oq), f"recip={recip}"
+        assert np.array_equal(np_sf(s).view(np.uint32), os_.view(np.uint32))
+        qt, st = ops.fp8_cast_per_block(xt.cuda().t(), 0, recip=recip)
+        otq, ots = orc.cast_per_block(x.T, 0, recip=recip)
+        assert np.array_equal(np_bytes(qt), otq) and np.array_equal(np_sf(st).view(np.uint32), ots.view(np.uint32))
+    assert not np.array_equal(orc.cast_per_block(x, 0)[0], orc.cast_per_block(x, 0, recip=True)[0])
+
+
+@pytest.mark.parametrize("gran", GRANS)
+def test_token_cast_recip_where_readings_differ(orc, ops, gran):
+    """The per-token cast's recip option on rows built so that the two
+    readings give different bytes: row, transposed-view and dual kernels."""
+    import recip_inputs
+    x = recip_inputs.sensitive_rows(130, 520, gran, seed=10)
+    xt = torch.from_numpy(x).cuda()
+    for recip in (False, True):
+        oq, os_ = orc.cast_per_token(x, gran, 0, recip=recip)
+        q, s = ops.fp8_cast_per_token(xt, gran, 0, recip=recip)
+        assert np.array_equal(np_bytes(q), oq), f"recip={recip}"
+        assert np.array_equal(np_sf(s).view(np.uint32), os_.view(np.uint32))
+        qt, st = ops.fp8_cast_per_token(xt.t().contiguous().t(), gran, 0, recip=recip)   # column-major input
+        assert np.array_equal(np_bytes(qt), oq) and np.array_equal(np_sf(st).view(np.uint32), os_.view(np.uint32))
+        if gran == 128:
+            qr, sr, qc, sc = ops.fp8_cast_per_token_dual(xt, 0, recip)
+            assert np.array_equal(np_bytes(qr), oq)
+            assert np.array_equal(np.ascontiguousarray(np_sf(sr)).view(np.uint32), os_.view(np.uint32))
+            oqt, ost = orc.cast_per_token(x.T, 128, 0, recip=recip)
+            assert np.array_equal(np_bytes(qc).T, oqt)
+            assert np.array_equal(np.ascontiguousarray(np_sf(sc)).view(np.uint32),
+                                  np.ascontiguousarray(ost).view(np.uint32))
+    oq0 = orc.cast_per_token(x, gran, 0)[0]
+    assert not np.array_equal(oq0, orc.cast_per_token(x, gran, 0, recip=True)[0])
+
+
 def test_block_cast_large_weight_ue8m0(orc, ops):
     """The 18432 x 7168 weight of the large cast+GEMM workload, UE8M0."""
     w = syn.randn((18432, 7168), seed=syn.SEED_W, mul=0.02)

@@ -5,14 +5,15 @@ High-Performance FP8 Matrix Multiplication" Part 3, with the group and UE8M0
 options) of the bf16 output that the bf16 GEMM computes with the same tiles:
 the bf16 GEMM's output (itself judged against the exact product elsewhere) is
 fed to the CPU oracle's cast, whose bytes and scales must match bit for bit.
-The dequantised fused output is also checked against the exact product with
-a bound that adds E4M3's rounding step to the GEMM tolerance.
+The bf16 output is held to the GEMM tolerance against the oracle's exact
+product in the same case, and the dequantised fused output is checked against
+that product with a bound that adds E4M3's rounding step.
 """
 import numpy as np
 import pytest
 import torch
 
-from helpers import np_bytes, np_input, np_sf
+from helpers import check_gemm, np_bytes, np_input, np_sf
 from quantised_linear_layers_gb300 import synthetic as syn
 
 pytestmark = pytest.mark.gpu
@@ -71,6 +72,9 @@ def test_fused_cast_equals_cast_of_bf16_output(orc, ops, kcase, gran, out_fmt, r
         ops.set_gemm_block_n(0)
         ops.set_gemm_path(0)
     assert ops.device_status() == 0
+    # the bf16 output the fused cast starts from is itself the method's output
+    ref = orc.gemm(np_bytes(xq), np_sf(xs), np_bytes(wq), np_sf(ws), fmt)
+    check_gemm(y.float().cpu().numpy(), orc.round_output(ref, "bf16"), "bf16 output")
     oq, osf = orc.cast_per_token(np_input(y), gran, out_fmt, recip)
     assert np.array_equal(np_bytes(q), oq), "E4M3 bytes differ from the cast of the bf16 output"
     got_sf = np_sf(sf)
@@ -79,7 +83,6 @@ def test_fused_cast_equals_cast_of_bf16_output(orc, ops, kcase, gran, out_fmt, r
     else:
         assert np.array_equal(got_sf.view(np.uint32), osf.view(np.uint32))
     # against the exact product: GEMM tolerance plus half an E4M3 step
-    ref = orc.gemm(np_bytes(xq), np_sf(xs), np_bytes(wq), np_sf(ws), fmt)
     deq = dequant(q, sf, gran, out_fmt, n)
     rel = np.linalg.norm(deq - ref) / np.linalg.norm(ref)
     assert rel < 0.05, f"relative Frobenius error {rel:.3e}"
@@ -102,7 +105,6 @@ def test_worked_shape_default_path(orc, ops):
     w2q, w2s = ops.fp8_cast_per_block(w2.cuda(), 2)
     d2 = ops.gemm_fp8_nt_bf16(q, sf, w2q, w2s, 2)
     ref2 = orc.gemm(np_bytes(q), np_sf(sf), np_bytes(w2q), np_sf(w2s), 2, out="bf16")
-    from helpers import check_gemm
     check_gemm(d2.float().cpu().numpy(), ref2, "next layer")
 
 

@@ -124,15 +124,28 @@ def test_linear_fwd_hidden7168(orc, ops, m, fmt):
     check_gemm(got if rows is None else got[rows], ref)
 
 
+def rows_per_tile(m, seed):
+    """Two sampled rows in every 256-row M tile, one in each 128-row half (the
+    two CTAs of a pair tile, two M tiles of the single-SM kernels), plus the
+    first and last rows; every column of each row is checked."""
+    rng = np.random.default_rng(seed)
+    rows = [0, m - 1]
+    for t0 in range(0, m, 256):
+        for h in (0, 128):
+            lo = t0 + h
+            if lo < m:
+                rows.append(int(rng.integers(lo, min(lo + 128, m))))
+    return np.unique(np.array(rows))
+
+
 def test_large_ue8m0_sampled_rows(orc, ops):
     """X [16384, 7168] x W [18432, 7168]^T with UE8M0 scales, checked on
-    sampled rows (the oracle computes them one by one)."""
+    sampled rows of every M tile (the oracle computes them one by one)."""
     m, n, k = 16384, 18432, 7168
     x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, 1, w_mul=0.02)
     d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 1)
-    rows = np.sort(np.random.default_rng(3).choice(m, 12, replace=False))
-    rows[0] = 0
-    rows[-1] = m - 1
+    rows = rows_per_tile(m, 3)
+    assert len(rows) >= 2 * (m // 256)
     ref = oracle_fwd(orc, xq, xs, wq, ws, 1, rows=rows)
     check_gemm(d[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref)
 
@@ -290,7 +303,8 @@ def test_block_scaled_matches_promotion_random(orc, ops, fmt):
 @pytest.mark.parametrize("path", [2, 3], ids=["block_scaled", "pair"])
 def test_large_packed_sampled_rows(orc, ops, path):
     """The large cast+GEMM workload with packed UE8M0 scales on the 1-SM and
-    CTA-pair block-scaled kernels, sampled rows and the ragged last rows."""
+    CTA-pair block-scaled kernels, two sampled rows in every 256-row M tile
+    (both CTAs of each pair tile) and the last row."""
     m, n, k = 16384, 18432, 7168
     x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, 2, w_mul=0.02)
     ops.set_gemm_path(path)
@@ -299,8 +313,7 @@ def test_large_packed_sampled_rows(orc, ops, path):
     finally:
         ops.set_gemm_path(0)
     assert ops.device_status() == 0
-    rows = np.sort(np.random.default_rng(5).choice(m, 10, replace=False))
-    rows[0], rows[-1] = 0, m - 1
+    rows = rows_per_tile(m, 5)
     ref = oracle_fwd(orc, xq, xs, wq, ws, 2, rows=rows)
     check_gemm(d[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref)
 

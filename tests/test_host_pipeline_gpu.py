@@ -74,3 +74,61 @@ def test_host_pipeline_large_workload_sampled(orc, ops):
     check_gemm(out[rows].float().numpy(), oref, "host pipeline, large")
     ref = device_reference(ops, x, wq, ws, 2, chunk)
     assert torch.equal(out, ref)
+
+
+_TWO_THREADS = r"""
+import sys, threading
+import torch
+sys.path.insert(0, sys.argv[1])
+from quantised_linear_layers_gb300 import ops
+from quantised_linear_layers_gb300 import synthetic as syn
+
+torch.cuda.init()
+m, n, k, chunk, fmt = 700, 512, 384, 128, 2
+wq, ws = ops.fp8_cast_per_block(syn.randn((n, k), seed=syn.SEED_W, mul=0.02).cuda(), fmt)
+xs = [syn.randn((m, k), seed=s).pin_memory() for s in (31, 32)]
+outs = [torch.zeros((m, n), dtype=torch.bfloat16).pin_memory() for _ in xs]
+streams = [torch.cuda.Stream() for _ in xs]
+wsps = [torch.empty(ops.cast_gemm_host_workspace_size(n, k, chunk, fmt), dtype=torch.uint8, device="cuda")
+        for _ in xs]
+torch.cuda.synchronize()
+start = threading.Barrier(2)
+errors = []
+
+def run(i):
+    try:
+        torch.cuda.set_device(0)
+        with torch.cuda.stream(streams[i]):
+            start.wait()
+            ops.cast_gemm_host(xs[i], wq, ws, fmt, outs[i], chunk, wsps[i])
+            streams[i].synchronize()
+    except Exception as e:  # reported by the parent
+        errors.append(repr(e))
+
+threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+for t in threads:
+    t.start()
+for t in threads:
+    t.join()
+assert not errors, errors
+assert ops.device_status() == 0
+for i in range(2):       # the same calls one after the other
+    ref = torch.zeros((m, n), dtype=torch.bfloat16).pin_memory()
+    ops.cast_gemm_host(xs[i], wq, ws, fmt, ref, chunk, wsps[i])
+    torch.cuda.synchronize()
+    assert torch.equal(outs[i], ref), f"thread {i} differs from the sequential call"
+print("TWO_THREADS_OK")
+"""
+
+
+def test_first_calls_from_two_threads(ops):
+    """Two host threads make the process's first ql_cast_gemm_host calls at
+    the same moment, on their own streams and workspaces (a fresh process, so
+    the pipeline's one-time set-up is what they race on). Both results equal
+    the same calls made one after the other, bit for bit."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _TWO_THREADS, root], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "TWO_THREADS_OK" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]

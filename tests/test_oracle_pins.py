@@ -418,6 +418,59 @@ def test_block_cast_equals_torch_restatement(orc):
     assert np.array_equal(s, (amax / 448.0).view(3, 3).numpy())
 
 
+def _torch_per_block(w: torch.Tensor, ue8m0: bool, recip: bool):
+    """Part 4's computation restated in torch CPU ops (own code, not shared)."""
+    m, n = w.shape
+    R, C = -(-m // 128), -(-n // 128)
+    wp = torch.zeros((R * 128, C * 128), dtype=w.dtype)
+    wp[:m, :n] = w
+    v = wp.view(R, 128, C, 128)
+    amax = v.abs().float().amax(dim=(1, 3), keepdim=True).clamp(min=1e-4)
+    scale = amax / 448.0
+    if ue8m0:
+        scale = torch.pow(2.0, torch.ceil(torch.log2(scale)))
+    factor = (torch.ones_like(scale) / scale) if (recip or ue8m0) else (torch.full_like(amax, 448.0) / amax)
+    q = (v * factor).to(torch.float8_e4m3fn).view(R * 128, C * 128)[:m, :n]
+    return q.contiguous().view(torch.uint8).numpy(), scale.view(R, C).numpy()
+
+
+@pytest.mark.parametrize("shape", [(300, 260), (256, 512)])
+@pytest.mark.parametrize("ue8m0,recip", [(False, False), (False, True), (True, False)])
+def test_block_cast_options_equal_torch_restatement(orc, shape, ue8m0, recip):
+    """The block cast's fp32, reciprocal-of-scale and UE8M0 branches against
+    Part 4's formula restated in torch, on randn weights and on fp32 blocks
+    built so that the two readings of the factor give different bytes."""
+    import recip_inputs
+    fmt = orc.SF_UE8M0 if ue8m0 else orc.SF_FP32
+    w = syn.randn(shape, seed=syn.SEED_W, mul=0.02)
+    q, s = orc.cast_per_block(bf16_bits(w), fmt, recip=recip)
+    tq, ts = _torch_per_block(w, ue8m0, recip)
+    assert np.array_equal(q, tq) and np.array_equal(s, ts)
+    ws = recip_inputs.sensitive_blocks(*shape, seed=4)
+    q, s = orc.cast_per_block(ws, fmt, recip=recip)
+    tq, ts = _torch_per_block(torch.from_numpy(ws), ue8m0, recip)
+    assert np.array_equal(q, tq) and np.array_equal(s, ts)
+
+
+def test_recip_branches_differ_where_the_readings_do(orc):
+    """On inputs built for it, the reciprocal-of-scale branch of both casts
+    gives bytes different from the default factor (the pins above would not
+    notice a branch that ignored the option otherwise) while the scales are
+    the same."""
+    import recip_inputs
+    wb = recip_inputs.sensitive_blocks(256, 384, seed=5)
+    q0, s0 = orc.cast_per_block(wb, orc.SF_FP32)
+    q1, s1 = orc.cast_per_block(wb, orc.SF_FP32, recip=True)
+    assert np.array_equal(s0, s1) and not np.array_equal(q0, q1)
+    for gran in (32, 128):
+        xr = recip_inputs.sensitive_rows(6, 520, gran, seed=6)
+        q0, s0 = orc.cast_per_token(xr, gran, orc.SF_FP32)
+        q1, s1 = orc.cast_per_token(xr, gran, orc.SF_FP32, recip=True)
+        assert np.array_equal(s0, s1) and not np.array_equal(q0, q1)
+        tq, ts = _torch_per_token(torch.from_numpy(xr), gran, False, True)
+        assert np.array_equal(q1, tq) and np.array_equal(s1, ts)
+
+
 # ------------------------------------------------------- strided / dtype paths
 def test_cast_transposed_view_equals_copy(orc):
     x = syn.randn_row_exp(300, 256, dtype=torch.bfloat16)

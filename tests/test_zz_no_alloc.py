@@ -16,6 +16,7 @@ from quantised_linear_layers_gb300 import synthetic as syn
 
 pytestmark = pytest.mark.gpu
 
+QL_ERR_INVALID_ARG = 1
 QL_ERR_UNSUPPORTED = 2
 NOALLOC_BYTES = 64 << 20
 
@@ -66,3 +67,21 @@ def test_noalloc_rejects_chunks_beyond_the_array(ops):
     wq = torch.zeros((n, k), dtype=torch.float8_e4m3fn, device="cuda")
     ws = torch.zeros((n // 128, 14), dtype=torch.int32, device="cuda")
     assert call_noalloc(ops, x, wq, ws, fmt, out, 4096) == QL_ERR_UNSUPPORTED
+
+
+def test_noalloc_empty_and_bad_format_as_workspace_call(ops):
+    """Empty shapes return QL_OK and a bad scale format QL_ERR_INVALID_ARG,
+    as the workspace call does, whatever the chunk size."""
+    n, k = 18432, 7168
+    x = torch.zeros((8, k), dtype=torch.bfloat16).pin_memory()
+    out = torch.zeros((8, n), dtype=torch.bfloat16).pin_memory()
+    wq = torch.zeros((n, k), dtype=torch.float8_e4m3fn, device="cuda")
+    ws = torch.zeros((n // 128, 14), dtype=torch.int32, device="cuda")
+    lib = ops.load_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    for m_, n_ in ((0, n), (8, 0)):
+        assert lib.ql_cast_gemm_host_noalloc(x.data_ptr(), k, wq.data_ptr(), k, ws.data_ptr(), 14, 1, 2,
+                                             out.data_ptr(), n, m_, n_, k, 4096, stream) == 0
+    assert call_noalloc(ops, x, wq, ws, 7, out, 4096) == QL_ERR_INVALID_ARG
+    torch.cuda.current_stream().synchronize()
+    assert torch.count_nonzero(out) == 0
