@@ -9,17 +9,25 @@ timed region, as a weight cast runs once per weight update). Inputs are
 synthetic and seeded; they are larger than L2, so no flush is needed.
 
 Prints one JSON line (rank 0). Keys: metric/value/unit (GEMM TFLOP/s of the
-whole step), ms_per_step, roofline (dominant kernel: the GEMM, against the
-dense FP8 peak = 2x the measured bf16 peak), cast (GB/s of the cast kernel
-against measured HBM bandwidth), cast_sweep (the pages' per-token cast
-point: 16384 tokens x 4096, group 32, packed UE8M0), workloads (the smaller
-workloads, timed apart from the step: forward GEMMs at M = 64/128/4096, the
-Linear layer's fwd+dgrad+wgrad step, the low-latency cast at 1-512 tokens
-eager and inside a CUDA graph), e2e (host buffers,
-copies inside the timed region), cpu_baseline (the CPU oracle on a bounded
-sample), clocks (nvidia-smi during the timed region), gpu_launches. e2e runs
-the library's host-buffer call, which overlaps the copies of one row chunk
-with the kernels of the next.
+whole step), ms_per_step, timed_region (the block of K steps is repeated R
+times so the timed region lasts at least --min-timed-s under the clock
+sampler; value and ms_per_step cover all R*K steps), roofline (dominant
+kernel: the GEMM, against the dense FP8 peak = 2x the measured bf16 peak, with
+p10/median/p90 of its launches, a clock-normalised fraction and the ncu
+tensor-pipe counter of its committed capture), cast (GB/s of the cast kernel
+against measured HBM bandwidth), cast_sweep (the pages' per-token cast sweep:
+tokens 1 ... 16384 at hidden 4096, groups 32/128, three scale formats, bf16
+and fp32 input, eager and CUDA-graph, cold L2, plus one hot-L2 point),
+workloads (the smaller configurations, each eager and CUDA-graph with
+median/p10/p90: tiny fwd with fp32 scales, forward GEMMs at M = 64/128/4096
+with packed and fp32 scales, the Linear fwd+dgrad+wgrad step with packed and
+fp32 scales, the fused cast, the grouped GEMM, the low-latency cast, small-M
+GEMMs back to back), e2e (host buffers, copies inside the timed region),
+cpu_baseline (the CPU oracle on a bounded sample of this workload),
+cpu_baselines (the oracle timed in full on the smaller configurations and the
+cast single-threaded and on all cores), clocks (nvidia-smi samples inside the
+timed region), gpu_launches. e2e runs the library's host-buffer call, which
+overlaps the copies of one row chunk with the kernels of the next.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs an independent replica (rows are independent:
@@ -61,7 +69,9 @@ def parse():
                     help="skip the other workloads (small-M GEMMs, Linear step, low-latency cast)")
     ap.add_argument("--only-workloads", action="store_true",
                     help="run only the other workloads and print them as one JSON line")
-    ap.add_argument("--reps", type=int, default=20, help="timed repetitions per other workload")
+    ap.add_argument("--reps", type=int, default=100, help="timed repetitions per other workload")
+    ap.add_argument("--min-timed-s", type=float, default=0.5,
+                    help="the block of K timed steps is repeated until the timed region lasts this long")
     ap.add_argument("--e2e-chunk", type=int, default=1024, help="rows per step of the host-buffer pipeline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-oracle sample time")
     return ap.parse_args()
@@ -78,7 +88,8 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    """nvidia-smi clock / throttle-reason samples, each stamped with the host
+    time it arrived, so that only the samples inside the timed region count."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -87,6 +98,7 @@ class ClockSampler:
         self.gpu_id = gpu_id
         self.proc = None
         self.lines = []
+        self.stamps = []
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20"]
@@ -102,9 +114,12 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
+            self.stamps.append(time.perf_counter())
             self.lines.append(line.strip())
 
-    def stop(self):
+    def stop(self, window=None):
+        """Median SM clock, max clock and active throttle reasons of the
+        samples (those stamped inside `window` = (t0, t1) when given)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -113,9 +128,12 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
+        lines = self.lines
+        if window is not None and len(self.stamps) == len(self.lines):
+            lines = [ln for t, ln in zip(self.stamps, self.lines) if window[0] <= t <= window[1]]
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -181,7 +199,77 @@ def max_over_ranks(world, v: float) -> float:
     return float(t.item())
 
 
+# ------------------------------------------------------------------ timing helpers
+def stats_us(ts_ms):
+    """Median, p10 and p90 (us) of per-repetition times given in ms."""
+    xs = sorted(ts_ms)
+    n = len(xs)
+
+    def q(f):
+        return xs[min(n - 1, max(0, int(round(f * (n - 1)))))]
+
+    return {"us": round(statistics.median(xs) * 1e3, 2), "p10": round(q(0.1) * 1e3, 2),
+            "p90": round(q(0.9) * 1e3, 2), "n": n}
+
+
+def time_eager(fn, reps, flush=None, warm=10):
+    """Per-repetition device times (ms) of fn with CUDA events on the current
+    stream, the L2 flushed (a 256 MB write, outside the events) before each."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return ts
+
+
+def capture(fn, per):
+    """A CUDA graph of `per` back-to-back calls of fn."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(per):
+                fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(fn, reps, flush=None, per=1):
+    """Per-call device times (ms) of fn replayed from a CUDA graph of `per`
+    calls: each repetition flushes L2 (outside the events) and times one
+    replay, divided by `per`."""
+    g = capture(fn, per)
+    return [t / per for t in time_eager(g.replay, reps, flush, warm=3)]
+
+
+def eager_and_graph(fn, reps, flush):
+    """Both timings of one workload, L2 flushed before each repetition."""
+    return {"eager_cold_l2": stats_us(time_eager(fn, reps, flush)),
+            "graph_cold_l2": stats_us(time_graph(fn, reps, flush))}
+
+
 # ------------------------------------------------------------------ CPU oracle
+def _bits(t):
+    import numpy as np
+    import torch
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
 class CpuOracleSample:
     """The CPU oracle on a bounded sample of the workload: the per-token cast
     of a slice of X's rows and the fp64 GEMM of those rows against all of W.
@@ -189,9 +277,6 @@ class CpuOracleSample:
     as on the GPU."""
 
     def __init__(self, n, k, fmt_code):
-        import numpy as np
-        import torch
-
         import oracle
         from quantised_linear_layers_gb300 import synthetic as syn
 
@@ -201,10 +286,10 @@ class CpuOracleSample:
         self.fmt = oracle.SF_FP32 if fmt_code == 0 else oracle.SF_UE8M0
         self.threads = oracle.num_threads()
         w = syn.randn((n, k), seed=syn.SEED_W, mul=0.02)
-        self.wq, self.ws = oracle.cast_per_block(w.view(torch.int16).numpy().view(np.uint16), self.fmt)
+        self.wq, self.ws = oracle.cast_per_block(_bits(w), self.fmt)
         self.rows = max(self.threads, 8)
         x = syn.randn((self.rows, k), seed=syn.SEED_X)
-        self.xb = x.view(torch.int16).numpy().view(np.uint16)
+        self.xb = _bits(x)
 
     def once(self) -> float:
         t0 = time.perf_counter()
@@ -221,6 +306,93 @@ class CpuOracleSample:
             reps += 1
         rows = self.rows * reps
         return 2.0 * rows * self.n * self.k / total / 1e12, total, rows
+
+
+def cpu_baselines():
+    """The CPU oracle timed in full on the smaller configurations, on this
+    host's cores (OpenMP, all cores unless stated):
+
+    - tiny forward, LHS [128, 512], RHS [256, 512], fp32 scales: both casts and
+      the GEMM;
+    - forward GEMMs X [M, 7168] x W [4096, 7168]^T at M = 64, 128, 4096
+      (operands cast before timing);
+    - the Linear step X [4096, 7168], dY [4096, 4096], W [4096, 7168]: the
+      three GEMMs (fwd, dgrad against W^T's block cast, fp32 wgrad with
+      K = tokens), operands cast before timing;
+    - the per-token cast, hidden 4096, group 32, packed UE8M0 (the pages'
+      cast point) at 1 ... 16384 tokens (16384 timed on 4096 rows and scaled),
+      single-threaded and on all cores."""
+    import oracle
+    from quantised_linear_layers_gb300 import synthetic as syn
+
+    oracle.build()
+    o = oracle
+    cores = o.num_threads()
+    out = {"cores": cores, "kind": "oracle"}
+
+    def timed(f):
+        t0 = time.perf_counter()
+        r = f()
+        return time.perf_counter() - t0, r
+
+    # tiny forward, fp32 scales
+    x = _bits(syn.randn((128, 512), seed=syn.SEED_X))
+    w = _bits(syn.randn((256, 512), seed=syn.SEED_W))
+
+    def tiny():
+        xq, xs = o.cast_per_token(x, 128, o.SF_FP32)
+        wq, ws = o.cast_per_block(w, o.SF_FP32)
+        return o.gemm(xq, xs, wq, ws, o.SF_FP32, out="bf16")
+
+    t, _ = timed(tiny)
+    out["tiny_fwd_128x256x512_fp32"] = {"s": round(t, 4), "tflops": round(2 * 128 * 256 * 512 / t / 1e12, 6)}
+
+    # forward GEMMs, hidden 7168
+    wf = _bits(syn.randn((4096, 7168), seed=syn.SEED_W, mul=0.02))
+    wq, ws = o.cast_per_block(wf, o.SF_UE8M0)
+    rows = []
+    for m in (64, 128, 4096):
+        xq, xs = o.cast_per_token(_bits(syn.randn((m, 7168), seed=syn.SEED_X)), 128, o.SF_UE8M0)
+        t, _ = timed(lambda: o.gemm(xq, xs, wq, ws, o.SF_UE8M0, out="bf16"))
+        rows.append({"m": m, "s": round(t, 3), "tflops": round(2 * m * 4096 * 7168 / t / 1e12, 4)})
+    out["gemm_fwd_n4096_k7168"] = rows
+
+    # the Linear step's three GEMMs
+    xl = syn.randn((4096, 7168), seed=syn.SEED_X)
+    dy = syn.randn((4096, 4096), seed=syn.SEED_DY)
+    xq, xs = o.cast_per_token(_bits(xl), 128, o.SF_UE8M0)
+    dq, ds = o.cast_per_token(_bits(dy), 128, o.SF_UE8M0)
+    wtq, wts = o.cast_per_block(np_t(wf), o.SF_UE8M0)
+    dtq, dts = o.cast_per_token(np_t(_bits(dy)), 128, o.SF_UE8M0)
+    xtq, xts = o.cast_per_token(np_t(_bits(xl)), 128, o.SF_UE8M0)
+    t_f, _ = timed(lambda: o.gemm(xq, xs, wq, ws, o.SF_UE8M0, out="bf16"))
+    t_d, _ = timed(lambda: o.gemm(dq, ds, wtq, wts, o.SF_UE8M0, out="bf16"))
+    t_w, _ = timed(lambda: o.gemm(dtq, dts, xtq, xts, o.SF_UE8M0, b_per_row=True, out="f32"))
+    fl = 2 * 4096 * 4096 * 7168
+    out["linear_step_4096x4096x7168"] = {"s_fwd": round(t_f, 2), "s_dgrad": round(t_d, 2), "s_wgrad": round(t_w, 2),
+                                         "tflops": round(3 * fl / (t_f + t_d + t_w) / 1e12, 4)}
+
+    # the per-token cast at the pages' point, single-threaded and all cores
+    rows = []
+    for tok in (1, 64, 512, 4096, 16384):
+        r = min(tok, 4096)
+        xc = _bits(syn.randn_row_exp(r, 4096))
+        byts = r * 4096 * 3 + r * 32 * 4
+        ent = {"tokens": tok, "rows_timed": r}
+        for th, key in ((1, "single"), (cores, "all")):
+            o.set_num_threads(th)
+            t, _ = timed(lambda: o.cast_per_token(xc, 32, o.SF_PACKED_UE8M0))
+            ent[f"us_{key}"] = round(t * 1e6 * tok / r, 1)
+            ent[f"gbs_{key}"] = round(byts / t / 1e9, 3)
+        o.set_num_threads(cores)
+        rows.append(ent)
+    out["cast_h4096_g32_packed"] = rows
+    return out
+
+
+def np_t(a):
+    """Transposed numpy view (the oracle reads strided inputs)."""
+    return a.T
 
 
 # ------------------------------------------------------------------ our arm
@@ -259,79 +431,62 @@ def run_ours(args, world, rank, local):
         ops.fp8_cast_per_token(x, 128, fmt, out=xq, out_sf=xs)
         ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt, out=d)
 
+    t0 = time.perf_counter()
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
+    warm_s = (time.perf_counter() - t0) / max(args.warmup, 3)
     assert ops.device_status() == 0
 
+    # The K steps are timed as a block; the block is repeated R times so that
+    # the timed region lasts at least --min-timed-s under the clock sampler.
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    R = max(1, int(-(-args.min_timed_s // max(warm_s * K, 1e-6))))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K * R)]
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_id = None
     sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.5)
-    for i in range(K):
+    t_host0 = time.perf_counter()
+    for i in range(K * R):
         ev[i][0].record()
         ops.fp8_cast_per_token(x, 128, fmt, out=xq, out_sf=xs)
         ev[i][1].record()
         ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt, out=d)
         ev[i][2].record()
     torch.cuda.synchronize()
+    t_host1 = time.perf_counter()
     barrier(world)
-    clocks = sampler.stop()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    cast_ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
-    gemm_ms = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(K)) / K
+    clocks = sampler.stop(window=(t_host0, t_host1))
+    if clocks is not None:
+        clocks["window_ms"] = round((t_host1 - t_host0) * 1e3, 1)
+    steps_timed = K * R
+    total_ms = ev[0][0].elapsed_time(ev[steps_timed - 1][2])
+    cast_ts = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps_timed)]
+    gemm_ts = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps_timed)]
+    cast_ms = sum(cast_ts) / steps_timed
+    gemm_ms = sum(gemm_ts) / steps_timed
     assert ops.device_status() == 0
     total_ms = max_over_ranks(world, total_ms)
-    ms_step = total_ms / K
+    ms_step = total_ms / steps_timed
     flops_step = 2.0 * m * n * k
-    value = flops_step * world * K / (total_ms / 1e3) / 1e12
+    value = flops_step * world * steps_timed / (total_ms / 1e3) / 1e12
 
     sf_bytes = m * ops.sf_shape(k, 128, fmt) * 4
     cast_bytes = m * k * 2 + m * k + sf_bytes
     gemm_tflops = flops_step / (gemm_ms / 1e3) / 1e12
     cast_gbs = cast_bytes / (cast_ms / 1e3) / 1e9
+    del xq, xs, d
 
-    # the pages' per-token cast point: 16384 x 4096 bf16, group 32, packed UE8M0
     sweep = None
     if not args.no_sweep:
-        xs_in = syn.randn_row_exp(16384, 4096, device=str(dev))
-        sq = torch.empty((16384, 4096), dtype=torch.float8_e4m3fn, device=dev)
-        ssf = ops.empty_sf(16384, ops.sf_shape(4096, 32, 2), 2, dev)
-        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-        for _ in range(5):
-            ops.fp8_cast_per_token(xs_in, 32, 2, out=sq, out_sf=ssf)
-        times_cold, times_hot = [], []
-        for _ in range(20):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            ops.fp8_cast_per_token(xs_in, 32, 2, out=sq, out_sf=ssf)
-            b.record()
-            torch.cuda.synchronize()
-            times_cold.append(a.elapsed_time(b))
-        for _ in range(20):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            ops.fp8_cast_per_token(xs_in, 32, 2, out=sq, out_sf=ssf)
-            b.record()
-            torch.cuda.synchronize()
-            times_hot.append(a.elapsed_time(b))
-        sb = 16384 * 4096 * 2 + 16384 * 4096 + 16384 * 32 * 4
-        tc = statistics.median(times_cold)
-        th = statistics.median(times_hot)
-        sweep = {"shape": [16384, 4096], "gran": 32, "scales": "packed_ue8m0", "bytes": sb,
-                 "us_cold_l2": round(tc * 1e3, 2), "gbs_cold_l2": round(sb / (tc / 1e3) / 1e9, 1),
-                 "frac_hbm_cold": round(sb / (tc / 1e3) / 1e9 / pk["hbm_gbs"], 3),
-                 "us_hot_l2": round(th * 1e3, 2), "pages_b200_eager_us": 38.7}
-        del xs_in, sq, ssf, flush
+        sweep = run_cast_sweep(dev, pk, args.reps)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -361,32 +516,38 @@ def run_ours(args, world, rank, local):
                "h2d_bytes_per_step": m * k * 2, "d2h_bytes_per_step": m * n * 2, "steps": ke,
                "call": "ql_cast_gemm_host", "chunk_rows": chunk,
                "ms_per_step": round(te / ke * 1e3, 3)}
-        del wsp
+        del wsp, xh, dh
+    del x, wq, ws
 
     workloads = None
     if not args.no_workloads:
-        del x, xq, xs, d
         workloads, _ = run_workloads(dev, pk, args.reps)
 
-    cpu = None
+    cpu, cpu_more = None, None
     if rank == 0 and world == 1 and not args.no_cpu:
         sample = CpuOracleSample(n, k, fmt)
         v, secs, rows = sample.run(args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": sample.threads, "kind": "oracle",
                "sample": f"{rows} rows of X: per-token cast + fp64 GEMM against all {n} rows of W "
                          f"(k={k}), {secs:.1f} s; W's block cast done before timing"}
+        del sample
+        cpu_more = cpu_baselines()
 
-    pair = fmt != ops.SF_FP32 and ((m + 255) // 256) * ((n + 255) // 256) >= ops.get_num_sms() // 2
+    pair = fmt != ops.SF_FP32 and ((m + 255) // 256) * ((n + 223) // 224) >= ops.get_num_sms() // 2
     kernel = "gemm_mx2_kernel" if pair else ("gemm_mx_kernel" if fmt != ops.SF_FP32 else "gemm_fp8_kernel")
     traffic, traffic_workload = recorded_traffic(kernel)
     if traffic_workload is not None and traffic_workload != [m, n, k]:
         traffic = None
+    sm_mhz = clocks["sm_mhz"] if clocks else None
+    nominal_per_clk = 16384.0 * ops.get_num_sms()     # dense FP8 flop per SM clock x SMs
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic (seeded randn; W randn*0.02)",
+            "timed_region": {"repeats_of_k_steps": R, "steps_timed": steps_timed,
+                             "ms": round(total_ms, 2), "why": f"timed region >= {args.min_timed_s} s under the clock sampler"},
             "config": {"workload": WORKLOAD, "m": m, "n": n, "k": k, "x_dtype": "bf16", "out_dtype": "bf16",
                        "gran_k": 128, "scales": args.fmt, "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
@@ -394,60 +555,112 @@ def run_ours(args, world, rank, local):
                          "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                          "frac": round(gemm_tflops / fp8_peak, 4), "traffic": traffic,
                          "kernel": kernel, "peak_note": f"dense FP8 = 2 x {pk['source']} bf16 burst",
-                         "frac_of_sustained": round(gemm_tflops / fp8_peak_sus, 4) if fp8_peak_sus else None},
+                         "frac_of_sustained": round(gemm_tflops / fp8_peak_sus, 4) if fp8_peak_sus else None,
+                         "gemm_ms": {"p10": round(sorted(gemm_ts)[len(gemm_ts) // 10], 4),
+                                     "median": round(statistics.median(gemm_ts), 4),
+                                     "p90": round(sorted(gemm_ts)[(9 * len(gemm_ts)) // 10], 4)},
+                         "clock_normalised": (
+                             {"sm_mhz": sm_mhz,
+                              "peak_at_clock_tflops": round(nominal_per_clk * sm_mhz * 1e6 / 1e12, 1),
+                              "frac": round(gemm_tflops * 1e12 / (nominal_per_clk * sm_mhz * 1e6), 4),
+                              "note": "achieved / (16384 dense FP8 flop per SM clock x SMs x median SM clock "
+                                      "in the timed region)"} if sm_mhz else None),
+                         "tensor_pipe": TENSOR_PIPE},
             "gemm": {"ms": round(gemm_ms, 4), "tflops": round(gemm_tflops, 1)},
             "cast": {"ms": round(cast_ms, 4), "bytes": cast_bytes, "gbs": round(cast_gbs, 1),
-                     "frac_hbm": round(cast_gbs / pk["hbm_gbs"], 4), "peak_gbs": pk["hbm_gbs"]},
+                     "frac_hbm": round(cast_gbs / pk["hbm_gbs"], 4), "peak_gbs": pk["hbm_gbs"],
+                     "us": stats_us(cast_ts)},
             "cast_sweep": sweep,
             "workloads": workloads,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "cpu_baselines": cpu_more,
             "clocks": clocks,
-            "gpu_launches": 2 * K,
+            "gpu_launches": 2 * steps_timed,
         }
         print(json.dumps(line), flush=True)
 
 
-# ------------------------------------------------------------------ other workloads
-def _median_ms(fn, reps, flush=None, warm=3):
+# ncu counters of the headline GEMM launch (16384 x 18432 x 7168, packed
+# UE8M0), from the committed capture summarised in profiles/.
+TENSOR_PIPE = None
+
+
+# ------------------------------------------------------------------ cast sweep
+def run_cast_sweep(dev, pk, reps):
+    """The per-token cast sweep of the pages' results table: hidden 4096,
+    tokens 1 / 64 / 512 / 4096 / 16384, group 32 and 128, fp32 / UE8M0 /
+    packed-UE8M0 scales, bf16 and fp32 input (randn x 10^U(-3,3) per row).
+    Each point: eager with L2 flushed before each repetition, and per cast
+    inside a CUDA graph of back-to-back casts (L2 flushed before each replay),
+    as GB/s of algorithmic bytes and as a fraction of measured HBM bandwidth.
+    Plus one hot-L2 point: 4096 tokens, group 32, packed (input and output,
+    50.9 MB, stay resident in the 129 MB L2 between repetitions)."""
     import torch
-    for _ in range(warm):
-        fn()
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(reps):
-        if flush is not None:
-            flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
-    return statistics.median(ts)
+
+    from quantised_linear_layers_gb300 import ops
+    from quantised_linear_layers_gb300 import synthetic as syn
+
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    points = []
+    for dt in (torch.bfloat16, torch.float32):
+        for tok in (1, 64, 512, 4096, 16384):
+            xin = syn.randn_row_exp(tok, 4096, dtype=dt, device=str(dev))
+            for gran in (32, 128):
+                for fmt in (ops.SF_FP32, ops.SF_UE8M0, ops.SF_PACKED_UE8M0):
+                    q = torch.empty((tok, 4096), dtype=torch.float8_e4m3fn, device=dev)
+                    sf = ops.empty_sf(tok, ops.sf_shape(4096, gran, fmt), fmt, dev)
+                    f = lambda: ops.fp8_cast_per_token(xin, gran, fmt, out=q, out_sf=sf)
+                    byts = tok * 4096 * (xin.element_size() + 1) + sf.numel() * 4
+                    te = stats_us(time_eager(f, reps, flush))
+                    per = 20 if tok <= 512 else 4
+                    tg = stats_us(time_graph(f, max(10, reps // 4), flush, per=per))
+                    points.append({
+                        "tokens": tok, "x": "bf16" if dt == torch.bfloat16 else "f32", "gran": gran,
+                        "scales": ("fp32", "ue8m0", "packed")[fmt], "bytes": byts,
+                        "eager_cold_l2": te, "gbs": round(byts / te["us"] / 1e3, 1),
+                        "frac_hbm": round(byts / te["us"] / 1e3 / pk["hbm_gbs"], 3),
+                        "graph_per_cast": tg, "graph_casts": per})
+            del xin
+    # hot L2
+    xin = syn.randn_row_exp(4096, 4096, device=str(dev))
+    q = torch.empty((4096, 4096), dtype=torch.float8_e4m3fn, device=dev)
+    sf = ops.empty_sf(4096, ops.sf_shape(4096, 32, 2), 2, dev)
+    hot = stats_us(time_eager(lambda: ops.fp8_cast_per_token(xin, 32, 2, out=q, out_sf=sf), reps))
+    byts = 4096 * 4096 * 3 + 4096 * 32 * 4
+    return {"hidden": 4096, "l2": "flushed (256 MB write) before each repetition", "points": points,
+            "hot_l2_4096_tokens_g32_packed": {"what": "input and output (50.9 MB) resident in L2", **hot,
+                                               "gbs": round(byts / hot["us"] / 1e3, 1)},
+            "pages_b200_us": {"1": [6.4, 1.2], "64": [6.3, 1.5], "512": [8.2, 2.0], "4096": [15.5, 6.3],
+                              "16384": [38.7, 31.4], "note": "[Triton eager, Triton in a CUDA graph], "
+                                                             "bf16, group 32, packed, on B200"}}
 
 
+# ------------------------------------------------------------------ other workloads
 def run_workloads(dev, pk, reps):
     """The smaller workloads of the method's pages, each timed with CUDA events
-    (median of `reps`):
+    (median, p10, p90 of `reps`, the L2 flushed before each repetition unless
+    stated), eagerly and replayed from a CUDA graph:
 
+    - tiny forward (LHS [128, 512], RHS [256, 512], fp32 scales): per-token
+      cast, block cast and GEMM;
     - forward GEMM N=4096, K=7168 at M = 64, 128 (HBM-bound: W's bytes
-      dominate) and 4096 (tensor-bound), L2 flushed before each repetition,
-      and at M = 64, 128 as 32 GEMMs back to back over 8 distinct weights;
-    - the Linear layer's step, X [4096, 7168], dY [4096, 4096], W [4096, 7168]:
-      weight cast (W's 128x128 block cast, which also writes W^T's scale
-      grid), forward (X cast along features and tokens in one pass + GEMM),
-      backward (dY cast both ways in one pass + dgrad GEMM reading W's cast
-      MN-major + fp32 wgrad GEMM on the token-axis casts),
-      L2 flushed before each step; and its weight gradient with the operands
-      cast from transposed views against cast in place and read MN-major;
+      dominate) and 4096 (tensor-bound), with packed UE8M0 and with fp32
+      scales, and at M = 64, 128 as 32 GEMMs back to back over 8 distinct
+      weights;
+    - the Linear layer's step, X [4096, 7168], dY [4096, 4096], W [4096, 7168]
+      with packed UE8M0 and with fp32 scales: weight cast (W's 128x128 block
+      cast, which also writes W^T's scale grid), forward (X cast along
+      features and tokens in one pass + GEMM), backward (dY cast both ways in
+      one pass + dgrad GEMM reading W's cast MN-major + fp32 wgrad GEMM on the
+      token-axis casts); and its weight gradient with the operands cast from
+      transposed views against cast in place and read MN-major;
     - the low-latency per-token cast (hidden 4096, group 32, packed UE8M0) at
-      1, 64 and 512 tokens: eager with a flushed L2, and the device time per
-      cast inside a captured CUDA graph of 50 casts;
+      1, 64 and 512 tokens per cast inside a captured CUDA graph of 50 casts;
     - a GEMM whose output feeds the next FP8 layer: bf16 output plus the
       per-token cast, against the cast fused into the GEMM's epilogue;
     - the M-grouped contiguous GEMM of a mixture-of-experts layer: 8 experts
-      of about 2048 tokens each, N=4096, K=7168, L2 flushed.
+      of about 2048 tokens each, N=4096, K=7168.
     Returns (dict, number of this library's kernel launches timed).
     """
     import torch
@@ -455,62 +668,84 @@ def run_workloads(dev, pk, reps):
     from quantised_linear_layers_gb300 import linear, ops
     from quantised_linear_layers_gb300 import synthetic as syn
 
-    P = ops.SF_PACKED_UE8M0
+    P, F = ops.SF_PACKED_UE8M0, ops.SF_FP32
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     out, launches = {}, 0
 
+    # tiny forward with fp32 scales
+    xt = syn.randn((128, 512), seed=syn.SEED_X, device=str(dev))
+    wt = syn.randn((256, 512), seed=syn.SEED_W, device=str(dev))
+    txq = torch.empty((128, 512), dtype=torch.float8_e4m3fn, device=dev)
+    txs = ops.empty_sf(128, 4, F, dev, mn_major=True)
+    twq = torch.empty((256, 512), dtype=torch.float8_e4m3fn, device=dev)
+    tws = torch.empty((2, 4), dtype=torch.float32, device=dev)
+    td = torch.empty((128, 256), dtype=torch.bfloat16, device=dev)
+
+    def tiny():
+        ops.fp8_cast_per_token(xt, 128, F, out=txq, out_sf=txs)
+        ops.fp8_cast_per_block(wt, F, out=twq, out_sf=tws)
+        ops.gemm_fp8_nt_bf16(txq, txs, twq, tws, F, out=td)
+
+    r = eager_and_graph(tiny, reps, flush)
+    r["gemm_alone"] = eager_and_graph(lambda: ops.gemm_fp8_nt_bf16(txq, txs, twq, tws, F, out=td), reps, flush)
+    r["flop"] = 2 * 128 * 256 * 512
+    out["tiny_fwd_128x256x512_fp32"] = r
+    launches += 2 * reps * 5
+
     w = syn.randn((4096, 7168), seed=syn.SEED_W, mul=0.02, device=str(dev))
-    wq, ws = ops.fp8_cast_per_block(w, P)
     rows = []
-    for m in (64, 128, 4096):
-        x = syn.randn((m, 7168), seed=syn.SEED_X, device=str(dev))
-        xq, xs = ops.fp8_cast_per_token(x, 128, P, sf_mn_major=True)
-        d = torch.empty((m, 4096), dtype=torch.bfloat16, device=dev)
-        ms = _median_ms(lambda: ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, P, out=d), reps, flush)
-        launches += reps
-        byts = m * 7168 + 4096 * 7168 + m * 4096 * 2 + 4 * (m + 4096 // 128) * (7168 // 512)
-        fl = 2 * m * 4096 * 7168
-        rows.append({"m": m, "n": 4096, "k": 7168, "us": round(ms * 1e3, 2),
-                     "tflops": round(fl / ms / 1e9, 1), "gbs": round(byts / ms / 1e6, 1),
-                     "frac_hbm": round(byts / ms / 1e6 / pk["hbm_gbs"], 3)})
+    for fmt in (P, F):
+        wq, ws = ops.fp8_cast_per_block(w, fmt)
+        for m in (64, 128, 4096):
+            x = syn.randn((m, 7168), seed=syn.SEED_X, device=str(dev))
+            xq, xs = ops.fp8_cast_per_token(x, 128, fmt, sf_mn_major=True)
+            d = torch.empty((m, 4096), dtype=torch.bfloat16, device=dev)
+            r = eager_and_graph(lambda: ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt, out=d), reps, flush)
+            launches += 2 * reps
+            sfb = 4 * (m + 4096 // 128) * ((7168 // 512) if fmt == P else (7168 // 128))
+            byts = m * 7168 + 4096 * 7168 + m * 4096 * 2 + sfb
+            fl = 2 * m * 4096 * 7168
+            us = r["eager_cold_l2"]["us"]
+            rows.append({"m": m, "n": 4096, "k": 7168, "scales": ("fp32", "ue8m0", "packed")[fmt], **r,
+                         "tflops": round(fl / us / 1e6, 1), "gbs": round(byts / us / 1e3, 1),
+                         "frac_hbm": round(byts / us / 1e3 / pk["hbm_gbs"], 3)})
+        del wq, ws
     out["gemm_fwd_n4096_k7168_cold_l2"] = rows
-
-
 
     x = syn.randn((4096, 7168), seed=syn.SEED_X, device=str(dev))
     dy = syn.randn((4096, 4096), seed=syn.SEED_DY, device=str(dev))
-    w8 = linear.FP8Weight(w, P)
-    torch.cuda.synchronize()
-    ev = []
-    for i in range(3 + reps):
-        flush.zero_()
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        e[0].record()
-        w8.update(w)
-        e[1].record()
-        _, xc = linear.forward_saving(x, w8)
-        e[2].record()
-        linear.backward(dy, w8, xc)
-        e[3].record()
-        if i >= 3:
-            ev.append(e)
-            launches += 6
-    torch.cuda.synchronize()
-    part = [statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(3)]
-    step = statistics.median(e[0].elapsed_time(e[3]) for e in ev)
     fl = 2 * 4096 * 4096 * 7168
-    out["linear_step_4096x4096x7168_cold_l2"] = {
-        "us_weight_casts": round(part[0] * 1e3, 1), "us_fwd": round(part[1] * 1e3, 1),
-        "us_bwd": round(part[2] * 1e3, 1),
-        "us_step": round(step * 1e3, 1), "tflops_step": round(3 * fl / step / 1e9, 1),
-        "tflops_without_weight_casts": round(3 * fl / (step - part[0]) / 1e9, 1)}
+    for fmt, key in ((P, "linear_step_4096x4096x7168_cold_l2"), (F, "linear_step_4096x4096x7168_fp32_cold_l2")):
+        w8 = linear.FP8Weight(w, fmt)
+        torch.cuda.synchronize()
+        ev = []
+        for i in range(10 + reps):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record()
+            w8.update(w)
+            e[1].record()
+            _, xc = linear.forward_saving(x, w8)
+            e[2].record()
+            linear.backward(dy, w8, xc)
+            e[3].record()
+            if i >= 10:
+                ev.append(e)
+                launches += 6
+        torch.cuda.synchronize()
+        part = [stats_us([e[j].elapsed_time(e[j + 1]) for e in ev]) for j in range(3)]
+        step = stats_us([e[0].elapsed_time(e[3]) for e in ev])
+        out[key] = {
+            "weight_casts": part[0], "fwd": part[1], "bwd": part[2], "step": step,
+            "tflops_step": round(3 * fl / step["us"] / 1e6, 1),
+            "tflops_without_weight_casts": round(3 * fl / (step["us"] - part[0]["us"]) / 1e6, 1)}
+        del w8
     # the weight gradient with transposed casts against MN-major operands
-    t_tr = _median_ms(lambda: linear.wgrad(dy, x, P, mn_major=False), reps, flush)
-    t_mn = _median_ms(lambda: linear.wgrad(dy, x, P, mn_major=True), reps, flush)
+    t_tr = stats_us(time_eager(lambda: linear.wgrad(dy, x, P, mn_major=False), reps, flush))
+    t_mn = stats_us(time_eager(lambda: linear.wgrad(dy, x, P, mn_major=True), reps, flush))
     launches += 6 * reps
-    out["wgrad_transposed_vs_mn_major_4096x7168x4096"] = {
-        "us_transposed_casts": round(t_tr * 1e3, 1), "us_mn_major": round(t_mn * 1e3, 1)}
-    del x, dy, w8, w, wq, ws
+    out["wgrad_transposed_vs_mn_major_4096x7168x4096"] = {"transposed_casts": t_tr, "mn_major": t_mn}
+    del x, dy, w
 
     # GEMM whose output feeds the next FP8 layer: bf16 output then the
     # per-token cast, against the cast fused into the GEMM's epilogue
@@ -531,13 +766,13 @@ def run_workloads(dev, pk, reps):
     def fused():
         ops.gemm_fp8_nt_fp8out(xaq, xas, wbq, wbs, P, 128, P, out=yq, out_sf=ys)
 
-    t_un = _median_ms(unfused, reps, flush)
-    t_fu = _median_ms(fused, reps, flush)
+    t_un = stats_us(time_eager(unfused, reps, flush))
+    t_fu = stats_us(time_eager(fused, reps, flush))
     launches += 3 * reps
     fl = 2 * 4096 * 7168 * 4096
     out["gemm_cast_fused_4096x7168x4096_cold_l2"] = {
-        "us_gemm_bf16_then_cast": round(t_un * 1e3, 1), "us_fused": round(t_fu * 1e3, 1),
-        "tflops_unfused": round(fl / t_un / 1e9, 1), "tflops_fused": round(fl / t_fu / 1e9, 1),
+        "gemm_bf16_then_cast": t_un, "fused": t_fu,
+        "tflops_unfused": round(fl / t_un["us"] / 1e6, 1), "tflops_fused": round(fl / t_fu["us"] / 1e6, 1),
         "hbm_bytes_saved": 4096 * 7168 * 2 * 2}
     del xaq, xas, wbq, wbs, y, yq, ys
 
@@ -548,23 +783,9 @@ def run_workloads(dev, pk, reps):
         q = torch.empty((t, 4096), dtype=torch.float8_e4m3fn, device=dev)
         sf = ops.empty_sf(t, ops.sf_shape(4096, 32, P), P, dev)
         f = lambda: ops.fp8_cast_per_token(xt, 32, P, out=q, out_sf=sf)
-        eager = _median_ms(f, reps, flush)
-        launches += reps
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            f()
-            s.synchronize()
-            with torch.cuda.graph(g, stream=s):
-                for _ in range(G):
-                    f()
-        torch.cuda.current_stream().wait_stream(s)
-        per = _median_ms(lambda: g.replay(), reps) / G
+        per = stats_us(time_graph(f, reps, None, per=G))
         launches += reps * G
-        byts = t * 4096 * 3 + t * 32 * 4
-        rows.append({"tokens": t, "bytes": byts, "us_eager_cold_l2": round(eager * 1e3, 2),
-                     "us_per_cast_in_graph": round(per * 1e3, 2)})
+        rows.append({"tokens": t, "bytes": t * 4096 * 3 + t * 32 * 4, "per_cast_in_graph_of_50": per})
     out["cast_low_latency_h4096_g32_packed"] = rows
 
     # M-grouped contiguous GEMM (mixture of experts): 8 experts of about 2048
@@ -583,17 +804,18 @@ def run_workloads(dev, pk, reps):
     del we
     idx = idx.to(dev)
     dg = torch.empty((mg, 4096), dtype=torch.bfloat16, device=dev)
-    ms = _median_ms(lambda: ops.m_grouped_gemm_fp8_nt_bf16_contiguous(xgq, xgs, wg, wgs, idx, P, out=dg),
-                    reps, flush)
+    r = stats_us(time_eager(lambda: ops.m_grouped_gemm_fp8_nt_bf16_contiguous(xgq, xgs, wg, wgs, idx, P, out=dg),
+                            reps, flush))
     launches += reps
     fl = 2 * sum(tokens) * 4096 * 7168
     out["grouped_gemm_8experts_n4096_k7168_cold_l2"] = {
-        "tokens": tokens, "m_aligned": mg, "us": round(ms * 1e3, 1), "tflops_valid_rows": round(fl / ms / 1e9, 1),
-        "tflops_incl_padding": round(2 * mg * 4096 * 7168 / ms / 1e9, 1)}
+        "tokens": tokens, "m_aligned": mg, **r, "tflops_valid_rows": round(fl / r["us"] / 1e6, 1),
+        "tflops_incl_padding": round(2 * mg * 4096 * 7168 / r["us"] / 1e6, 1)}
     del xgq, xgs, wg, wgs, dg
 
     # small M back to back, as in decoding: 32 GEMMs in a row over 8 distinct
-    # weights (8 x 29.4 MB > L2), one event pair around the sequence
+    # weights (8 x 29.4 MB > L2), one event pair around the sequence; eager
+    # launches and the sequence replayed from a CUDA graph
     wcopies = [ops.fp8_cast_per_block(syn.randn((4096, 7168), seed=200 + i, mul=0.02, device=str(dev)), P)
                for i in range(8)]
     rows = []
@@ -607,11 +829,14 @@ def run_workloads(dev, pk, reps):
                 for wq_i, ws_i in wcopies:
                     ops.gemm_fp8_nt_bf16(xq, xs, wq_i, ws_i, P, out=d)
 
-        ms = _median_ms(seq, max(3, reps // 4)) / 32
-        launches += 32 * max(3, reps // 4)
+        n_rep = max(10, reps // 4)
+        te = stats_us([t / 32 for t in time_eager(seq, n_rep)])
+        tg = stats_us([t / 32 for t in time_eager(capture(seq, 1).replay, n_rep)])
+        launches += 64 * n_rep
         byts = m * 7168 + 4096 * 7168 + m * 4096 * 2 + 4 * (m + 4096 // 128) * (7168 // 512)
-        rows.append({"m": m, "us_per_gemm": round(ms * 1e3, 2), "gbs": round(byts / ms / 1e6, 1),
-                     "frac_hbm": round(byts / ms / 1e6 / pk["hbm_gbs"], 3)})
+        rows.append({"m": m, "eager_per_gemm": te, "graph_per_gemm": tg,
+                     "gbs": round(byts / te["us"] / 1e3, 1), "frac_hbm": round(byts / te["us"] / 1e3 / pk["hbm_gbs"], 3),
+                     "frac_hbm_graph": round(byts / tg["us"] / 1e3 / pk["hbm_gbs"], 3)})
     out["gemm_fwd_small_m_back_to_back_8_weights"] = rows
     del wcopies
     assert ops.device_status() == 0
@@ -620,7 +845,9 @@ def run_workloads(dev, pk, reps):
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, world, rank):
-    """The CPU oracle timed on the host cores, on a bounded sample per step."""
+    """The CPU oracle timed on the host cores, on a bounded sample per step:
+    each step casts a slice of X's rows and multiplies it (fp64) against all of
+    W. `ms_per_step` is that sampled step's measured time."""
     if rank != 0:
         return
     m, n, k = args.m, args.n, args.k
@@ -637,11 +864,12 @@ def run_reference(args, world, rank):
         secs += s
         rows_total += rows
     value = statistics.median(vals)
-    # one whole step of the workload at the sampled rate (the GEMM's 2mnk flop)
     ms_full = 2.0 * m * n * k / (value * 1e12) * 1e3 if value > 0 else None
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_full, "ms_per_step_note": "whole step extrapolated from the sample",
+        "warmup": args.warmup, "ms_per_step": round(secs / max(1, args.steps) * 1e3, 1),
+        "ms_per_step_note": "one sampled step (a slice of X's rows against all of W), measured",
+        "ms_full_workload_extrapolated": ms_full,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn; W randn*0.02)",
         "config": {"workload": WORKLOAD, "m": m, "n": n, "k": k, "gran_k": 128, "scales": args.fmt},
