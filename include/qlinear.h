@@ -414,12 +414,15 @@ ql_status ql_set_gemm_block_n(int block_n);
  * CTA pairs (256 x 224 or 256 x 256 tiles over two SMs) when the problem has
  * at least one such tile per pair of SMs; with fewer tiles, split over K
  * across a thread-block cluster when that fills the SMs, else on CTA pairs
- * while there is a tile for every other pair, else on single SMs. 1 forces
- * the CUDA-core promotion path used for fp32 scales; 2 forces the single-SM
- * block-scaled kernel, 3 the CTA-pair kernel and 4 the cluster split-K
- * kernel where it applies (2-4 ignored for QL_SF_FP32). All give results
- * within the GEMM tolerance of each other. Process-wide; for tuning and
- * tests. */
+ * while there is a tile for every other pair, else on single SMs. With
+ * QL_SF_FP32 scales (and with path 1) the partial product of every 128-wide
+ * K block is promoted on the CUDA cores of one SM per tile. 1 forces the
+ * CUDA-core promotion path, 5 runs it on CTA pairs (256 x 256 tiles; plain
+ * GEMMs only, measured no faster than one SM per tile) and 6 forces the
+ * single-SM kernel; 2 forces the single-SM block-scaled kernel,
+ * 3 the block-scaled CTA-pair kernel and 4 the cluster split-K kernel where
+ * it applies (2-4 ignored for QL_SF_FP32). All give results within the GEMM
+ * tolerance of each other. Process-wide; for tuning and tests. */
 ql_status ql_set_gemm_path(int path);
 
 /* Time limit of every bounded wait inside the GEMM kernel, in milliseconds

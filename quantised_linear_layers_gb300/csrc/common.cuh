@@ -175,6 +175,13 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Relaxed form: no memory ordering (a release at cluster scope waits for all
+// of the thread's outstanding memory operations). For signals that publish no
+// memory writes, such as "this warp's tensor-memory loads have completed"
+// (tcgen05.wait::ld has returned, so there is nothing left to order).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 
 // Lowers the barrier's pending transaction count by `bytes` (as if that many
 // bytes had arrived), and raises it.
@@ -380,6 +387,20 @@ __device__ __forceinline__ void mma_mxf8_block_scaled_pair(uint32_t d_tmem, uint
         "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n"
         "}\n" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+// Pair form of mma_e4m3: the leader's one instruction computes the pair's
+// 2*128-row tile; A and B are read from both CTAs' shared memory at the same
+// offsets, D lands in both CTAs' tensor memory (each its own 128 rows).
+__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Copies the 32x128-bit shared-memory matrix at the same offset in each CTA of

@@ -22,8 +22,8 @@
 //               decoded here), several K blocks per memory round trip.
 //   warps 4-11  two math warpgroups: each thread owns one accumulator row and
 //               BN/2 columns in registers; per K block it reads P_kb from TMEM
-//               (tcgen05.ld) and promotes acc += (sa*sb) * P_kb with packed
-//               fp32x2 FMAs; after the last K block it writes bf16 (or fp32,
+//               (tcgen05.ld) and promotes acc += (sa*sb) * P_kb with fp32
+//               FMAs (packed f32x2 when every column has its own scale); after the last K block it writes bf16 (or fp32,
 //               optionally accumulated) output.
 // Tiles are 128 x BN (BN in {256,128,64,32}), visited in grouped raster order
 // (GROUP_M m-blocks share each n-block sweep) for L2 reuse. Every wait is
@@ -43,6 +43,7 @@
 #include "epilogue_fp8.cuh"
 #include "epilogue_tma.cuh"
 #include "gemm.cuh"
+#include "promote.cuh"
 
 namespace ql {
 // ---------------------------------------------------------------------------
@@ -172,49 +173,6 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb,
     const int w = t - group * group_size;
     mb = first_m + w % gm;
     nb = w / gm;
-}
-
-__device__ __forceinline__ float decode_scale(const void* base, int fmt, int64_t row_off, int kb, int64_t sk) {
-    if (fmt != 2) return __ldg(static_cast<const float*>(base) + row_off + kb * sk);
-    const uint32_t w = __ldg(static_cast<const uint32_t*>(base) + row_off + (kb >> 2) * sk);
-    const uint32_t e = (w >> (8 * (kb & 3))) & 0xFFu;
-    return __uint_as_float(e ? (e << 23) : 0x00400000u);   // 2^(e-127)
-}
-
-__device__ __forceinline__ uint64_t pack2(float a, float b) {
-    return static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
-}
-
-// acc2 = p2 * s2 + acc2 on two fp32 lanes at once
-__device__ __forceinline__ void fma2(uint64_t& acc2, uint64_t p2, uint64_t s2) {
-    asm volatile("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(p2), "l"(s2));
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a2, uint64_t b2) {
-    uint64_t r;
-    asm volatile("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a2), "l"(b2));
-    return r;
-}
-
-// Reads N (16, 32 or 64) consecutive fp32 accumulator columns of this warp's
-// 32 TMEM lanes and waits for them.
-template <int N>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&v)[N]) {
-    if constexpr (N == 16) {
-        tmem_ld_32x32b_x16(taddr, v);
-    } else if constexpr (N == 32) {
-        tmem_ld_32x32b_x32(taddr, v);
-    } else {
-        static_assert(N == 64, "16, 32 or 64 columns");
-        tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-    }
-    tmem_wait_ld(v);
-}
-
-// Bounded wait whose outcome is the same for every lane of the warp (the
-// .sync.aligned tensor-memory loads that follow need a converged warp).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl)) != 0;
 }
 
 template <int BN, bool PER_ROW_B, bool OUT_F32, bool OUT_FP8 = false>
@@ -434,9 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 const uint32_t tcol = tmem_base + lane_base + ts * BN + wg * CPT;
                 constexpr int U = CPT < 64 ? CPT : 64;     // columns per TMEM read round
+                // one scale per 128 columns: one fp32 FMA per element (single
+                // rounding); the packed f32x2 form retires the same 32 FMAs
+                // per clock per SMSP and needs the accumulators paired and
+                // unpaired around it (measured: 8192 x 8192 x 7168 439 -> 421 us)
                 if constexpr (!PER_ROW_B) {
                     const float sab = sa * src[BM + ((BN == 256) ? wg : 0)];
-                    const uint64_t s2 = pack2(sab, sab);
 #pragma unroll
                     for (int c0 = 0; c0 < CPT; c0 += U) {
                         uint32_t v[U];
@@ -446,15 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_arrive(&tempty[ts]);
                         }
 #pragma unroll
-                        for (int j = 0; j < U; j += 2) {
-                            uint64_t a2 = pack2(acc[c0 + j], acc[c0 + j + 1]);
-                            fma2(a2, pack2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2);
-                            acc[c0 + j] = __uint_as_float(static_cast<uint32_t>(a2));
-                            acc[c0 + j + 1] = __uint_as_float(static_cast<uint32_t>(a2 >> 32));
-                        }
+                        for (int j = 0; j < U; ++j) acc[c0 + j] = fmaf(__uint_as_float(v[j]), sab, acc[c0 + j]);
                     }
                     mbar_arrive(&sempty[slot]);
                 } else {
+                    // a scale per column: (sa * sb) and the FMA, two elements
+                    // per packed f32x2 instruction (half the instructions of
+                    // the scalar form)
                     const uint64_t sa2 = pack2(sa, sa);
 #pragma unroll
                     for (int c0 = 0; c0 < CPT; c0 += U) {
@@ -641,10 +600,16 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     // tensor core's block-scaled MMA unless the CUDA-core path is requested.
     const bool ue8m0 = L.fmt == 1 || L.fmt == 2;
     const bool grouped = L.m_indices != nullptr;   // the pair kernel's two M halves share one B
+    // CUDA-core promotion (fp32 scales, or forced): on one SM per tile; path 5
+    // runs it on CTA pairs (256 x 256 tiles), which measured no faster (its two
+    // accumulator stages leave the promotion hand-off exposed), 6 forces the
+    // single-SM kernel.
+    const bool promote = !ue8m0 || L.path == 1 || L.path == 5 || L.path == 6;
+    if (promote && !grouped && !L.out_fp8 && L.path == 5) return launch_gemm_pair(L, p, st, num_sms);
     if (L.a_mn || L.b_mn) {
         // MN-major operands: one 128-byte swizzle atom of M / N per CTA, so
         // 128-column tiles on one SM, or the CTA pair (128 columns per CTA)
-        if (ue8m0 && L.path != 1) {
+        if (!promote) {
             const int64_t pair_tiles = ((L.m + 255) / 256) * ((L.n + 255) / 256);
             if (L.path == 3 || (L.path == 0 && pair_tiles >= num_sms / 2)) return launch_gemm_mx2(L, p, st, num_sms);
             return launch_gemm_mx(L, p, 128, st, num_sms);
@@ -655,7 +620,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     if (L.out_fp8) {
         // E4M3 output: 256-wide tiles, so every epilogue thread owns whole
         // 128-column groups of its row (pair, single-SM or promotion kernel)
-        if (ue8m0 && L.path != 1) {
+        if (!promote) {
             const int64_t pair_tiles = ((L.m + 255) / 256) * ((L.n + 255) / 256);
             if (L.path == 3 || (L.path == 0 && pair_tiles >= num_sms / 2)) return launch_gemm_mx2(L, p, st, num_sms);
             return launch_gemm_mx(L, p, 256, st, num_sms);
@@ -678,7 +643,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
         if (split >= 2) return launch_gemm_mx_sk(L, p, split, st);
         if (pair_tiles >= num_sms / 4) return launch_gemm_mx2(L, p, st, num_sms);
     }
-    if (ue8m0 && L.path != 1) return launch_gemm_mx(L, p, bn, st, num_sms);
+    if (!promote) return launch_gemm_mx(L, p, bn, st, num_sms);
     if (L.out_f32) return dispatch_bn<true, true>(bn, L, p, st, num_sms);
     return dispatch_bn<false, false>(bn, L, p, st, num_sms);
 }

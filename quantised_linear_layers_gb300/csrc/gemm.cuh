@@ -62,7 +62,8 @@ struct GemmLaunch {
     int block_n;              // 0 = heuristic, else 32/64/128/256
     int path;                 // 0 = auto, 1 = CUDA-core promotion, 2 = block-scaled MMA on one SM,
                               // 3 = block-scaled MMA on CTA pairs, 4 = split-K over a cluster
-                              // (3 and 4: UE8M0 formats only)
+                              // (3 and 4: UE8M0 formats only), 5 = CUDA-core promotion on
+                              // CTA pairs, 6 = CUDA-core promotion on one SM
     uint32_t* dev_status;
     uint64_t wait_limit_ns;
     int stall_producer;
@@ -147,6 +148,9 @@ int choose_block_n(int64_t m, int64_t n, int num_sms);
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms);
 cudaError_t launch_gemm_mx(const GemmLaunch& L, const GemmParams& p, int bn, cudaStream_t st, int num_sms);
 cudaError_t launch_gemm_mx2(const GemmLaunch& L, const GemmParams& p, cudaStream_t st, int num_sms);
+// CUDA-core promotion (any fp32 scales) on CTA pairs, 256 x 256 tiles; plain
+// GEMMs with bf16 output or fp32 (wgrad) output, K- or MN-major operands.
+cudaError_t launch_gemm_pair(const GemmLaunch& L, const GemmParams& p, cudaStream_t st, int num_sms);
 // Split-K over a thread-block cluster (bf16 output, UE8M0 formats): cluster
 // size for the shape (1 = no split applies) and the launch.
 int choose_split_k(int64_t m, int64_t n, int64_t k, int num_sms);

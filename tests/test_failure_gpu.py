@@ -5,8 +5,8 @@ operand producer issue no copies, so the tensor-core issuer's wait on a barrier
 that nothing will complete runs out: the kernel must record
 QL_ERR_DEVICE_TIMEOUT in the device status word, free its tensor memory and
 return, and the context must stay usable (the next call is correct). Covered
-for the CUDA-core promotion kernel, the single-SM block-scaled kernel, the
-CTA-pair kernel and the split-K cluster kernel.
+for the CUDA-core promotion kernels (single SM and CTA pairs), the single-SM
+block-scaled kernel, the CTA-pair kernel and the split-K cluster kernel.
 """
 import pytest
 import torch
@@ -32,8 +32,8 @@ def ops():
     o.set_gemm_path(0)
 
 
-@pytest.mark.parametrize("path,fmt", [(1, 0), (2, 2), (3, 2), (4, 2)],
-                         ids=["promotion", "block_scaled", "pair", "split_k"])
+@pytest.mark.parametrize("path,fmt", [(1, 0), (5, 0), (2, 2), (3, 2), (4, 2)],
+                         ids=["promotion", "promotion_pair", "block_scaled", "pair", "split_k"])
 def test_bounded_wait_times_out_and_context_survives(orc, ops, path, fmt):
     m, n, k = 512, 512, 1024
     x = syn.randn((m, k), seed=syn.SEED_X).cuda()

@@ -222,7 +222,7 @@ def _pow2_grid(rows, cols, seed, lo=-2, hi=2):
     return torch.pow(2.0, torch.randint(lo, hi + 1, (rows, cols), generator=g).float())
 
 
-@pytest.mark.parametrize("path", [1, 2, 3], ids=["promotion", "block_scaled", "pair"])
+@pytest.mark.parametrize("path", [1, 5, 2, 3], ids=["promotion", "promotion_pair", "block_scaled", "pair"])
 @pytest.mark.parametrize("bn", [32, 64, 128, 256])
 @pytest.mark.parametrize("k", [1024, 1152, 256])
 @pytest.mark.parametrize("packed", [False, True])
@@ -258,7 +258,7 @@ def test_wgrad_exact_pow2_scales(orc, ops, path, bn, k, packed):
     assert bad.size == 0, f"{len(bad)} mismatches; first {bad[0]} got {got[tuple(bad[0])]} ref {ref[tuple(bad[0])]}"
 
 
-@pytest.mark.parametrize("path", [1, 2, 3, 4], ids=["promotion", "block_scaled", "pair", "split_k"])
+@pytest.mark.parametrize("path", [1, 5, 2, 3, 4], ids=["promotion", "promotion_pair", "block_scaled", "pair", "split_k"])
 @pytest.mark.parametrize("bn", [32, 64, 128, 256])
 def test_fwd_exact_pow2_block_scales(orc, ops, path, bn):
     """fwd form: 1x128 A scales and 128x128 B block scales, all powers of two,
@@ -294,7 +294,13 @@ def test_block_scaled_matches_promotion_random(orc, ops, fmt):
         d3 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
     finally:
         ops.set_gemm_path(0)
+    ops.set_gemm_path(5)
+    try:
+        d5 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    finally:
+        ops.set_gemm_path(0)
     ref = oracle_fwd(orc, xq, xs, wq, ws, fmt)
+    check_gemm(d5.float().cpu().numpy(), ref, "promotion on CTA pairs")
     check_gemm(d1.float().cpu().numpy(), ref, "promotion")
     check_gemm(d2.float().cpu().numpy(), ref, "block-scaled")
     check_gemm(d3.float().cpu().numpy(), ref, "pair")
@@ -351,7 +357,7 @@ def test_split_k_cluster(orc, ops, case, fmt):
 @pytest.mark.parametrize("n", [520, 300])
 @pytest.mark.parametrize("offset", [64, 4], ids=["aligned", "unaligned"])
 @pytest.mark.parametrize("out", ["bf16", "f32", "f32_acc"])
-@pytest.mark.parametrize("path", [1, 2, 3], ids=["promotion", "block_scaled", "pair"])
+@pytest.mark.parametrize("path", [1, 5, 2, 3], ids=["promotion", "promotion_pair", "block_scaled", "pair"])
 def test_output_view_leaves_rest_untouched(orc, ops, path, out, offset, n):
     """D written into a view of a taller, wider buffer (row pitch 1024, view at
     column `offset`). The kernels write through TMA tile stores only when the
@@ -395,3 +401,61 @@ def test_output_view_leaves_rest_untouched(orc, ops, path, out, offset, n):
         refo = orc.gemm(np_bytes(aq), np_sf(sa), np_bytes(bq), np_sf(sb), 1, b_per_row=(out != "bf16"),
                         rows=np.array([0, 129, 256, m - 1]), out="bf16" if out == "bf16" else "f32")
         check_gemm(view[[0, 129, 256, m - 1]].double().cpu().numpy(), refo)
+
+
+# ------------------------------------------------- CUDA-core promotion on CTA pairs
+@pytest.mark.parametrize("path", [5, 6], ids=["pair", "single_sm"])
+@pytest.mark.parametrize("shape", [(256, 256, 128), (300, 520, 640), (1, 40, 16), (513, 1000, 1936), (2048, 2304, 1024)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_promotion_fp32_scales_ragged(orc, ops, path, shape):
+    """fp32 scales (any values), ragged M, N and K: partial pair tiles in both
+    directions, a peer CTA with no rows, one-row and one-K-slice problems."""
+    m, n, k = shape
+    x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, 0, w_mul=0.02, seed_x=61, seed_w=62)
+    ops.set_gemm_path(path)
+    try:
+        d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 0)
+    finally:
+        ops.set_gemm_path(0)
+    assert ops.device_status() == 0
+    ref = oracle_fwd(orc, xq, xs, wq, ws, 0)
+    check_gemm(d.float().cpu().numpy(), ref, f"path {path}")
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+@pytest.mark.parametrize("shape", [(300, 520, 640), (1024, 1280, 2048)], ids=lambda s: "x".join(map(str, s)))
+def test_promotion_pair_wgrad_fp32(orc, ops, shape, accumulate):
+    """The weight-gradient form on CTA pairs: per-row fp32 scales on both
+    operands, fp32 output written or added to D (TMA reduce-add)."""
+    m, n, k = shape
+    aq, sa = ops.fp8_cast_per_token(syn.randn((m, k), seed=71).cuda(), 128, 0)
+    bq, sb = ops.fp8_cast_per_token(syn.randn((n, k), seed=72).cuda(), 128, 0)
+    d0 = syn.randn((m, n), seed=73, dtype=torch.float32).cuda()
+    d = d0.clone() if accumulate else torch.empty((m, n), dtype=torch.float32, device="cuda")
+    ops.set_gemm_path(5)
+    try:
+        ops.gemm_fp8_wgrad_fp32(aq, sa, bq, sb, out=d, accumulate=accumulate, fmt=0)
+    finally:
+        ops.set_gemm_path(0)
+    assert ops.device_status() == 0
+    d_in = d0.double().cpu().numpy() if accumulate else None
+    ref = orc.gemm(np_bytes(aq), np_sf(sa), np_bytes(bq), np_sf(sb), 0, b_per_row=True, d_in=d_in, out="f32")
+    check_gemm(d.double().cpu().numpy(), ref, "wgrad on CTA pairs")
+
+
+@pytest.mark.parametrize("path", [0, 5], ids=["default", "promotion_pair"])
+def test_promotion_fp32_large_sampled_rows(orc, ops, path):
+    """X [16384, 7168] x W [18432, 7168]^T with fp32 scales (CUDA-core
+    promotion on one SM per tile by default, on CTA pairs with path 5): two
+    sampled rows in every 256-row M tile, every column."""
+    m, n, k = 16384, 18432, 7168
+    x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, 0, w_mul=0.02)
+    ops.set_gemm_path(path)
+    try:
+        d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 0)
+    finally:
+        ops.set_gemm_path(0)
+    assert ops.device_status() == 0
+    rows = rows_per_tile(m, 9)
+    ref = oracle_fwd(orc, xq, xs, wq, ws, 0, rows=rows)
+    check_gemm(d[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref, "fp32 scales, large")

@@ -41,7 +41,7 @@ def pack_words(s):
     return (e[..., 0] | (e[..., 1] << 8) | (e[..., 2] << 16) | (e[..., 3] << 24)).contiguous()
 
 
-PATHS = [(1, "promotion"), (2, "block_scaled"), (3, "pair")]
+PATHS = [(1, "promotion"), (5, "promotion_pair"), (2, "block_scaled"), (3, "pair")]
 
 
 @pytest.mark.parametrize("path", [p for p, _ in PATHS], ids=[n for _, n in PATHS])
@@ -147,7 +147,7 @@ def test_dgrad_nn_with_w_own_cast(orc, ops, fmt):
     check_gemm(d_nn.float().cpu().numpy(), ref, "dgrad nn")
 
 
-@pytest.mark.parametrize("path", [0, 1, 2, 3], ids=["default", "promotion", "block_scaled", "pair"])
+@pytest.mark.parametrize("path", [0, 1, 5, 2, 3], ids=["default", "promotion", "promotion_pair", "block_scaled", "pair"])
 @pytest.mark.parametrize("fmt", [0, 1, 2], ids=["fp32", "ue8m0", "packed"])
 @pytest.mark.parametrize("shape", [(512, 1024, 768), (300, 640, 520)], ids=["512x1024x768", "ragged"])
 def test_dgrad_from_dual_block_cast(orc, ops, fmt, path, shape):
