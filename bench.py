@@ -150,13 +150,13 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def recorded_traffic(kernel_file: str):
-    """DRAM bytes per launch of the GEMM kernel from the committed ncu record,
-    or None when the kernel source changed since the counters were taken."""
+def recorded_counters(kernel_file: str):
+    """The committed ncu counters of the GEMM kernel's launch (dict), or None
+    when the kernel sources changed since they were taken."""
     import hashlib
     rec = os.path.join(ROOT, "profiles", "gemm_traffic.json")
     if not os.path.exists(rec):
-        return None, None
+        return None
     with open(rec) as fh:
         data = json.load(fh)
     h = hashlib.sha256()
@@ -165,6 +165,16 @@ def recorded_traffic(kernel_file: str):
             h.update(fh.read())
     entry = data.get("kernels", {}).get(kernel_file)
     if not entry or data.get("sources_sha256") != h.hexdigest():
+        return None
+    return entry
+
+
+def recorded_traffic(kernel_file: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu record
+    and the workload they were taken on, or (None, None) when the kernel
+    sources changed since the counters were taken."""
+    entry = recorded_counters(kernel_file)
+    if entry is None:
         return None, None
     return entry.get("dram_bytes_per_launch"), entry.get("workload")
 
@@ -538,6 +548,12 @@ def run_ours(args, world, rank, local):
     traffic, traffic_workload = recorded_traffic(kernel)
     if traffic_workload is not None and traffic_workload != [m, n, k]:
         traffic = None
+    counters = recorded_counters(kernel)
+    tensor_pipe = None
+    if counters is not None and counters.get("workload") == [m, n, k] and "tensor_pipe_active_pct_of_elapsed" in counters:
+        tensor_pipe = {"active_pct_of_elapsed": counters["tensor_pipe_active_pct_of_elapsed"],
+                       "sm_clock_hz_under_ncu": counters.get("sm_clock_hz_under_ncu"),
+                       "source": "profiles/gemm_traffic.json (one ncu capture of this launch)"}
     sm_mhz = clocks["sm_mhz"] if clocks else None
     nominal_per_clk = 16384.0 * ops.get_num_sms()     # dense FP8 flop per SM clock x SMs
     if rank == 0:
@@ -565,7 +581,7 @@ def run_ours(args, world, rank, local):
                               "frac": round(gemm_tflops * 1e12 / (nominal_per_clk * sm_mhz * 1e6), 4),
                               "note": "achieved / (16384 dense FP8 flop per SM clock x SMs x median SM clock "
                                       "in the timed region)"} if sm_mhz else None),
-                         "tensor_pipe": TENSOR_PIPE},
+                         "tensor_pipe": tensor_pipe},
             "gemm": {"ms": round(gemm_ms, 4), "tflops": round(gemm_tflops, 1)},
             "cast": {"ms": round(cast_ms, 4), "bytes": cast_bytes, "gbs": round(cast_gbs, 1),
                      "frac_hbm": round(cast_gbs / pk["hbm_gbs"], 4), "peak_gbs": pk["hbm_gbs"],
@@ -579,11 +595,6 @@ def run_ours(args, world, rank, local):
             "gpu_launches": 2 * steps_timed,
         }
         print(json.dumps(line), flush=True)
-
-
-# ncu counters of the headline GEMM launch (16384 x 18432 x 7168, packed
-# UE8M0), from the committed capture summarised in profiles/.
-TENSOR_PIPE = None
 
 
 # ------------------------------------------------------------------ cast sweep
