@@ -41,7 +41,8 @@ typedef enum {
     QL_ERR_UNSUPPORTED = 2,     /* valid request this build does not implement */
     QL_ERR_ALIGNMENT = 3,       /* pointer / stride alignment the kernel needs is not met */
     QL_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed */
-    QL_ERR_DEVICE_TIMEOUT = 5   /* a kernel's bounded wait ran out (see ql_device_status) */
+    QL_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait ran out (see ql_device_status) */
+    QL_ERR_OUT_OF_BOUNDS = 6    /* bounds-checked builds only: an access outside its buffer was skipped */
 } ql_status;
 
 typedef enum { QL_BF16 = 0, QL_F32 = 1 } ql_dtype;
@@ -439,9 +440,23 @@ ql_status ql_test_stall_gemm_producer(int enable);
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * QL_OK; QL_ERR_DEVICE_TIMEOUT if any kernel's bounded wait ran out since the
- * last call; else QL_ERR_INVALID_ARG if a grouped GEMM met an invalid expert
- * index; QL_ERR_CUDA if the synchronisation itself failed. */
+ * last call; else QL_ERR_OUT_OF_BOUNDS if a bounds-checked build skipped an
+ * access outside its buffer; else QL_ERR_INVALID_ARG if a grouped GEMM met an
+ * invalid expert index; QL_ERR_CUDA if the synchronisation itself failed. */
 ql_status ql_device_status(ql_stream_t stream);
+
+/* ql_device_status, also returning the raw flag bits (1 time-out, 2 invalid
+ * expert index, 4 out-of-bounds access) and the first out-of-bounds address a
+ * bounds-checked build recorded (0 if none); either pointer may be null. */
+ql_status ql_device_status_detail(ql_stream_t stream, uint32_t* flags, uint64_t* first_bad_address);
+
+/* 1 if this library was built with QL_BOUNDS_CHECK: every plain global load
+ * and store of the kernels (TMA copies are clipped by the hardware) is checked
+ * against the byte range of the caller's buffer it belongs to, derived from
+ * the call's pointers, shapes and strides; an access outside it is skipped
+ * and recorded (QL_ERR_OUT_OF_BOUNDS from ql_device_status), never trapped.
+ * A debugging build: slower, same results for in-range programs. 0 otherwise. */
+int ql_bounds_checked(void);
 
 #ifdef __cplusplus
 }

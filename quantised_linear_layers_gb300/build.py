@@ -39,14 +39,19 @@ def _stale(obj: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = "") -> str:
+    """Compile the library; returns its path. `variant` (e.g. "bounds" with
+    extra_flags=("-DQL_BOUNDS_CHECK",)) builds into its own folder and
+    libqlinear_<variant>.so, leaving the product library as it is."""
+    build_dir = BUILD + (f"_{variant}" if variant else "")
+    lib = LIB.replace(".so", f"_{variant}.so") if variant else LIB
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(INCLUDE, "qlinear.h"))
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
             cmd = [nvcc()] + _flags(extra_flags) + ["-c", s, "-o", o]
@@ -64,16 +69,25 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
             if verbose and (r.stdout or r.stderr):
                 print(r.stdout + r.stderr)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".{os.getpid()}.tmp"
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart_static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+def build_bounds_checked(force: bool = False) -> str:
+    """The debugging build with every plain global access range-checked
+    (QL_BOUNDS_CHECK): libqlinear_bounds.so beside the product library."""
+    return build(force=force, extra_flags=("-DQL_BOUNDS_CHECK",), variant="bounds")
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--bounds" in sys.argv:
+        print(build_bounds_checked(force="--force" in sys.argv))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

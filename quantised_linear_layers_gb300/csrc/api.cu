@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "../../include/qlinear.h"
+#include "bounds.cuh"
 #include "cast.cuh"
 #include "gemm.cuh"
 
@@ -15,9 +16,11 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Device status word (time-out flags raised by kernels). One copy per device
-// that loads the library; its address is looked up once per device.
-__device__ uint32_t g_dev_status = 0;
+// Device status words: [0] flags raised by kernels (time-out, invalid grouped
+// index, out-of-bounds access in bounds-checked builds), [2..3] the first
+// out-of-bounds address as a 64-bit word. One copy per device that loads the
+// library; its address is looked up once per device.
+__device__ __align__(16) uint32_t g_dev_status[4] = {0u, 0u, 0u, 0u};
 
 std::atomic<int> g_num_sms_override{0};
 std::atomic<int> g_block_n_override{0};
@@ -231,6 +234,7 @@ const char* ql_status_string(ql_status s) {
         case QL_ERR_ALIGNMENT: return "QL_ERR_ALIGNMENT: pointer or stride alignment not met";
         case QL_ERR_CUDA: return "QL_ERR_CUDA: CUDA runtime error";
         case QL_ERR_DEVICE_TIMEOUT: return "QL_ERR_DEVICE_TIMEOUT: a kernel wait ran out of time";
+        case QL_ERR_OUT_OF_BOUNDS: return "QL_ERR_OUT_OF_BOUNDS: a bounds-checked build skipped an out-of-range access";
     }
     return "unknown ql_status";
 }
@@ -291,7 +295,10 @@ static ql_status cast_per_block_common(const void* x, ql_dtype x_dtype, int64_t 
     if (x == nullptr || out == nullptr || out_sf == nullptr) return QL_ERR_INVALID_ARG;
     if (dual && out_sf_t == nullptr) return QL_ERR_INVALID_ARG;
     if ((m + 127) / 128 > 65535) return QL_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (ql_status s = device_info(di); s != QL_OK) return s;
     ql::CastBlockArgs a{};
+    a.dev_status = di.status;
     a.x = x;
     a.is_bf16 = x_dtype == QL_BF16;
     a.m = m;
@@ -328,7 +335,10 @@ ql_status fp8_cast_per_token_dual(const void* x, ql_dtype x_dtype, int64_t m, in
         return QL_ERR_INVALID_ARG;
     if (x_stride_m < n || out_rows_stride_m < n || out_cols_stride_m < n) return QL_ERR_INVALID_ARG;
     if ((m + 127) / 128 > 65535) return QL_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (ql_status s = device_info(di); s != QL_OK) return s;
     ql::CastDualArgs a{};
+    a.dev_status = di.status;
     a.x = x;
     a.is_bf16 = x_dtype == QL_BF16;
     a.m = m;
@@ -584,19 +594,33 @@ ql_status ql_test_stall_gemm_producer(int enable) {
     return QL_OK;
 }
 
-ql_status ql_device_status(ql_stream_t stream) {
+ql_status ql_device_status_detail(ql_stream_t stream, uint32_t* flags, uint64_t* first_bad_address) {
     DeviceInfo di;
     ql_status s = device_info(di);
     if (s != QL_OK) return s;
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QL_ERR_CUDA;
-    uint32_t v = 0;
-    if (cudaMemcpy(&v, di.status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QL_ERR_CUDA;
-    if (v != 0) {
-        const uint32_t zero = 0;
-        if (cudaMemcpy(di.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return QL_ERR_CUDA;
-        return (v & ql::kDevErrTimeout) ? QL_ERR_DEVICE_TIMEOUT : QL_ERR_INVALID_ARG;
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    if (cudaMemcpy(v, di.status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QL_ERR_CUDA;
+    if (flags != nullptr) *flags = v[0];
+    if (first_bad_address != nullptr) *first_bad_address = static_cast<uint64_t>(v[2]) | (static_cast<uint64_t>(v[3]) << 32);
+    if (v[0] != 0 || v[2] != 0 || v[3] != 0) {
+        const uint32_t zero[4] = {0u, 0u, 0u, 0u};
+        if (cudaMemcpy(di.status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return QL_ERR_CUDA;
     }
+    if (v[0] & ql::kDevErrTimeout) return QL_ERR_DEVICE_TIMEOUT;
+    if (v[0] & ql::kDevErrBounds) return QL_ERR_OUT_OF_BOUNDS;
+    if (v[0] != 0) return QL_ERR_INVALID_ARG;
     return QL_OK;
+}
+
+ql_status ql_device_status(ql_stream_t stream) { return ql_device_status_detail(stream, nullptr, nullptr); }
+
+int ql_bounds_checked(void) {
+#ifdef QL_BOUNDS_CHECK
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 }  // extern "C"

@@ -15,6 +15,7 @@
 
 #include <utility>
 
+#include "bounds.cuh"
 #include "cast.cuh"
 #include "common.cuh"
 #include "gemm.cuh"
@@ -41,7 +42,8 @@ template <typename T, int GRAN, int FMT, bool RECIP>
 __global__ void __launch_bounds__(256, 4) cast_rows_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx,
                                                         uint8_t* __restrict__ out, int64_t ldo,
                                                         void* __restrict__ sf, int64_t ssm, int64_t ssg,
-                                                        int64_t chunks_per_row, int vec_in, int vec_out) {
+                                                        int64_t chunks_per_row, int vec_in, int vec_out,
+                                                        const Bounds bnd) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int kElemsPerLane = 64 / sizeof(T);          // 32 (bf16) or 16 (fp32)
     constexpr int kChunk = 32 * kElemsPerLane;
@@ -67,11 +69,12 @@ __global__ void __launch_bounds__(256, 4) cast_rows_kernel(const T* __restrict__
         for (int l = 0; l < kLoads; ++l) {
             const int64_t e = e0 + l * kVec;
             if (vec_in && e + kVec <= n) {
-                raw[l] = __ldg(reinterpret_cast<const uint4*>(xr + e));
+                raw[l] = QL_IN(bnd, 0, xr + e, 16) ? __ldg(reinterpret_cast<const uint4*>(xr + e)) : make_uint4(0, 0, 0, 0);
             } else {
                 union { uint4 u; T t[kVec]; } tmp;
 #pragma unroll
-                for (int i = 0; i < kVec; ++i) tmp.t[i] = (e + i < n) ? xr[e + i] : T(0.0f);
+                for (int i = 0; i < kVec; ++i)
+                    tmp.t[i] = (e + i < n && QL_IN(bnd, 0, xr + e + i, sizeof(T))) ? xr[e + i] : T(0.0f);
                 raw[l] = tmp.u;
             }
         }
@@ -112,17 +115,21 @@ __global__ void __launch_bounds__(256, 4) cast_rows_kernel(const T* __restrict__
             if (vec_out && e0 + kElemsPerLane <= n) {
 #pragma unroll
                 for (int q = 0; q < kElemsPerLane / 16; ++q)
-                    *reinterpret_cast<uint4*>(orow + e0 + 16 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    if (QL_IN(bnd, 1, orow + e0 + 16 * q, 16))
+                        *reinterpret_cast<uint4*>(orow + e0 + 16 * q) =
+                            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             } else {
 #pragma unroll
                 for (int i = 0; i < kElemsPerLane; ++i)
-                    if (e0 + i < n) orow[e0 + i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+                    if (e0 + i < n && QL_IN(bnd, 1, orow + e0 + i, 1))
+                        orow[e0 + i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
             }
         }
 
         const int64_t g = e0 / GRAN;
         if constexpr (FMT != kSfPacked) {
-            if ((lane % kLanesPerGroup) == 0 && g < G) static_cast<float*>(sf)[row * ssm + g * ssg] = s;
+            float* sp = static_cast<float*>(sf) + row * ssm + g * ssg;
+            if ((lane % kLanesPerGroup) == 0 && g < G && QL_IN(bnd, 2, sp, 4)) *sp = s;
         } else {
             // four consecutive groups per int32 word; groups past the last are 0
             constexpr int kWordLanes = 4 * kLanesPerGroup;  // 4 .. 32
@@ -132,8 +139,8 @@ __global__ void __launch_bounds__(256, 4) cast_rows_kernel(const T* __restrict__
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 word |= __shfl_sync(0xffffffffu, mine, base + j * kLanesPerGroup) << (8 * j);
-            if ((lane % kWordLanes) == 0 && g < G)
-                static_cast<int32_t*>(sf)[row * ssm + (g / 4) * ssg] = static_cast<int32_t>(word);
+            int32_t* wp = static_cast<int32_t*>(sf) + row * ssm + (g / 4) * ssg;
+            if ((lane % kWordLanes) == 0 && g < G && QL_IN(bnd, 2, wp, 4)) *wp = static_cast<int32_t>(word);
         }
     }
     // this CTA's work is done: the next kernel of the stream may be scheduled
@@ -159,7 +166,7 @@ template <typename T, int GRAN, int FMT, bool RECIP>
 __global__ void __launch_bounds__(256, 1) cast_cols_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx,
                                                            uint8_t* __restrict__ out, int64_t ldo,
                                                            void* __restrict__ sf, int64_t ssm, int64_t ssg,
-                                                           int vec_in, int vec_out) {
+                                                           int vec_in, int vec_out, const Bounds bnd) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int V = 16 / sizeof(T);          // 8 (bf16) or 4 (fp32)
     constexpr int WI = 4 * V;                  // logical rows per warp
@@ -186,11 +193,14 @@ __global__ void __launch_bounds__(256, 1) cast_cols_kernel(const T* __restrict__
         for (int l = 0; l < 16; ++l) {
             const int64_t j = j0 + l;
             if (j < n && full_cols) {
-                raw[l] = __ldg(reinterpret_cast<const uint4*>(x + j * ldx + i0));
+                const T* src = x + j * ldx + i0;
+                raw[l] = QL_IN(bnd, 0, src, 16) ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
             } else {
                 union { uint4 u; T t[V]; } tmp;
 #pragma unroll
-                for (int c = 0; c < V; ++c) tmp.t[c] = (j < n && i0 + c < m) ? x[j * ldx + i0 + c] : T(0.0f);
+                for (int c = 0; c < V; ++c)
+                    tmp.t[c] = (j < n && i0 + c < m && QL_IN(bnd, 0, x + j * ldx + i0 + c, sizeof(T)))
+                                   ? x[j * ldx + i0 + c] : T(0.0f);
                 raw[l] = tmp.u;
             }
         }
@@ -228,14 +238,17 @@ __global__ void __launch_bounds__(256, 1) cast_cols_kernel(const T* __restrict__
             if (i < m && j0 < n) {
                 uint8_t* orow = out + i * ldo;
                 if (vec_out && j0 + 16 <= n) {
-                    *reinterpret_cast<uint4*>(orow + j0) = make_uint4(w[0], w[1], w[2], w[3]);
+                    if (QL_IN(bnd, 1, orow + j0, 16))
+                        *reinterpret_cast<uint4*>(orow + j0) = make_uint4(w[0], w[1], w[2], w[3]);
                 } else {
                     for (int e = 0; e < 16; ++e)
-                        if (j0 + e < n) orow[j0 + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+                        if (j0 + e < n && QL_IN(bnd, 1, orow + j0 + e, 1))
+                            orow[j0 + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
                 }
             }
             if constexpr (FMT != kSfPacked) {
-                if (leader && i < m && g < Gtot) static_cast<float*>(sf)[i * ssm + g * ssg] = s;
+                float* sp = static_cast<float*>(sf) + i * ssm + g * ssg;
+                if (leader && i < m && g < Gtot && QL_IN(bnd, 2, sp, 4)) *sp = s;
             } else if constexpr (GRAN == 32) {
                 // the subtile's 128 rows are one word: groups of lanes jr = 0, 2, 4, 6
                 const uint32_t mine = (g < Gtot) ? ebyte : 0u;
@@ -243,8 +256,8 @@ __global__ void __launch_bounds__(256, 1) cast_cols_kernel(const T* __restrict__
 #pragma unroll
                 for (int k = 0; k < 4; ++k) word |= __shfl_sync(0xffffffffu, mine, ic + 8 * k) << (8 * k);
                 const int64_t g0 = (jw + sub * WJ) / GRAN;
-                if (jr == 0 && i < m && g0 < Gtot)
-                    static_cast<int32_t*>(sf)[i * ssm + (g0 / 4) * ssg] = static_cast<int32_t>(word);
+                int32_t* wp = static_cast<int32_t*>(sf) + i * ssm + (g0 / 4) * ssg;
+                if (jr == 0 && i < m && g0 < Gtot && QL_IN(bnd, 2, wp, 4)) *wp = static_cast<int32_t>(word);
             } else {
                 ebytes[c] |= ((g < Gtot) ? ebyte : 0u) << (8 * sub);
             }
@@ -255,8 +268,8 @@ __global__ void __launch_bounds__(256, 1) cast_cols_kernel(const T* __restrict__
 #pragma unroll
         for (int c = 0; c < V; ++c) {
             const int64_t i = i0 + c;
-            if (jr == 0 && i < m && g0 < Gtot)
-                static_cast<int32_t*>(sf)[i * ssm + (g0 / 4) * ssg] = static_cast<int32_t>(ebytes[c]);
+            int32_t* wp = static_cast<int32_t*>(sf) + i * ssm + (g0 / 4) * ssg;
+            if (jr == 0 && i < m && g0 < Gtot && QL_IN(bnd, 2, wp, 4)) *wp = static_cast<int32_t>(ebytes[c]);
         }
     }
     // this CTA's work is done: the next kernel of the stream may be scheduled
@@ -286,7 +299,8 @@ template <typename T, int GRAN, int FMT, bool RECIP>
 __global__ void __launch_bounds__(96) cast_cols_tma_kernel(const __grid_constant__ CUtensorMap tmap, int64_t m,
                                                           int64_t n, uint8_t* __restrict__ out, int64_t ldo,
                                                           void* __restrict__ sf, int64_t ssm, int64_t ssg,
-                                                          int vec_out, uint32_t* dev_status, uint64_t limit_ns) {
+                                                          int vec_out, uint32_t* dev_status, uint64_t limit_ns,
+                                                          const Bounds bnd) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     using namespace cols_tma;
     constexpr int V = 16 / sizeof(T);
@@ -390,22 +404,25 @@ __global__ void __launch_bounds__(96) cast_cols_tma_kernel(const __grid_constant
                     if (i < m && j0 < n) {
                         uint8_t* orow = out + i * ldo;
                         if (vec_out && j0 + 16 <= n) {
-                            *reinterpret_cast<uint4*>(orow + j0) = make_uint4(w[0], w[1], w[2], w[3]);
+                            if (QL_IN(bnd, 1, orow + j0, 16))
+                                *reinterpret_cast<uint4*>(orow + j0) = make_uint4(w[0], w[1], w[2], w[3]);
                         } else {
                             for (int e = 0; e < 16; ++e)
-                                if (j0 + e < n) orow[j0 + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+                                if (j0 + e < n && QL_IN(bnd, 1, orow + j0 + e, 1))
+                                    orow[j0 + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
                         }
                     }
                     if constexpr (FMT != kSfPacked) {
-                        if (leader && i < m && g < Gtot) static_cast<float*>(sf)[i * ssm + g * ssg] = sc;
+                        float* sp = static_cast<float*>(sf) + i * ssm + g * ssg;
+                        if (leader && i < m && g < Gtot && QL_IN(bnd, 2, sp, 4)) *sp = sc;
                     } else if constexpr (GRAN == 32) {
                         const uint32_t mine = (g < Gtot) ? ebyte : 0u;
                         uint32_t word = 0;
 #pragma unroll
                         for (int k = 0; k < 4; ++k) word |= __shfl_sync(0xffffffffu, mine, ic + 8 * k) << (8 * k);
                         const int64_t g0 = (jb * kUnit + b) * kRows / GRAN;
-                        if (jr == 0 && i < m && g0 < Gtot)
-                            static_cast<int32_t*>(sf)[i * ssm + (g0 / 4) * ssg] = static_cast<int32_t>(word);
+                        int32_t* wp = static_cast<int32_t*>(sf) + i * ssm + (g0 / 4) * ssg;
+                        if (jr == 0 && i < m && g0 < Gtot && QL_IN(bnd, 2, wp, 4)) *wp = static_cast<int32_t>(word);
                     } else {
                         words[c] |= ((g < Gtot) ? ebyte : 0u) << (8 * b);
                     }
@@ -417,8 +434,8 @@ __global__ void __launch_bounds__(96) cast_cols_tma_kernel(const __grid_constant
 #pragma unroll
                     for (int c = 0; c < V; ++c) {
                         const int64_t i = i0 + c;
-                        if (jr == 0 && i < m && g0 < Gtot)
-                            static_cast<int32_t*>(sf)[i * ssm + (g0 / 4) * ssg] = static_cast<int32_t>(words[c]);
+                        int32_t* wp = static_cast<int32_t*>(sf) + i * ssm + (g0 / 4) * ssg;
+                        if (jr == 0 && i < m && g0 < Gtot && QL_IN(bnd, 2, wp, 4)) *wp = static_cast<int32_t>(words[c]);
                     }
                 }
             }
@@ -451,7 +468,7 @@ template <typename T, int GRAN, int FMT, bool RECIP>
 __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restrict__ x, int64_t m, int64_t n,
                                                                int64_t ldx, uint8_t* __restrict__ out, int64_t ldo,
                                                                void* __restrict__ sf, int64_t ssm, int64_t ssg,
-                                                               int vec_in, int vec_out) {
+                                                               int vec_in, int vec_out, const Bounds bnd) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     using namespace colmajor;
     constexpr int V = kLaneBytes / sizeof(T);       // columns per lane (4 bf16 or 2 fp32)
@@ -472,11 +489,11 @@ __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restri
         const int64_t j = j0 + r;
         const T* src = x + j * ldx + i0;
         if (j < n && vec_in && i0 + V <= m) {
-            raw[r] = __ldg(reinterpret_cast<const uint2*>(src));
+            raw[r] = QL_IN(bnd, 0, src, 8) ? __ldg(reinterpret_cast<const uint2*>(src)) : make_uint2(0, 0);
         } else {
             T t[V];
 #pragma unroll
-            for (int c = 0; c < V; ++c) t[c] = (j < n && i0 + c < m) ? src[c] : T(0.0f);
+            for (int c = 0; c < V; ++c) t[c] = (j < n && i0 + c < m && QL_IN(bnd, 0, src + c, sizeof(T))) ? src[c] : T(0.0f);
             raw[r] = *reinterpret_cast<const uint2*>(t);
         }
     }
@@ -508,10 +525,11 @@ __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restri
         group_scale<FMT, RECIP>(a, sc, f[c], eb);
         const int64_t i = i0 + c;
         if constexpr (FMT != kSfPacked) {
-            if (group_lead && i < m && g < G) static_cast<float*>(sf)[i * ssm + g * ssg] = sc;
+            float* sp = static_cast<float*>(sf) + i * ssm + g * ssg;
+            if (group_lead && i < m && g < G && QL_IN(bnd, 2, sp, 4)) *sp = sc;
         } else if constexpr (GRAN == 128) {
-            if (group_lead && i < m && g < G) {
-                uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + i * ssm + (g / 4) * ssg);
+            uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + i * ssm + (g / 4) * ssg);
+            if (group_lead && i < m && g < G && QL_IN(bnd, 2, word, 4)) {
                 word[g % 4] = static_cast<uint8_t>(eb);
                 if (g == G - 1)
                     for (int z = static_cast<int>(g % 4) + 1; z < 4; ++z) word[z] = 0;
@@ -531,12 +549,14 @@ __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restri
         if constexpr (V == 4)
             w |= e4m3x2(__fmul_rn(to_f32(t[2]), f[2]), __fmul_rn(to_f32(t[3]), f[3])) << 16;
         if (vec_out && i0 + V <= m) {
-            if constexpr (V == 4) *reinterpret_cast<uint32_t*>(dst) = w;
-            else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w);
+            if (QL_IN(bnd, 1, dst, V)) {
+                if constexpr (V == 4) *reinterpret_cast<uint32_t*>(dst) = w;
+                else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w);
+            }
         } else {
 #pragma unroll
             for (int c = 0; c < V; ++c)
-                if (i0 + c < m) dst[c] = static_cast<uint8_t>(w >> (8 * c));
+                if (i0 + c < m && QL_IN(bnd, 1, dst + c, 1)) dst[c] = static_cast<uint8_t>(w >> (8 * c));
         }
     }
     if constexpr (FMT == kSfPacked && GRAN == 32) {
@@ -547,10 +567,11 @@ __global__ void __launch_bounds__(512, 2) cast_colmajor_kernel(const T* __restri
 #pragma unroll
             for (int c = 0; c < V; ++c) {
                 const int64_t i = i0 + c;
-                if (i < m && gw < G) {
+                int32_t* wp = static_cast<int32_t*>(sf) + i * ssm + (gw / 4) * ssg;
+                if (i < m && gw < G && QL_IN(bnd, 2, wp, 4)) {
                     const uint32_t word = ebuf[0][lane][c] | (ebuf[1][lane][c] << 8) | (ebuf[2][lane][c] << 16) |
                                           (ebuf[3][lane][c] << 24);
-                    static_cast<int32_t*>(sf)[i * ssm + (gw / 4) * ssg] = static_cast<int32_t>(word);
+                    *wp = static_cast<int32_t>(word);
                 }
             }
         }
@@ -595,7 +616,7 @@ __global__ void __launch_bounds__(colmajor_sw::kThreads, 1)
     cast_colmajor_sw_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap omap,
                             int64_t m, int64_t n, uint8_t* __restrict__ out, int64_t ldo, void* __restrict__ sf,
                             int64_t ssm, int64_t ssg, int vec_out, int tma_out, uint32_t* dev_status,
-                            uint64_t limit_ns) {
+                            uint64_t limit_ns, const Bounds bnd) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     using namespace colmajor_sw;
     static_assert(GRAN == 32 || GRAN == 128, "groups of 32 or 128 rows");
@@ -732,10 +753,11 @@ __global__ void __launch_bounds__(colmajor_sw::kThreads, 1)
                 const int64_t i = i0 + p_e;
                 const int64_t g = band * NGS + p_gi;
                 if constexpr (FMT != kSfPacked) {
-                    if (lane < NP && i < m && g < G) static_cast<float*>(sf)[i * ssm + g * ssg] = sc;
+                    float* sp = static_cast<float*>(sf) + i * ssm + g * ssg;
+                    if (lane < NP && i < m && g < G && QL_IN(bnd, 2, sp, 4)) *sp = sc;
                 } else if constexpr (GRAN == 128) {
-                    if (lane < NP && i < m && g < G) {
-                        uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + i * ssm + (g / 4) * ssg);
+                    uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + i * ssm + (g / 4) * ssg);
+                    if (lane < NP && i < m && g < G && QL_IN(bnd, 2, word, 4)) {
                         word[g % 4] = static_cast<uint8_t>(eb);
                         if (g == G - 1)
                             for (int z = static_cast<int>(g % 4) + 1; z < 4; ++z) word[z] = 0;
@@ -746,9 +768,9 @@ __global__ void __launch_bounds__(colmajor_sw::kThreads, 1)
                     const uint32_t b1 = __shfl_sync(0xffffffffu, b0, (lane + E) & 31);
                     const uint32_t b2 = __shfl_sync(0xffffffffu, b0, (lane + 2 * E) & 31);
                     const uint32_t b3 = __shfl_sync(0xffffffffu, b0, (lane + 3 * E) & 31);
-                    if (lane < E && i < m && band * 4 < G)
-                        static_cast<int32_t*>(sf)[i * ssm + band * ssg] =
-                            static_cast<int32_t>(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
+                    int32_t* wp = static_cast<int32_t*>(sf) + i * ssm + band * ssg;
+                    if (lane < E && i < m && band * 4 < G && QL_IN(bnd, 2, wp, 4))
+                        *wp = static_cast<int32_t>(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
                 }
             }
             float f[NGS][E];
@@ -786,12 +808,14 @@ __global__ void __launch_bounds__(colmajor_sw::kThreads, 1)
                 if (j >= n) break;
                 uint8_t* dst = out + j * ldo + i0;
                 if (vec_out && i0 + E <= m) {
-                    if constexpr (E == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-                    else *reinterpret_cast<uint32_t*>(dst) = w[0];
+                    if (QL_IN(bnd, 1, dst, E)) {
+                        if constexpr (E == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                        else *reinterpret_cast<uint32_t*>(dst) = w[0];
+                    }
                 } else {
 #pragma unroll
                     for (int e = 0; e < E; ++e)
-                        if (i0 + e < m) dst[e] = static_cast<uint8_t>(w[e / 4] >> (8 * (e % 4)));
+                        if (i0 + e < m && QL_IN(bnd, 1, dst + e, 1)) dst[e] = static_cast<uint8_t>(w[e / 4] >> (8 * (e % 4)));
                 }
             }
             if (tile_out) {
@@ -814,7 +838,7 @@ template <typename T, int GRAN, int FMT, bool RECIP>
 __global__ void __launch_bounds__(128) cast_generic_kernel(const T* __restrict__ x, int64_t m, int64_t n,
                                                            int64_t sxm, int64_t sxn, uint8_t* __restrict__ out,
                                                            int64_t som, int64_t son, void* __restrict__ sf,
-                                                           int64_t ssm, int64_t ssg) {
+                                                           int64_t ssm, int64_t ssg, const Bounds bnd) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     const int64_t G = (n + GRAN - 1) / GRAN;
     const int64_t W = (G + 3) / 4;
@@ -828,17 +852,25 @@ __global__ void __launch_bounds__(128) cast_generic_kernel(const T* __restrict__
             if (g >= G) break;
             const int64_t j0 = g * GRAN, j1 = (j0 + GRAN < n) ? j0 + GRAN : n;
             float amax = 0.0f;
-            for (int64_t j = j0; j < j1; ++j) amax = fmaxf(amax, fabsf(to_f32(x[i * sxm + j * sxn])));
+            for (int64_t j = j0; j < j1; ++j)
+                if (QL_IN(bnd, 0, x + i * sxm + j * sxn, sizeof(T))) amax = fmaxf(amax, fabsf(to_f32(x[i * sxm + j * sxn])));
             float s, f;
             uint32_t ebyte;
             group_scale<FMT, RECIP>(amax, s, f, ebyte);
             for (int64_t j = j0; j < j1; ++j)
-                out[i * som + j * son] =
-                    static_cast<uint8_t>(e4m3x2(__fmul_rn(to_f32(x[i * sxm + j * sxn]), f), 0.0f) & 0xFFu);
-            if constexpr (FMT != kSfPacked) static_cast<float*>(sf)[i * ssm + g * ssg] = s;
+                if (QL_IN(bnd, 0, x + i * sxm + j * sxn, sizeof(T)) && QL_IN(bnd, 1, out + i * som + j * son, 1))
+                    out[i * som + j * son] =
+                        static_cast<uint8_t>(e4m3x2(__fmul_rn(to_f32(x[i * sxm + j * sxn]), f), 0.0f) & 0xFFu);
+            if constexpr (FMT != kSfPacked) {
+                float* sp = static_cast<float*>(sf) + i * ssm + g * ssg;
+                if (QL_IN(bnd, 2, sp, 4)) *sp = s;
+            }
             word |= ebyte << (8 * q);
         }
-        if constexpr (FMT == kSfPacked) static_cast<int32_t*>(sf)[i * ssm + w * ssg] = static_cast<int32_t>(word);
+        if constexpr (FMT == kSfPacked) {
+            int32_t* wp = static_cast<int32_t*>(sf) + i * ssm + w * ssg;
+            if (QL_IN(bnd, 2, wp, 4)) *wp = static_cast<int32_t>(word);
+        }
     }
     // this CTA's work is done: the next kernel of the stream may be scheduled
     pdl_launch_dependents();
@@ -863,7 +895,7 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
                                                          uint8_t* __restrict__ out, int64_t som, int64_t son,
                                                          int out_mode, void* __restrict__ sf, int64_t ssr,
                                                          int64_t ssc, void* __restrict__ sf_t, int64_t sst_c,
-                                                         int64_t sst_r) {
+                                                         int64_t sst_r, const Bounds bnd) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int B = 128;
     // E4M3 bytes of the block, [row][col] with a row pitch of 144 bytes (16-byte
@@ -908,7 +940,7 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
         if (in_mode == 0) { p = x + gr * sxm + gc; full = gr < m && gc + 8 <= n; step = 1; }
         else if (in_mode == 1) { p = x + gr + gc * sxn; full = gc < n && gr + 8 <= m; step = 1; }
         else { p = x + gr * sxm + gc * sxn; full = false; step = sxn; }
-        if (full) {
+        if (full && QL_IN(bnd, 0, p, 8 * sizeof(T))) {
             const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
             raw[it * WPG + 0] = u.x; raw[it * WPG + 1] = u.y; raw[it * WPG + 2] = u.z; raw[it * WPG + 3] = u.w;
             if constexpr (sizeof(T) == 4) {
@@ -921,7 +953,7 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const bool in = (in_mode == 1) ? (gc < n && gr + e < m) : (gr < m && gc + e < n);
-                if (in) put(it, e, elem_bits(p + e * step));
+                if (in && QL_IN(bnd, 0, p + e * step, sizeof(T))) put(it, e, elem_bits(p + e * step));
             }
         }
     }
@@ -952,24 +984,30 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
     if (tid == 0) {
         const int64_t br = blockIdx.y, bc = blockIdx.x;
         if constexpr (FMT != kSfPacked) {
-            static_cast<float*>(sf)[br * ssr + bc * ssc] = s;
+            float* sp = static_cast<float*>(sf) + br * ssr + bc * ssc;
+            if (QL_IN(bnd, 2, sp, 4)) *sp = s;
         } else {
             // packed along the column-block axis: block bc is byte bc % 4 of
             // word bc / 4; the last column block also zeroes the pad bytes
             uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf) + br * ssr + (bc / 4) * ssc);
-            word[bc % 4] = static_cast<uint8_t>(ebyte);
-            if (bc == static_cast<int64_t>(gridDim.x) - 1)
-                for (int64_t z = bc % 4 + 1; z < 4; ++z) word[z] = 0;
+            if (QL_IN(bnd, 2, word, 4)) {
+                word[bc % 4] = static_cast<uint8_t>(ebyte);
+                if (bc == static_cast<int64_t>(gridDim.x) - 1)
+                    for (int64_t z = bc % 4 + 1; z < 4; ++z) word[z] = 0;
+            }
         }
         if (sf_t != nullptr) {
             if constexpr (FMT != kSfPacked) {
-                static_cast<float*>(sf_t)[bc * sst_c + br * sst_r] = s;
+                float* sp = static_cast<float*>(sf_t) + bc * sst_c + br * sst_r;
+                if (QL_IN(bnd, 3, sp, 4)) *sp = s;
             } else {
                 // packed along the row-block axis: block br is byte br % 4 of word br / 4
                 uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sf_t) + bc * sst_c + (br / 4) * sst_r);
-                word[br % 4] = static_cast<uint8_t>(ebyte);
-                if (br == static_cast<int64_t>(gridDim.y) - 1)
-                    for (int64_t z = br % 4 + 1; z < 4; ++z) word[z] = 0;
+                if (QL_IN(bnd, 3, word, 4)) {
+                    word[br % 4] = static_cast<uint8_t>(ebyte);
+                    if (br == static_cast<int64_t>(gridDim.y) - 1)
+                        for (int64_t z = br % 4 + 1; z < 4; ++z) word[z] = 0;
+                }
             }
         }
     }
@@ -1021,11 +1059,11 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
                 }
             }
             if (gc + 16 <= n) {
-                *reinterpret_cast<uint4*>(o) = u;
+                if (QL_IN(bnd, 1, o, 16)) *reinterpret_cast<uint4*>(o) = u;
             } else {
                 const uint8_t* ub = reinterpret_cast<const uint8_t*>(&u);
                 for (int e = 0; e < 16; ++e)
-                    if (gc + e < n) o[e] = ub[e];
+                    if (gc + e < n && QL_IN(bnd, 1, o + e, 1)) o[e] = ub[e];
             }
         } else if (out_mode == 1) {
             const int64_t gc = c0 + line, gr = r0 + off;
@@ -1040,16 +1078,17 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     uw[e] = b16[4 * e] | (b16[4 * e + 1] << 8) | (b16[4 * e + 2] << 16) | (static_cast<uint32_t>(b16[4 * e + 3]) << 24);
-                *reinterpret_cast<uint4*>(o) = u;
+                if (QL_IN(bnd, 1, o, 16)) *reinterpret_cast<uint4*>(o) = u;
             } else {
                 for (int e = 0; e < 16; ++e)
-                    if (gr + e < m) o[e] = b16[e];
+                    if (gr + e < m && QL_IN(bnd, 1, o + e, 1)) o[e] = b16[e];
             }
         } else {
             const int64_t gr = r0 + line, gc = c0 + off;
             if (gr >= m) continue;
             for (int e = 0; e < 16; ++e)
-                if (gc + e < n) out[gr * som + (gc + e) * son] = qbuf[line * pitch + off + e];
+                if (gc + e < n && QL_IN(bnd, 1, out + gr * som + (gc + e) * son, 1))
+                    out[gr * som + (gc + e) * son] = qbuf[line * pitch + off + e];
         }
     }
     // this CTA's work is done: the next kernel of the stream may be scheduled
@@ -1079,7 +1118,8 @@ template <typename T, int FMT, bool RECIP>
 __global__ void __launch_bounds__(dual::kThreads, 2)
     cast_dual_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx, uint8_t* __restrict__ qr,
                      int64_t ldr, void* __restrict__ sfr, int64_t srm, int64_t srg, uint8_t* __restrict__ qc,
-                     int64_t ldc, void* __restrict__ sfc, int64_t scn, int64_t scg, int vec_in, int vec_out) {
+                     int64_t ldc, void* __restrict__ sfc, int64_t scn, int64_t scg, int vec_in, int vec_out,
+                     const Bounds bnd) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int WPG = (8 * static_cast<int>(sizeof(T))) / 4;      // words per 8 elements
     constexpr int NIT = dual::kRowsPerThread;
@@ -1097,7 +1137,7 @@ __global__ void __launch_bounds__(dual::kThreads, 2)
     for (int it = 0; it < NIT; ++it) {
         const int64_t gr = r0 + it * RS + tid / 16;
         const T* p = x + gr * ldx + gc;
-        if (vec_in && gr < m && gc + 8 <= n) {
+        if (vec_in && gr < m && gc + 8 <= n && QL_IN(bnd, 0, p, 8 * sizeof(T))) {
             const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
             raw[it * WPG + 0] = u.x; raw[it * WPG + 1] = u.y; raw[it * WPG + 2] = u.z; raw[it * WPG + 3] = u.w;
             if constexpr (sizeof(T) == 4) {
@@ -1107,7 +1147,7 @@ __global__ void __launch_bounds__(dual::kThreads, 2)
         } else {
             union { uint32_t w[WPG]; T t[8]; } tmp;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) tmp.t[e] = (gr < m && gc + e < n) ? p[e] : T(0.0f);
+            for (int e = 0; e < 8; ++e) tmp.t[e] = (gr < m && gc + e < n && QL_IN(bnd, 0, p + e, sizeof(T))) ? p[e] : T(0.0f);
 #pragma unroll
             for (int w = 0; w < WPG; ++w) raw[it * WPG + w] = tmp.w[w];
         }
@@ -1158,12 +1198,15 @@ __global__ void __launch_bounds__(dual::kThreads, 2)
         const int64_t gr = r0 + my_it * RS + tid / 16;
         if (gr < m) {
             if constexpr (FMT != kSfPacked) {
-                static_cast<float*>(sfr)[gr * srm + bc * srg] = s_r;
+                float* sp = static_cast<float*>(sfr) + gr * srm + bc * srg;
+                if (QL_IN(bnd, 2, sp, 4)) *sp = s_r;
             } else {
                 uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sfr) + gr * srm + (bc / 4) * srg);
-                word[bc % 4] = static_cast<uint8_t>(e_r);
-                if (bc == static_cast<int64_t>(gridDim.x) - 1)
-                    for (int64_t z = bc % 4 + 1; z < 4; ++z) word[z] = 0;
+                if (QL_IN(bnd, 2, word, 4)) {
+                    word[bc % 4] = static_cast<uint8_t>(e_r);
+                    if (bc == static_cast<int64_t>(gridDim.x) - 1)
+                        for (int64_t z = bc % 4 + 1; z < 4; ++z) word[z] = 0;
+                }
             }
         }
     }
@@ -1182,12 +1225,15 @@ __global__ void __launch_bounds__(dual::kThreads, 2)
         const int64_t col = c0 + tid;
         if (col < n) {
             if constexpr (FMT != kSfPacked) {
-                static_cast<float*>(sfc)[col * scn + br * scg] = s_c;
+                float* sp = static_cast<float*>(sfc) + col * scn + br * scg;
+                if (QL_IN(bnd, 4, sp, 4)) *sp = s_c;
             } else {
                 uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sfc) + col * scn + (br / 4) * scg);
-                word[br % 4] = static_cast<uint8_t>(e_c);
-                if (br == static_cast<int64_t>(gridDim.y) - 1)
-                    for (int64_t z = br % 4 + 1; z < 4; ++z) word[z] = 0;
+                if (QL_IN(bnd, 4, word, 4)) {
+                    word[br % 4] = static_cast<uint8_t>(e_c);
+                    if (br == static_cast<int64_t>(gridDim.y) - 1)
+                        for (int64_t z = br % 4 + 1; z < 4; ++z) word[z] = 0;
+                }
             }
         }
     }
@@ -1210,14 +1256,14 @@ __global__ void __launch_bounds__(dual::kThreads, 2)
         uint8_t* dr = qr + gr * ldr + gc;
         uint8_t* dc = qc + gr * ldc + gc;
         if (vec_out && gc + 8 <= n) {
-            *reinterpret_cast<uint2*>(dr) = make_uint2(r_lo, r_hi);
-            *reinterpret_cast<uint2*>(dc) = make_uint2(c_lo, c_hi);
+            if (QL_IN(bnd, 1, dr, 8)) *reinterpret_cast<uint2*>(dr) = make_uint2(r_lo, r_hi);
+            if (QL_IN(bnd, 3, dc, 8)) *reinterpret_cast<uint2*>(dc) = make_uint2(c_lo, c_hi);
         } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 if (gc + e < n) {
-                    dr[e] = static_cast<uint8_t>((e < 4 ? r_lo : r_hi) >> (8 * (e & 3)));
-                    dc[e] = static_cast<uint8_t>((e < 4 ? c_lo : c_hi) >> (8 * (e & 3)));
+                    if (QL_IN(bnd, 1, dr + e, 1)) dr[e] = static_cast<uint8_t>((e < 4 ? r_lo : r_hi) >> (8 * (e & 3)));
+                    if (QL_IN(bnd, 3, dc + e, 1)) dc[e] = static_cast<uint8_t>((e < 4 ? c_lo : c_hi) >> (8 * (e & 3)));
                 }
             }
         }
@@ -1246,9 +1292,46 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Byte ranges of the buffers of each cast (checked in bounds-checked builds).
+Bounds token_bounds(const CastTokenArgs& a, int64_t es, int gran, int fmt) {
+    Bounds b{};
+    const int64_t G = (a.n + gran - 1) / gran;
+    b.s[0] = span_of(a.x, es, a.m, a.sxm, a.n, a.sxn);
+    b.s[1] = span_of(a.out, 1, a.m, a.som, a.n, a.son);
+    b.s[2] = span_of(a.sf, 4, a.m, a.ssm, fmt == kSfPacked ? (G + 3) / 4 : G, a.ssg);
+    b.status = a.dev_status;
+    return b;
+}
+
+Bounds block_bounds(const CastBlockArgs& a, int64_t es, int fmt) {
+    Bounds b{};
+    const int64_t rb = (a.m + 127) / 128, cb = (a.n + 127) / 128;
+    const bool packed = fmt == kSfPacked;
+    b.s[0] = span_of(a.x, es, a.m, a.sxm, a.n, a.sxn);
+    b.s[1] = span_of(a.out, 1, a.m, a.som, a.n, a.son);
+    b.s[2] = span_of(a.sf, 4, rb, a.ssr, packed ? (cb + 3) / 4 : cb, a.ssc);
+    b.s[3] = span_of(a.sf_t, 4, cb, a.sst_c, packed ? (rb + 3) / 4 : rb, a.sst_r);
+    b.status = a.dev_status;
+    return b;
+}
+
+Bounds dual_bounds(const CastDualArgs& a, int64_t es, int fmt) {
+    Bounds b{};
+    const int64_t gr = (a.n + 127) / 128, gc = (a.m + 127) / 128;
+    const bool packed = fmt == kSfPacked;
+    b.s[0] = span_of(a.x, es, a.m, a.sxm, a.n, 1);
+    b.s[1] = span_of(a.qr, 1, a.m, a.ldr, a.n, 1);
+    b.s[2] = span_of(a.sfr, 4, a.m, a.srm, packed ? (gr + 3) / 4 : gr, a.srg);
+    b.s[3] = span_of(a.qc, 1, a.m, a.ldc, a.n, 1);
+    b.s[4] = span_of(a.sfc, 4, a.n, a.scn, packed ? (gc + 3) / 4 : gc, a.scg);
+    b.status = a.dev_status;
+    return b;
+}
+
 template <typename T, int GRAN, int FMT, bool RECIP>
 cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms) {
     const T* x = static_cast<const T*>(a.x);
+    const Bounds bnd = token_bounds(a, sizeof(T), GRAN, FMT);
     if (a.sxn == 1 && a.son == 1) {
         const int vec_in = aligned16(x) && ((a.sxm * static_cast<int64_t>(sizeof(T))) % 16 == 0);
         const int vec_out = aligned16(a.out) && (a.som % 16 == 0);
@@ -1260,7 +1343,7 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         const int64_t cap = static_cast<int64_t>(num_sms) * 4;
         if (blocks > cap) blocks = cap;
         return launch_pdl(cast_rows_kernel<T, GRAN, FMT, RECIP>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
-                          x, a.m, a.n, a.sxm, a.out, a.som, a.sf, a.ssm, a.ssg, chunks, vec_in, vec_out);
+                          x, a.m, a.n, a.sxm, a.out, a.som, a.sf, a.ssm, a.ssg, chunks, vec_in, vec_out, bnd);
     }
     if (a.sxm == 1 && a.som == 1 && a.tma_ok) {
         using namespace colmajor_sw;
@@ -1283,7 +1366,7 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
             int64_t grid = num_sms;
             if (grid > units) grid = units;
             return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, st, tmap, omap, a.m,
-                              a.n, a.out, a.son, a.sf, a.ssm, a.ssg, vec_out, tma_out, a.dev_status, a.wait_limit_ns);
+                              a.n, a.out, a.son, a.sf, a.ssm, a.ssg, vec_out, tma_out, a.dev_status, a.wait_limit_ns, bnd);
         }
     }
     if (a.sxm == 1 && a.som == 1) {
@@ -1292,7 +1375,7 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) % V) == 0) && (a.son % V == 0);
         dim3 grid(static_cast<unsigned>((a.m + 32 * V - 1) / (32 * V)), static_cast<unsigned>((a.n + 127) / 128));
         return launch_pdl(cast_colmajor_kernel<T, GRAN, FMT, RECIP>, grid, dim3(32 * colmajor::kWarps), 0, st, x, a.m,
-                          a.n, a.sxn, a.out, a.son, a.sf, a.ssm, a.ssg, vec_in, vec_out);
+                          a.n, a.sxn, a.out, a.son, a.sf, a.ssm, a.ssg, vec_in, vec_out, bnd);
     }
     if (a.sxm == 1 && a.son == 1 && a.tma_ok) {
         using namespace cols_tma;
@@ -1309,7 +1392,7 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
             int64_t grid = static_cast<int64_t>(num_sms) * 3;
             if (grid > units) grid = units;
             return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, st, tmap, a.m, a.n, a.out,
-                              a.som, a.sf, a.ssm, a.ssg, vec_out, a.dev_status, a.wait_limit_ns);
+                              a.som, a.sf, a.ssm, a.ssg, vec_out, a.dev_status, a.wait_limit_ns, bnd);
         }
     }
     if (a.sxm == 1 && a.son == 1) {
@@ -1320,7 +1403,7 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
         dim3 grid(static_cast<unsigned>((a.m + 32 * V - 1) / (32 * V)),
                   static_cast<unsigned>((a.n + kRowsPerCta - 1) / kRowsPerCta));
         return launch_pdl(cast_cols_kernel<T, GRAN, FMT, RECIP>, grid, dim3(256), 0, st, x, a.m, a.n, a.sxn, a.out,
-                          a.som, a.sf, a.ssm, a.ssg, vec_in, vec_out);
+                          a.som, a.sf, a.ssm, a.ssg, vec_in, vec_out, bnd);
     }
     const int64_t G = (a.n + GRAN - 1) / GRAN;
     const int64_t total = a.m * ((G + 3) / 4);
@@ -1328,7 +1411,7 @@ cudaError_t launch_token_t(const CastTokenArgs& a, cudaStream_t st, int num_sms)
     if (blocks > static_cast<int64_t>(num_sms) * 16) blocks = static_cast<int64_t>(num_sms) * 16;
     if (blocks < 1) blocks = 1;
     return launch_pdl(cast_generic_kernel<T, GRAN, FMT, RECIP>, dim3(static_cast<unsigned>(blocks)), dim3(128), 0, st,
-                      x, a.m, a.n, a.sxm, a.sxn, a.out, a.som, a.son, a.sf, a.ssm, a.ssg);
+                      x, a.m, a.n, a.sxm, a.sxn, a.out, a.som, a.son, a.sf, a.ssm, a.ssg, bnd);
 }
 
 template <typename T, int GRAN>
@@ -1353,7 +1436,8 @@ cudaError_t launch_block_t(const CastBlockArgs& a, cudaStream_t st) {
     else if (a.som == 1 && aligned16(a.out) && a.son % 16 == 0) out_mode = 1;
     dim3 grid(static_cast<unsigned>((a.n + 127) / 128), static_cast<unsigned>((a.m + 127) / 128));
     return launch_pdl(cast_block_kernel<T, FMT, RECIP>, grid, dim3(256), 0, st, x, a.m, a.n, a.sxm, a.sxn, in_mode,
-                      a.out, a.som, a.son, out_mode, a.sf, a.ssr, a.ssc, a.sf_t, a.sst_c, a.sst_r);
+                      a.out, a.som, a.son, out_mode, a.sf, a.ssr, a.ssc, a.sf_t, a.sst_c, a.sst_r,
+                      block_bounds(a, es, FMT));
 }
 
 template <typename T>
@@ -1387,7 +1471,8 @@ cudaError_t launch_dual_t(const CastDualArgs& a, cudaStream_t st) {
                         a.ldr % 8 == 0 && a.ldc % 8 == 0;
     dim3 grid(static_cast<unsigned>((a.n + 127) / 128), static_cast<unsigned>((a.m + 127) / 128));
     return launch_pdl(cast_dual_kernel<T, FMT, RECIP>, grid, dim3(dual::kThreads), 0, st, x, a.m, a.n, a.sxm, a.qr,
-                      a.ldr, a.sfr, a.srm, a.srg, a.qc, a.ldc, a.sfc, a.scn, a.scg, vec_in, vec_out);
+                      a.ldr, a.sfr, a.srm, a.srg, a.qc, a.ldc, a.sfc, a.scn, a.scg, vec_in, vec_out,
+                      dual_bounds(a, sizeof(T), FMT));
 }
 
 template <typename T>

@@ -17,7 +17,7 @@ struct CastTokenArgs {
     void* sf;
     int64_t ssm, ssg;
     bool tma_ok;            // the transposed view may be read with TMA
-    uint32_t* dev_status;   // time-out flags of the TMA-staged kernel
+    uint32_t* dev_status;   // time-out flags of the TMA-staged kernel; bounds violations
     uint64_t wait_limit_ns;
 };
 
@@ -35,6 +35,7 @@ struct CastBlockArgs {
     // block (r, c) at [c*sst_c + r*sst_r], packed along r for packed UE8M0
     void* sf_t;
     int64_t sst_c, sst_r;
+    uint32_t* dev_status;   // bounds-checked builds record violations here
 };
 
 // Per-token cast of x and of x^T from one read (1 x 128 groups both ways).
@@ -52,6 +53,7 @@ struct CastDualArgs {
     int64_t ldc;
     void* sfc;                  // its scales [n, ceil(m/128)] at (scn, scg)
     int64_t scn, scg;
+    uint32_t* dev_status;       // bounds-checked builds record violations here
 };
 
 cudaError_t launch_cast_per_token(const CastTokenArgs& a, cudaStream_t st, int num_sms);

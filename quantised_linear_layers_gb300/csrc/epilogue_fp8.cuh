@@ -65,22 +65,26 @@ __device__ __forceinline__ void store_row_e4m3(const float* acc, int64_t row, in
                     *reinterpret_cast<uint4*>(srow + ((((gi * GRAN + j) >> 4) ^ swz) << 4)) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                 } else if (p.vec_store && c + 16 <= p.n) {
-                    *reinterpret_cast<uint4*>(drow + c) = make_uint4(w[0], w[1], w[2], w[3]);
+                    if (QL_IN(p.bnd, 2, drow + c, 16)) *reinterpret_cast<uint4*>(drow + c) = make_uint4(w[0], w[1], w[2], w[3]);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        if (c + e < p.n) drow[c + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+                        if (c + e < p.n && QL_IN(p.bnd, 2, drow + c + e, 1))
+                            drow[c + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
                 }
             }
             const int64_t g = c0 / GRAN;
             if (!row_ok) continue;
             if (p.dfmt != kSfPacked) {
-                static_cast<float*>(p.dsf)[row * p.dsm + g * p.dsg] = s;
+                float* sp = static_cast<float*>(p.dsf) + row * p.dsm + g * p.dsg;
+                if (QL_IN(p.bnd, 3, sp, 4)) *sp = s;
             } else {
                 uint8_t* wb = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(p.dsf) + row * p.dsm + (g / 4) * p.dsg);
-                wb[g % 4] = static_cast<uint8_t>(eb);
-                if (g == G - 1)
-                    for (int z = static_cast<int>(g % 4) + 1; z < 4; ++z) wb[z] = 0;
+                if (QL_IN(p.bnd, 3, wb, 4)) {
+                    wb[g % 4] = static_cast<uint8_t>(eb);
+                    if (g == G - 1)
+                        for (int z = static_cast<int>(g % 4) + 1; z < 4; ++z) wb[z] = 0;
+                }
             }
         }
     }

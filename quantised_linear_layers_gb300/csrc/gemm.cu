@@ -39,6 +39,7 @@
 #include <set>
 #include <utility>
 
+#include "bounds.cuh"
 #include "common.cuh"
 #include "epilogue_fp8.cuh"
 #include "epilogue_tma.cuh"
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int64_t row = m0 + lane + 32 * i;
-                            va[j][i] = (j < cnt && row < p.m) ? decode_scale(p.sfa, p.fmt, row * p.sam, kb0 + j, p.sak) : 0.0f;
+                            va[j][i] = (j < cnt && row < p.m) ? decode_scale(p.sfa, p.fmt, row * p.sam, kb0 + j, p.sak, p.bnd, 0) : 0.0f;
                         }
 #pragma unroll
                         for (int i = 0; i < kSbLoads; ++i) {
@@ -331,11 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (j < cnt) {
                                 if constexpr (PER_ROW_B) {
                                     const int64_t col = n0 + lane + 32 * i;
-                                    if (col < p.n) v = decode_scale(p.sfb, p.fmt, sb_off + col * p.sbn, kb0 + j, p.sbk);
+                                    if (col < p.n) v = decode_scale(p.sfb, p.fmt, sb_off + col * p.sbn, kb0 + j, p.sbk, p.bnd, 1);
                                 } else {
                                     const int64_t r = n0 / 128 + lane;
                                     if (lane < (BN + 127) / 128 && r < nblocks_b)
-                                        v = decode_scale(p.sfb, p.fmt, sb_off + r * p.sbn, kb0 + j, p.sbk);
+                                        v = decode_scale(p.sfb, p.fmt, sb_off + r * p.sbn, kb0 + j, p.sbk, p.bnd, 1);
                                 }
                             }
                             vb[j][i] = v;
@@ -467,11 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             u.y = *reinterpret_cast<uint32_t*>(&h1);
                             u.z = *reinterpret_cast<uint32_t*>(&h2);
                             u.w = *reinterpret_cast<uint32_t*>(&h3);
-                            *reinterpret_cast<uint4*>(drow + c) = u;
+                            if (QL_IN(p.bnd, 2, drow + c, 16)) *reinterpret_cast<uint4*>(drow + c) = u;
                         } else {
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                if (c + e < p.n) drow[c + e] = __float2bfloat16_rn(acc[j + e]);
+                                if (c + e < p.n && QL_IN(p.bnd, 2, drow + c + e, 2)) drow[c + e] = __float2bfloat16_rn(acc[j + e]);
                         }
                     }
                 } else {
@@ -480,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < CPT; j += 4) {
                         const int64_t c = col0 + j;
                         if (vec_store && c + 4 <= p.n) {
+                            if (!QL_IN(p.bnd, 2, drow + c, 16)) continue;
                             float4 o = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
                             if (p.accumulate) {
                                 const float4 old = *reinterpret_cast<const float4*>(drow + c);
@@ -489,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                if (c + e < p.n) drow[c + e] = p.accumulate ? drow[c + e] + acc[j + e] : acc[j + e];
+                                if (c + e < p.n && QL_IN(p.bnd, 2, drow + c + e, 4))
+                                    drow[c + e] = p.accumulate ? drow[c + e] + acc[j + e] : acc[j + e];
                         }
                     }
                 }
@@ -595,6 +598,18 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     p.b_mn = L.b_mn ? 1 : 0;
     const int64_t es = L.out_fp8 ? 1 : (L.out_f32 ? 4 : 2);
     p.vec_store = ((reinterpret_cast<uintptr_t>(L.d) & 15u) == 0 && (L.ldd * es) % 16 == 0) ? 1 : 0;
+    {
+        // byte ranges of the buffers read or written with plain loads and stores
+        const int64_t kscales = L.fmt == 2 ? (p.num_kb + 3) / 4 : p.num_kb;
+        const int64_t brows = L.per_row_b ? L.n : (L.n + 127) / 128;
+        const int64_t dg = L.dgran > 0 ? (L.n + L.dgran - 1) / L.dgran : 0;
+        p.bnd.s[0] = span_of(L.sfa, 4, L.m, L.sam, kscales, L.sak);
+        p.bnd.s[1] = span_of(L.sfb, 4, brows, L.sbn, kscales, L.sbk, L.m_indices ? L.num_groups : 1, L.sbg);
+        p.bnd.s[2] = span_of(L.d, es, L.m, L.ldd, L.n, 1);
+        p.bnd.s[3] = L.out_fp8 ? span_of(L.dsf, 4, L.m, L.dsm, L.dfmt == 2 ? (dg + 3) / 4 : dg, L.dsg) : Span{0, 0};
+        p.bnd.s[4] = span_of(L.m_indices, 4, L.m, 1);
+        p.bnd.status = L.dev_status;
+    }
     const int bn = L.block_n > 0 ? L.block_n : choose_block_n(L.m, L.n, num_sms);
     // UE8M0 scales (fp32 powers of two or packed exponents): promotion by the
     // tensor core's block-scaled MMA unless the CUDA-core path is requested.

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "common.cuh"
 
 namespace ql {
@@ -40,6 +41,9 @@ struct GemmParams {
     int a_mn, b_mn;
     // fp32 output written (or added) through the kernel's D tensor map
     int tma_d;
+    // byte ranges of sfa, sfb, D, D's scales and m_indices, checked in
+    // bounds-checked builds (status: dev_status)
+    Bounds bnd;
 };
 
 // Host-side description of one GEMM call.
@@ -89,7 +93,8 @@ constexpr int kGroupAlignM = 128;
 // bad index in the device status word.
 __device__ __forceinline__ int tile_expert(const GemmParams& p, int mb, bool report) {
     if (p.m_indices == nullptr) return 0;
-    const int e = __ldg(p.m_indices + static_cast<int64_t>(mb) * kGroupAlignM);
+    const int* ip = p.m_indices + static_cast<int64_t>(mb) * kGroupAlignM;
+    const int e = QL_IN(p.bnd, 4, ip, 4) ? __ldg(ip) : -1;
     if (e < -1 || e >= p.num_groups) {
         if (report) atomicOr(p.dev_status, kDevErrBadIndex);
         return -1;
@@ -102,7 +107,7 @@ __device__ __forceinline__ int tile_expert(const GemmParams& p, int mb, bool rep
 // not starting on the alignment) is not stored and is recorded as a bad index.
 __device__ __forceinline__ bool row_in_expert(const GemmParams& p, int64_t row, int e) {
     if (p.m_indices == nullptr) return true;
-    const int r = __ldg(p.m_indices + row);
+    const int r = QL_IN(p.bnd, 4, p.m_indices + row, 4) ? __ldg(p.m_indices + row) : -1;
     if (r == e) return true;
     if (r != -1) atomicOr(p.dev_status, kDevErrBadIndex);
     return false;
@@ -110,7 +115,7 @@ __device__ __forceinline__ bool row_in_expert(const GemmParams& p, int64_t row, 
 
 // The same decision without recording (for the other threads of the row).
 __device__ __forceinline__ bool row_in_expert_quiet(const GemmParams& p, int64_t row, int e) {
-    return p.m_indices == nullptr || __ldg(p.m_indices + row) == e;
+    return p.m_indices == nullptr || (QL_IN(p.bnd, 4, p.m_indices + row, 4) && __ldg(p.m_indices + row) == e);
 }
 #endif
 

@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "common.cuh"
 #include "epilogue_fp8.cuh"
 #include "epilogue_tma.cuh"
@@ -118,11 +119,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // Exponent words of K group g for R scale rows (see gemm_mx.cu).
 template <int R>
 __device__ __forceinline__ void exp_words(const void* base, int fmt, const int64_t (&row_off)[R],
-                                          const bool (&valid)[R], int g, int64_t sk, int num_kb, uint32_t (&w)[R]) {
+                                          const bool (&valid)[R], int g, int64_t sk, int num_kb, uint32_t (&w)[R],
+                                          const Bounds& bnd, int si) {
     if (fmt == 2) {
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            w[r] = valid[r] ? __ldg(static_cast<const uint32_t*>(base) + row_off[r] + g * sk) : 0u;
+        {
+            const uint32_t* q = static_cast<const uint32_t*>(base) + row_off[r] + g * sk;
+            w[r] = (valid[r] && QL_IN(bnd, si, q, 4)) ? __ldg(q) : 0u;
+        }
         return;
     }
     uint32_t bits[R][4];
@@ -130,9 +135,10 @@ __device__ __forceinline__ void exp_words(const void* base, int fmt, const int64
     for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            bits[r][j] = (valid[r] && 4 * g + j < num_kb)
-                             ? __float_as_uint(__ldg(static_cast<const float*>(base) + row_off[r] + (4 * g + j) * sk))
-                             : 0u;
+        {
+            const float* q = static_cast<const float*>(base) + row_off[r] + (4 * g + j) * sk;
+            bits[r][j] = (valid[r] && 4 * g + j < num_kb && QL_IN(bnd, si, q, 4)) ? __float_as_uint(__ldg(q)) : 0u;
+        }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         w[r] = 0;
@@ -357,12 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int q = 0; q < 4; ++q) va[q] = vala[q] && in;
 #pragma unroll
                             for (int i = 0; i < NB; ++i) vb[i] = valb[i] && in;
-                            exp_words<4>(p.sfa, 2, offa, va, kg0 + j, p.sak, num_kb, wa[j]);
-                            exp_words<NB>(p.sfb, 2, offb, vb, kg0 + j, p.sbk, num_kb, wb[j]);
+                            exp_words<4>(p.sfa, 2, offa, va, kg0 + j, p.sak, num_kb, wa[j], p.bnd, 0);
+                            exp_words<NB>(p.sfb, 2, offb, vb, kg0 + j, p.sbk, num_kb, wb[j], p.bnd, 1);
                         }
                     } else {
-                        exp_words<4>(p.sfa, p.fmt, offa, vala, kg0, p.sak, num_kb, wa[0]);
-                        exp_words<NB>(p.sfb, p.fmt, offb, valb, kg0, p.sbk, num_kb, wb[0]);
+                        exp_words<4>(p.sfa, p.fmt, offa, vala, kg0, p.sak, num_kb, wa[0], p.bnd, 0);
+                        exp_words<NB>(p.sfb, p.fmt, offb, valb, kg0, p.sbk, num_kb, wb[0], p.bnd, 1);
                     }
                     for (int j = 0; j < cnt; ++j) {
                         const uint32_t gj = g + j;
@@ -466,11 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             u.y = *reinterpret_cast<uint32_t*>(&h1);
                             u.z = *reinterpret_cast<uint32_t*>(&h2);
                             u.w = *reinterpret_cast<uint32_t*>(&h3);
-                            *reinterpret_cast<uint4*>(drow + c) = u;
+                            if (QL_IN(p.bnd, 2, drow + c, 16)) *reinterpret_cast<uint4*>(drow + c) = u;
                         } else {
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                if (c + e < p.n) drow[c + e] = __float2bfloat16_rn(acc[j + e]);
+                                if (c + e < p.n && QL_IN(p.bnd, 2, drow + c + e, 2)) drow[c + e] = __float2bfloat16_rn(acc[j + e]);
                         }
                     }
                 } else {
@@ -479,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < CPT; j += 4) {
                         const int64_t c = col0 + j;
                         if (vec_store && c + 4 <= p.n) {
+                            if (!QL_IN(p.bnd, 2, drow + c, 16)) continue;
                             float4 o = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
                             if (p.accumulate) {
                                 const float4 old = *reinterpret_cast<const float4*>(drow + c);
@@ -488,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                if (c + e < p.n) drow[c + e] = p.accumulate ? drow[c + e] + acc[j + e] : acc[j + e];
+                                if (c + e < p.n && QL_IN(p.bnd, 2, drow + c + e, 4))
+                                    drow[c + e] = p.accumulate ? drow[c + e] + acc[j + e] : acc[j + e];
                         }
                     }
                 }

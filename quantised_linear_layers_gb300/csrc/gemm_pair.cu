@@ -59,6 +59,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "common.cuh"
 #include "epilogue_tma.cuh"
 #include "gemm.cuh"
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int64_t row = m0 + lane + 32 * i;
-                            va[j][i] = (j < cnt && row < p.m) ? decode_scale(p.sfa, p.fmt, row * p.sam, kb0 + j, p.sak)
+                            va[j][i] = (j < cnt && row < p.m) ? decode_scale(p.sfa, p.fmt, row * p.sam, kb0 + j, p.sak, p.bnd, 0)
                                                               : 0.0f;
                         }
 #pragma unroll
@@ -286,11 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (j < cnt) {
                                 if constexpr (PER_ROW_B) {
                                     const int64_t col = n0 + lane + 32 * i;
-                                    if (col < p.n) v = decode_scale(p.sfb, p.fmt, col * p.sbn, kb0 + j, p.sbk);
+                                    if (col < p.n) v = decode_scale(p.sfb, p.fmt, col * p.sbn, kb0 + j, p.sbk, p.bnd, 1);
                                 } else {
                                     const int64_t r = n0 / 128 + lane;
                                     if (lane < (BN + 127) / 128 && r < nblocks_b)
-                                        v = decode_scale(p.sfb, p.fmt, r * p.sbn, kb0 + j, p.sbk);
+                                        v = decode_scale(p.sfb, p.fmt, r * p.sbn, kb0 + j, p.sbk, p.bnd, 1);
                                 }
                             }
                             vb[j][i] = v;
@@ -405,11 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             u.y = *reinterpret_cast<uint32_t*>(&h1);
                             u.z = *reinterpret_cast<uint32_t*>(&h2);
                             u.w = *reinterpret_cast<uint32_t*>(&h3);
-                            *reinterpret_cast<uint4*>(drow + c) = u;
+                            if (QL_IN(p.bnd, 2, drow + c, 16)) *reinterpret_cast<uint4*>(drow + c) = u;
                         } else {
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                if (c + e < p.n) drow[c + e] = __float2bfloat16_rn(acc[j + e]);
+                                if (c + e < p.n && QL_IN(p.bnd, 2, drow + c + e, 2)) drow[c + e] = __float2bfloat16_rn(acc[j + e]);
                         }
                     }
                 } else {
@@ -418,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < CPT; j += 4) {
                         const int64_t c = col0 + j;
                         if (vec_store && c + 4 <= p.n) {
+                            if (!QL_IN(p.bnd, 2, drow + c, 16)) continue;
                             float4 o = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
                             if (p.accumulate) {
                                 const float4 old = *reinterpret_cast<const float4*>(drow + c);
@@ -427,7 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                if (c + e < p.n) drow[c + e] = p.accumulate ? drow[c + e] + acc[j + e] : acc[j + e];
+                                if (c + e < p.n && QL_IN(p.bnd, 2, drow + c + e, 4))
+                                    drow[c + e] = p.accumulate ? drow[c + e] + acc[j + e] : acc[j + e];
                         }
                     }
                 }

@@ -10,6 +10,7 @@
 
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "common.cuh"
 
 namespace ql {
@@ -17,9 +18,15 @@ namespace ql {
 // Scale of row `row_off` (element offset of the row in the scale tensor) and
 // K block `kb`: an fp32 value (fmt 0/1) or one byte of a packed UE8M0 word
 // (fmt 2: four K blocks per int32, block kb in byte kb % 4), as 2^(e - 127).
-__device__ __forceinline__ float decode_scale(const void* base, int fmt, int64_t row_off, int kb, int64_t sk) {
-    if (fmt != 2) return __ldg(static_cast<const float*>(base) + row_off + kb * sk);
-    const uint32_t w = __ldg(static_cast<const uint32_t*>(base) + row_off + (kb >> 2) * sk);
+// In bounds-checked builds the read is checked against span `si` of `bnd`.
+__device__ __forceinline__ float decode_scale(const void* base, int fmt, int64_t row_off, int kb, int64_t sk,
+                                              const Bounds& bnd, int si) {
+    if (fmt != 2) {
+        const float* q = static_cast<const float*>(base) + row_off + kb * sk;
+        return QL_IN(bnd, si, q, 4) ? __ldg(q) : 0.0f;
+    }
+    const uint32_t* q = static_cast<const uint32_t*>(base) + row_off + (kb >> 2) * sk;
+    const uint32_t w = QL_IN(bnd, si, q, 4) ? __ldg(q) : 0u;
     const uint32_t e = (w >> (8 * (kb & 3))) & 0xFFu;
     return __uint_as_float(e ? (e << 23) : 0x00400000u);   // 2^(e-127)
 }

@@ -14,7 +14,9 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libqlinear.so")
+# QL_LIBRARY selects another build of the library (the bounds-checked
+# libqlinear_bounds.so, for instance); the default is the product build.
+LIB_PATH = os.environ.get("QL_LIBRARY") or os.path.join(_HERE, "libqlinear.so")
 
 QL_BF16, QL_F32 = 0, 1
 SF_FP32, SF_UE8M0, SF_PACKED_UE8M0 = 0, 1, 2
@@ -59,6 +61,8 @@ _SIGS = {
     "ql_set_gemm_path": [_int],
     "ql_test_stall_gemm_producer": [_int],
     "ql_device_status": [_vp],
+    "ql_device_status_detail": [_vp, _vp, _vp],
+    "ql_bounds_checked": [],
     "ql_status_string": [_int],
 }
 
