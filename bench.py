@@ -751,6 +751,25 @@ def run_workloads(dev, pk, reps):
             "tflops_step": round(3 * fl / step["us"] / 1e6, 1),
             "tflops_without_weight_casts": round(3 * fl / (step["us"] - part[0]["us"]) / 1e6, 1)}
         del w8
+    # the step's casts alone, as GB/s of their algorithmic bytes: W's dual
+    # block cast, X's and dY's dual per-token casts (one read, two E4M3 casts)
+    casts = {}
+
+    def _packed_words(rows, groups):
+        return rows * ((groups + 3) // 4) * 4
+
+    for name, f, byts in (
+            ("w_block_dual_4096x7168", lambda: ops.fp8_cast_per_block_dual(w, P),
+             4096 * 7168 * 3 + _packed_words(32, 56) + _packed_words(56, 32)),
+            ("x_dual_4096x7168", lambda: ops.fp8_cast_per_token_dual(x, P),
+             4096 * 7168 * 4 + _packed_words(4096, 56) + _packed_words(7168, 32)),
+            ("dy_dual_4096x4096", lambda: ops.fp8_cast_per_token_dual(dy, P),
+             4096 * 4096 * 4 + _packed_words(4096, 32) + _packed_words(4096, 32))):
+        r = stats_us(time_eager(f, reps, flush))
+        casts[name] = {**r, "bytes": byts, "gbs": round(byts / r["us"] / 1e3, 1),
+                       "frac_hbm": round(byts / r["us"] / 1e3 / pk["hbm_gbs"], 3)}
+        launches += reps
+    out["linear_step_casts_cold_l2"] = casts
     # the weight gradient with transposed casts against MN-major operands
     t_tr = stats_us(time_eager(lambda: linear.wgrad(dy, x, P, mn_major=False), reps, flush))
     t_mn = stats_us(time_eager(lambda: linear.wgrad(dy, x, P, mn_major=True), reps, flush))

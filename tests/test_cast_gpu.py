@@ -365,7 +365,8 @@ def test_cast_column_major_into_view(orc, ops, fmt, feats):
 @pytest.mark.parametrize("fmt,recip", [(0, False), (0, True), (1, False), (2, False)],
                          ids=["fp32", "fp32-recip", "ue8m0", "packed"])
 @pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
-@pytest.mark.parametrize("shape", [(4096, 1024), (300, 200), (300, 336), (129, 7168), (1, 24), (640, 4096)],
+@pytest.mark.parametrize("shape", [(4096, 1024), (300, 200), (300, 336), (129, 7168), (1, 24), (640, 4096),
+                                   (4096, 7168), (3000, 4100)],
                          ids=lambda s: f"{s[0]}x{s[1]}")
 def test_cast_dual_per_token(orc, ops, dtype, fmt, recip, shape):
     """fp8_cast_per_token_dual: from one read of x [T, C], the per-token cast of
@@ -385,3 +386,21 @@ def test_cast_dual_per_token(orc, ops, dtype, fmt, recip, shape):
             assert np.array_equal(g, want)
         else:
             assert np.array_equal(g.view(np.uint32), np.ascontiguousarray(want).view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [0, 2], ids=["fp32", "packed"])
+def test_cast_dual_unaligned_rows_many_tiles(orc, ops, fmt):
+    """A view whose rows do not start on 16-byte boundaries (no prefetch path)
+    with more tiles than resident CTAs: bit for bit the oracle's two casts."""
+    base = syn.randn_row_exp(2600, 4101, dtype=torch.bfloat16)
+    x = base[:, 1:4100]
+    xg = base.cuda()[:, 1:4100]             # row stride 4101 elements, offset one element
+    assert xg.stride(0) == 4101
+    qr, sr, qc, sc = ops.fp8_cast_per_token_dual(xg, fmt)
+    assert ops.device_status() == 0
+    oq, os_ = orc.cast_per_token(np_input(x), 128, fmt)
+    oqt, ost = orc.cast_per_token(np_input(x).T, 128, fmt)
+    assert np.array_equal(np_bytes(qr), oq) and np.array_equal(np_bytes(qc).T, oqt)
+    for got, want in ((sr, os_), (sc, ost)):
+        g = np.ascontiguousarray(np_sf(got))
+        assert np.array_equal(g.view(np.uint32), np.ascontiguousarray(want).view(np.uint32))
