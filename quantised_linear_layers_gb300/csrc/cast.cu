@@ -1114,16 +1114,194 @@ constexpr int kThreads = 16 * (128 / kRowsPerThread);      // 16 threads per row
 constexpr int kWarps = kThreads / 32;
 }  // namespace dual
 
+// Input value e (< 8) of the thread's it-th row from its raw words.
+template <typename T>
+__device__ __forceinline__ float dual_val(const uint32_t* raw, int it, int e) {
+    constexpr int WPG = (8 * static_cast<int>(sizeof(T))) / 4;      // words per 8 elements
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t w = raw[it * WPG + e / 2];
+        return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    } else {
+        return __uint_as_float(raw[it * WPG + e]);
+    }
+}
+
+// First half of a tile: the column maxima over this warp's rows into red[warp]
+// and the maxima of the thread's rows (one half-warp per row; non-negative
+// floats order as their bits).
+template <typename T>
+__device__ __forceinline__ void dual_maxima(const uint32_t* raw, float (*red)[128], int a0, int lane, int warp,
+                                            uint32_t (&rmax)[dual::kRowsPerThread]) {
+    constexpr int NIT = dual::kRowsPerThread;
+    const uint32_t half = 0xFFFFu << (lane & 16);
+    if constexpr (sizeof(T) == 2) {
+        // bf16: maxima of |x| on pairs of columns (max.bf16x2 is exact and,
+        // like fmaxf, returns the other operand for a NaN; an all-NaN pair
+        // reaches red as NaN, which the column reduction's fmaxf from 0 drops)
+        uint32_t ab[NIT][4];
+#pragma unroll
+        for (int it = 0; it < NIT; ++it)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) ab[it][w] = raw[it * 4 + w] & 0x7FFF7FFFu;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t c = bf16x2_max(bf16x2_max(ab[0][w], ab[1][w]), bf16x2_max(ab[2][w], ab[3][w]));
+            c = bf16x2_max(c, __shfl_xor_sync(0xffffffffu, c, 16));
+            if (lane < 16) {
+                red[warp][a0 + 2 * w] = __uint_as_float(c << 16);
+                red[warp][a0 + 2 * w + 1] = __uint_as_float(c & 0xFFFF0000u);
+            }
+        }
+        static_assert(dual::kRowsPerThread == 4, "four rows per thread");
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+            const uint32_t r = bf16x2_max(bf16x2_max(ab[it][0], ab[it][1]), bf16x2_max(ab[it][2], ab[it][3]));
+            const float a = fmaxf(fmaxf(0.0f, __uint_as_float(r << 16)), __uint_as_float(r & 0xFFFF0000u));
+            rmax[it] = __reduce_max_sync(half, __float_as_uint(a));
+        }
+    } else {
+        float cmax[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float a = 0.0f;
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) a = fmaxf(a, fabsf(dual_val<T>(raw, it, e)));
+            cmax[e] = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+        }
+        if (lane < 16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) red[warp][a0 + e] = cmax[e];
+        }
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+            float a = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(dual_val<T>(raw, it, e)));
+            rmax[it] = __reduce_max_sync(half, __float_as_uint(a));
+        }
+    }
+}
+
+// Output pointers and strides of the dual cast.
+struct DualOut {
+    uint8_t* qr;
+    int64_t ldr;
+    void* sfr;
+    int64_t srm, srg;
+    uint8_t* qc;
+    int64_t ldc;
+    void* sfc;
+    int64_t scn, scg;
+    int vec_out;
+};
+
+// Second half of a tile (after the barrier that completes red): the row and
+// column scales, one thread per row and per column, then the E4M3 bytes of
+// both casts, 8 per row per cast (16 threads cover 128 contiguous bytes).
+// last_bc / last_br: the tile is in the last column / row block (packed words
+// there are completed with zero bytes). Contains one __syncthreads.
+template <typename T, int FMT, bool RECIP>
+__device__ __forceinline__ void dual_emit(const uint32_t* raw, const uint32_t (&rmax)[dual::kRowsPerThread],
+                                          float (*red)[128], float* fcol, int64_t br, int64_t bc, bool last_br,
+                                          bool last_bc, int64_t m, int64_t n, const DualOut& o, const Bounds& bnd) {
+    constexpr int NIT = dual::kRowsPerThread;
+    constexpr int RS = 128 / NIT;       // rows between a thread's rows
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int64_t r0 = br * 128, c0 = bc * 128;
+    const int a0 = (tid % 16) * 8;
+    const int64_t gc = c0 + a0;
+    // lane i (i < NIT) of each half-warp makes the scale of its i-th row
+    const int my_it = lane & 15;
+    uint32_t mine = rmax[0];
+#pragma unroll
+    for (int it = 1; it < NIT; ++it)
+        if (my_it == it) mine = rmax[it];
+    float s_r, f_r;
+    uint32_t e_r;
+    group_scale<FMT, RECIP>(__uint_as_float(mine), s_r, f_r, e_r);
+    if (my_it < NIT) {
+        const int64_t gr = r0 + my_it * RS + tid / 16;
+        if (gr < m) {
+            if constexpr (FMT != kSfPacked) {
+                float* sp = static_cast<float*>(o.sfr) + gr * o.srm + bc * o.srg;
+                if (QL_IN(bnd, 2, sp, 4)) *sp = s_r;
+            } else {
+                uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(o.sfr) + gr * o.srm + (bc / 4) * o.srg);
+                if (QL_IN(bnd, 2, word, 4)) {
+                    word[bc % 4] = static_cast<uint8_t>(e_r);
+                    if (last_bc)
+                        for (int64_t z = bc % 4 + 1; z < 4; ++z) word[z] = 0;
+                }
+            }
+        }
+    }
+    float frow[NIT];
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) frow[it] = __shfl_sync(0xffffffffu, f_r, (lane & 16) + it);
+    if (tid < 128) {
+        float a = 0.0f;
+#pragma unroll
+        for (int w = 0; w < dual::kWarps; ++w) a = fmaxf(a, red[w][tid]);
+        float s_c, f_c;
+        uint32_t e_c;
+        group_scale<FMT, RECIP>(a, s_c, f_c, e_c);
+        fcol[tid] = f_c;
+        const int64_t col = c0 + tid;
+        if (col < n) {
+            if constexpr (FMT != kSfPacked) {
+                float* sp = static_cast<float*>(o.sfc) + col * o.scn + br * o.scg;
+                if (QL_IN(bnd, 4, sp, 4)) *sp = s_c;
+            } else {
+                uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(o.sfc) + col * o.scn + (br / 4) * o.scg);
+                if (QL_IN(bnd, 4, word, 4)) {
+                    word[br % 4] = static_cast<uint8_t>(e_c);
+                    if (last_br)
+                        for (int64_t z = br % 4 + 1; z < 4; ++z) word[z] = 0;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    float fc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fc[e] = fcol[a0 + e];
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int64_t gr = r0 + it * RS + tid / 16;
+        if (gr >= m) continue;
+        auto v = [&](int e) { return dual_val<T>(raw, it, e); };
+        const uint32_t r_lo = quant4(v(0), v(1), v(2), v(3), frow[it]);
+        const uint32_t r_hi = quant4(v(4), v(5), v(6), v(7), frow[it]);
+        const uint32_t c_lo = e4m3x2(__fmul_rn(v(0), fc[0]), __fmul_rn(v(1), fc[1])) |
+                              (e4m3x2(__fmul_rn(v(2), fc[2]), __fmul_rn(v(3), fc[3])) << 16);
+        const uint32_t c_hi = e4m3x2(__fmul_rn(v(4), fc[4]), __fmul_rn(v(5), fc[5])) |
+                              (e4m3x2(__fmul_rn(v(6), fc[6]), __fmul_rn(v(7), fc[7])) << 16);
+        uint8_t* dr = o.qr + gr * o.ldr + gc;
+        uint8_t* dc = o.qc + gr * o.ldc + gc;
+        if (o.vec_out && gc + 8 <= n) {
+            if (QL_IN(bnd, 1, dr, 8)) *reinterpret_cast<uint2*>(dr) = make_uint2(r_lo, r_hi);
+            if (QL_IN(bnd, 3, dc, 8)) *reinterpret_cast<uint2*>(dc) = make_uint2(c_lo, c_hi);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (gc + e < n) {
+                    if (QL_IN(bnd, 1, dr + e, 1)) dr[e] = static_cast<uint8_t>((e < 4 ? r_lo : r_hi) >> (8 * (e & 3)));
+                    if (QL_IN(bnd, 3, dc + e, 1)) dc[e] = static_cast<uint8_t>((e < 4 ? c_lo : c_hi) >> (8 * (e & 3)));
+                }
+            }
+        }
+    }
+}
+
+// One CTA per tile; each thread loads its four rows' 8 elements from x.
 template <typename T, int FMT, bool RECIP>
 __global__ void __launch_bounds__(dual::kThreads, 2)
-    cast_dual_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx, uint8_t* __restrict__ qr,
-                     int64_t ldr, void* __restrict__ sfr, int64_t srm, int64_t srg, uint8_t* __restrict__ qc,
-                     int64_t ldc, void* __restrict__ sfc, int64_t scn, int64_t scg, int vec_in, int vec_out,
+    cast_dual_kernel(const T* __restrict__ x, int64_t m, int64_t n, int64_t ldx, const DualOut o, int vec_in,
                      const Bounds bnd) {
     pdl_wait_prior();           // the previous kernel's writes are complete and visible
     constexpr int WPG = (8 * static_cast<int>(sizeof(T))) / 4;      // words per 8 elements
     constexpr int NIT = dual::kRowsPerThread;
-    constexpr int RS = 128 / NIT;       // rows between a thread's rows
+    constexpr int RS = 128 / NIT;
     __shared__ float red[dual::kWarps][128];   // per-warp column maxima
     __shared__ float fcol[128];         // column factors
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1152,122 +1330,11 @@ __global__ void __launch_bounds__(dual::kThreads, 2)
             for (int w = 0; w < WPG; ++w) raw[it * WPG + w] = tmp.w[w];
         }
     }
-    auto val = [&](int it, int e) -> float {
-        if constexpr (sizeof(T) == 2) {
-            const uint32_t w = raw[it * WPG + e / 2];
-            return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
-        } else {
-            return __uint_as_float(raw[it * WPG + e]);
-        }
-    };
-
-    // column maxima: over this thread's rows, the lane 16 apart, the warps
-    float cmax[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        float a = 0.0f;
-#pragma unroll
-        for (int it = 0; it < NIT; ++it) a = fmaxf(a, fabsf(val(it, e)));
-        cmax[e] = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
-    }
-    if (lane < 16) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) red[warp][a0 + e] = cmax[e];
-    }
-    // row maxima: a row's 16 chunks are one half-warp (non-negative floats
-    // order as their bits)
-    const uint32_t half = 0xFFFFu << (lane & 16);
     uint32_t rmax[NIT];
-#pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-        float a = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(val(it, e)));
-        rmax[it] = __reduce_max_sync(half, __float_as_uint(a));
-    }
-    // lane i (i < NIT) of each half-warp makes the scale of its i-th row
-    const int my_it = lane & 15;
-    uint32_t mine = rmax[0];
-#pragma unroll
-    for (int it = 1; it < NIT; ++it)
-        if (my_it == it) mine = rmax[it];
-    float s_r, f_r;
-    uint32_t e_r;
-    group_scale<FMT, RECIP>(__uint_as_float(mine), s_r, f_r, e_r);
-    if (my_it < NIT) {
-        const int64_t gr = r0 + my_it * RS + tid / 16;
-        if (gr < m) {
-            if constexpr (FMT != kSfPacked) {
-                float* sp = static_cast<float*>(sfr) + gr * srm + bc * srg;
-                if (QL_IN(bnd, 2, sp, 4)) *sp = s_r;
-            } else {
-                uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sfr) + gr * srm + (bc / 4) * srg);
-                if (QL_IN(bnd, 2, word, 4)) {
-                    word[bc % 4] = static_cast<uint8_t>(e_r);
-                    if (bc == static_cast<int64_t>(gridDim.x) - 1)
-                        for (int64_t z = bc % 4 + 1; z < 4; ++z) word[z] = 0;
-                }
-            }
-        }
-    }
-    float frow[NIT];
-#pragma unroll
-    for (int it = 0; it < NIT; ++it) frow[it] = __shfl_sync(0xffffffffu, f_r, (lane & 16) + it);
+    dual_maxima<T>(raw, red, a0, lane, warp, rmax);
     __syncthreads();
-    if (tid < 128) {
-        float a = red[0][tid];
-#pragma unroll
-        for (int w = 1; w < dual::kWarps; ++w) a = fmaxf(a, red[w][tid]);
-        float s_c, f_c;
-        uint32_t e_c;
-        group_scale<FMT, RECIP>(a, s_c, f_c, e_c);
-        fcol[tid] = f_c;
-        const int64_t col = c0 + tid;
-        if (col < n) {
-            if constexpr (FMT != kSfPacked) {
-                float* sp = static_cast<float*>(sfc) + col * scn + br * scg;
-                if (QL_IN(bnd, 4, sp, 4)) *sp = s_c;
-            } else {
-                uint8_t* word = reinterpret_cast<uint8_t*>(static_cast<int32_t*>(sfc) + col * scn + (br / 4) * scg);
-                if (QL_IN(bnd, 4, word, 4)) {
-                    word[br % 4] = static_cast<uint8_t>(e_c);
-                    if (br == static_cast<int64_t>(gridDim.y) - 1)
-                        for (int64_t z = br % 4 + 1; z < 4; ++z) word[z] = 0;
-                }
-            }
-        }
-    }
-    __syncthreads();
-    float fc[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) fc[e] = fcol[a0 + e];
-
-    // E4M3 bytes of both casts, 8 per row per cast
-#pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-        const int64_t gr = r0 + it * RS + tid / 16;
-        if (gr >= m) continue;
-        const uint32_t r_lo = quant4(val(it, 0), val(it, 1), val(it, 2), val(it, 3), frow[it]);
-        const uint32_t r_hi = quant4(val(it, 4), val(it, 5), val(it, 6), val(it, 7), frow[it]);
-        const uint32_t c_lo = e4m3x2(__fmul_rn(val(it, 0), fc[0]), __fmul_rn(val(it, 1), fc[1])) |
-                              (e4m3x2(__fmul_rn(val(it, 2), fc[2]), __fmul_rn(val(it, 3), fc[3])) << 16);
-        const uint32_t c_hi = e4m3x2(__fmul_rn(val(it, 4), fc[4]), __fmul_rn(val(it, 5), fc[5])) |
-                              (e4m3x2(__fmul_rn(val(it, 6), fc[6]), __fmul_rn(val(it, 7), fc[7])) << 16);
-        uint8_t* dr = qr + gr * ldr + gc;
-        uint8_t* dc = qc + gr * ldc + gc;
-        if (vec_out && gc + 8 <= n) {
-            if (QL_IN(bnd, 1, dr, 8)) *reinterpret_cast<uint2*>(dr) = make_uint2(r_lo, r_hi);
-            if (QL_IN(bnd, 3, dc, 8)) *reinterpret_cast<uint2*>(dc) = make_uint2(c_lo, c_hi);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (gc + e < n) {
-                    if (QL_IN(bnd, 1, dr + e, 1)) dr[e] = static_cast<uint8_t>((e < 4 ? r_lo : r_hi) >> (8 * (e & 3)));
-                    if (QL_IN(bnd, 3, dc + e, 1)) dc[e] = static_cast<uint8_t>((e < 4 ? c_lo : c_hi) >> (8 * (e & 3)));
-                }
-            }
-        }
-    }
+    dual_emit<T, FMT, RECIP>(raw, rmax, red, fcol, br, bc, br == static_cast<int64_t>(gridDim.y) - 1,
+                             bc == static_cast<int64_t>(gridDim.x) - 1, m, n, o, bnd);
     // this CTA's work is done: the next kernel of the stream may be scheduled
     pdl_launch_dependents();
 }
@@ -1469,9 +1536,9 @@ cudaError_t launch_dual_t(const CastDualArgs& a, cudaStream_t st) {
     const int vec_in = aligned16(x) && (a.sxm * static_cast<int64_t>(sizeof(T))) % 16 == 0;
     const int vec_out = (reinterpret_cast<uintptr_t>(a.qr) % 8 == 0) && (reinterpret_cast<uintptr_t>(a.qc) % 8 == 0) &&
                         a.ldr % 8 == 0 && a.ldc % 8 == 0;
+    const DualOut o{a.qr, a.ldr, a.sfr, a.srm, a.srg, a.qc, a.ldc, a.sfc, a.scn, a.scg, vec_out};
     dim3 grid(static_cast<unsigned>((a.n + 127) / 128), static_cast<unsigned>((a.m + 127) / 128));
-    return launch_pdl(cast_dual_kernel<T, FMT, RECIP>, grid, dim3(dual::kThreads), 0, st, x, a.m, a.n, a.sxm, a.qr,
-                      a.ldr, a.sfr, a.srm, a.srg, a.qc, a.ldc, a.sfc, a.scn, a.scg, vec_in, vec_out,
+    return launch_pdl(cast_dual_kernel<T, FMT, RECIP>, grid, dim3(dual::kThreads), 0, st, x, a.m, a.n, a.sxm, o, vec_in,
                       dual_bounds(a, sizeof(T), FMT));
 }
 

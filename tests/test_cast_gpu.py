@@ -366,12 +366,14 @@ def test_cast_column_major_into_view(orc, ops, fmt, feats):
                          ids=["fp32", "fp32-recip", "ue8m0", "packed"])
 @pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f32"])
 @pytest.mark.parametrize("shape", [(4096, 1024), (300, 200), (300, 336), (129, 7168), (1, 24), (640, 4096),
-                                   (4096, 7168), (3000, 4100)],
+                                   (4096, 7168), (3000, 4100), (3000, 4104)],
                          ids=lambda s: f"{s[0]}x{s[1]}")
 def test_cast_dual_per_token(orc, ops, dtype, fmt, recip, shape):
     """fp8_cast_per_token_dual: from one read of x [T, C], the per-token cast of
     x and that of x^T (kept in x's layout), each bit for bit the oracle's cast,
-    with partial tiles in both directions, an all-zero group and huge values."""
+    with partial tiles in both directions, an all-zero group and huge values
+    (3000 x 4104: ragged tiles with 16-byte aligned bf16 rows; 3000 x 4100:
+    rows off that alignment, read element by element)."""
     t_rows, feats = shape
     x = make_x(t_rows, feats, dtype, 128, huge=t_rows > 1)
     qr, sr, qc, sc = ops.fp8_cast_per_token_dual(x.cuda(), fmt, recip)
