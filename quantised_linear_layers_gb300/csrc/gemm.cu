@@ -133,7 +133,10 @@ constexpr int kThreads = 384;
 constexpr int kMathThreads = 256;
 constexpr int BM = 128;
 constexpr int BK = 128;         // K block = scale granularity
-constexpr int kScaleSlots = 8;
+// Scale slots: with one B scale per 128 columns, a slot holds one loader run
+// of 4 K blocks and the math warps wait on it and release it once per run, one
+// arrive per warp; with a B scale per column (wgrad) a slot holds one K block
+// and every math thread releases it.
 
 // OUT_BYTES: element size of a D that leaves through shared memory and TMA
 // tile stores (2: bf16, 4: fp32; 0: stored directly), one 2 KB buffer of 32
@@ -148,13 +151,18 @@ struct Cfg {
     static constexpr int kTmemColsUsed = kTmemStages * BN;
     static constexpr int kTmemCols = kTmemColsUsed <= 32 ? 32 : (kTmemColsUsed <= 64 ? 64 : (kTmemColsUsed <= 128 ? 128 : (kTmemColsUsed <= 256 ? 256 : 512)));
     static constexpr int kSbPerSlot = PER_ROW_B ? BN : 4;
-    static constexpr int kSlotFloats = BM + kSbPerSlot;
+    static constexpr int kSlotFloats = BM + kSbPerSlot;      // one K block's scales
+    static constexpr int kRun = PER_ROW_B ? 2 : 4;           // K blocks per loader run
+    static constexpr int kSlotKb = PER_ROW_B ? 1 : kRun;     // K blocks per slot
+    static constexpr int kScaleSlots = PER_ROW_B ? 8 : 4;
+    static constexpr int kRunFloats = kSlotKb * kSlotFloats;
+    static constexpr uint32_t kRelease = PER_ROW_B ? kMathThreads : kMathThreads / 32;   // arrives per release
     static constexpr int kColsPerThread = BN / 2;
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kStageA;
     static constexpr int kOffScale = kOffB + kStages * kStageB;
-    static constexpr int kOffBar = kOffScale + kScaleSlots * kSlotFloats * 4;
+    static constexpr int kOffBar = kOffScale + kScaleSlots * kRunFloats * 4;
     static constexpr int kNumBars = 2 * kStages + 2 * kTmemStages + 2 * kScaleSlots + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr bool kStageOut = OUT_BYTES != 0 && (BN / 2) % (64 / (OUT_BYTES == 0 ? 1 : OUT_BYTES)) == 0;
@@ -192,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* tfull = empty + C::kStages;
     uint64_t* tempty = tfull + C::kTmemStages;
     uint64_t* sfull = tempty + C::kTmemStages;
-    uint64_t* sempty = sfull + kScaleSlots;
-    uint64_t* done_bar = sempty + kScaleSlots;
+    uint64_t* sempty = sfull + C::kScaleSlots;
+    uint64_t* done_bar = sempty + C::kScaleSlots;
     uint32_t* tmem_base_sm = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -202,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int s = 0; s < C::kTmemStages; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], kMathThreads); }
-        for (int s = 0; s < kScaleSlots; ++s) { mbar_init(&sfull[s], 32); mbar_init(&sempty[s], kMathThreads); }
+        for (int s = 0; s < C::kTmemStages; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], C::kRelease); }
+        for (int s = 0; s < C::kScaleSlots; ++s) { mbar_init(&sfull[s], 32); mbar_init(&sempty[s], C::kRelease); }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -301,11 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- scale loaders ----------------
             // Warps 2 and 3 take alternate runs of K blocks (four, or two when B
             // has a scale per row); all loads of a run are issued before any
-            // is stored, so a run costs one memory round trip.
-            constexpr int kRun = PER_ROW_B ? 2 : 4;
+            // is stored, so a run costs one memory round trip. A run fills one
+            // slot (kSlotKb == kRun) or one slot per K block.
+            constexpr int kRun = C::kRun;
             constexpr int kSbLoads = PER_ROW_B ? BN / 32 : 1;
             const uint32_t mine = static_cast<uint32_t>(warp - 2);
-            uint32_t g = 0, run = 0;
+            uint32_t run = 0, g = 0;
             bool ok = true;
             const int64_t nblocks_b = (p.n + 127) / 128;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -342,11 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             vb[j][i] = v;
                         }
                     }
-                    for (int j = 0; j < cnt; ++j) {
-                        const uint32_t gj = g + j;
-                        const uint32_t slot = gj % kScaleSlots, ph = (gj / kScaleSlots) & 1u;
-                        if (!warp_wait(&sempty[slot], ph ^ 1u, ctl)) { ok = false; break; }
-                        float* dst = sScale + slot * C::kSlotFloats;
+#pragma unroll
+                    for (int j = 0; j < kRun; ++j) {
+                        if (j >= cnt) break;
+                        // slot of this K block: the run's (per-run slots) or its own
+                        const uint32_t u = C::kSlotKb == 1 ? g + j : run;
+                        const uint32_t slot = u % C::kScaleSlots, ph = (u / C::kScaleSlots) & 1u;
+                        if ((C::kSlotKb == 1 || j == 0) && !warp_wait(&sempty[slot], ph ^ 1u, ctl)) { ok = false; break; }
+                        float* dst = sScale + slot * C::kRunFloats + (C::kSlotKb == 1 ? 0 : j) * C::kSlotFloats;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = va[j][i];
                         if constexpr (PER_ROW_B) {
@@ -355,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
                             if (lane < (BN + 127) / 128) dst[BM + lane] = vb[j][0];
                         }
-                        mbar_arrive(&sfull[slot]);
+                        if (C::kSlotKb == 1 || j == cnt - 1) mbar_arrive(&sfull[slot]);
                     }
                     if (!ok) break;
                     g += cnt;
@@ -372,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const bool vec_store = p.vec_store != 0;
         float acc[CPT];
-        uint32_t g = 0;
+        uint32_t g = 0, run = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             int mb, nb;
@@ -384,10 +396,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
             for (int kb = 0; kb < num_kb; ++kb, ++g) {
-                const uint32_t slot = g % kScaleSlots, sph = (g / kScaleSlots) & 1u;
+                // the slot of this K block: its loader run's, or its own
+                const int jr = C::kSlotKb == 1 ? 0 : kb % C::kSlotKb;
+                const uint32_t u = C::kSlotKb == 1 ? g : run;
+                const uint32_t slot = u % C::kScaleSlots, sph = (u / C::kScaleSlots) & 1u;
+                const bool slot_end = C::kSlotKb == 1 || jr == C::kSlotKb - 1 || kb == num_kb - 1;
                 const uint32_t ts = g % C::kTmemStages, tph = (g / C::kTmemStages) & 1u;
-                if (!warp_wait(&sfull[slot], sph, ctl)) { ok = false; break; }
-                const float* src = sScale + slot * C::kSlotFloats;
+                if (jr == 0 && !warp_wait(&sfull[slot], sph, ctl)) { ok = false; break; }
+                const float* src = sScale + slot * C::kRunFloats + jr * C::kSlotFloats;
                 const float sa = src[r_local];
                 if (!warp_wait(&tfull[ts], tph, ctl)) { ok = false; break; }
                 tc_fence_after_sync();
@@ -405,12 +421,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_load_cols<U>(tcol + c0, v);
                         if (c0 + U == CPT) {              // last read of this stage
                             tc_fence_before_sync();
-                            mbar_arrive(&tempty[ts]);
+                            __syncwarp();
+                            mbar_arrive_lane0(&tempty[ts], lane);
                         }
 #pragma unroll
                         for (int j = 0; j < U; ++j) acc[c0 + j] = fmaf(__uint_as_float(v[j]), sab, acc[c0 + j]);
                     }
-                    mbar_arrive(&sempty[slot]);
+                    if (slot_end) {
+                        __syncwarp();
+                        mbar_arrive_lane0(&sempty[slot], lane);
+                        ++run;
+                    }
                 } else {
                     // a scale per column: (sa * sb) and the FMA, two elements
                     // per packed f32x2 instruction (half the instructions of

@@ -61,6 +61,11 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&v)[N])
     tmem_wait_ld(v);
 }
 
+// One arrive on `bar` for the whole (converged) warp, by its lane 0.
+__device__ __forceinline__ void mbar_arrive_lane0(uint64_t* bar, int lane) {
+    if (lane == 0) mbar_arrive(bar);
+}
+
 // Bounded wait whose outcome is the same for every lane of the warp (the
 // .sync.aligned tensor-memory loads that follow need a converged warp).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
