@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued = 0;                         // stages this CTA's producer issued
 
     if (warp < 4) {
-        regs_dealloc<104>();  // 128 x 104 + 256 x 200 = 384 x 168 registers
+        regs_dealloc<136>();  // 128 x 136 + 256 x 184 = 384 x 168 registers
         if (warp == 0) {
             // ---------------- TMA producer (both CTAs) ----------------
             if (elect_one()) {
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        regs_alloc<200>();
+        regs_alloc<184>();
         // ---------------- epilogue (both CTAs): 128 rows x 256 columns ----------------
         constexpr int CPT = BN / 2;
         const int wg = (warp - 4) >> 2;
