@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int num_groups = (num_kb + 3) / 4;
 
     if (warp < 4) {
-        regs_dealloc<104>();  // 128 x 104 + 256 x 200 = 384 x 168 registers
+        regs_dealloc<136>();  // 128 x 136 + 256 x 184 = 384 x 168 registers
         if (warp == 0) {
             if (elect_one()) {
                 uint32_t it = 0;
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        regs_alloc<200>();
+        regs_alloc<184>();
         // ---------------- epilogue warpgroups ----------------
         constexpr int CPT = C::kColsPerThread;
         constexpr int U = CPT < 32 ? CPT : 32;
