@@ -399,7 +399,10 @@ size_t ql_gemm_workspace_size(int64_t m, int64_t n, int64_t k);
  * Knobs ("DeepGEMM Essentials" Part 15: get_num_sms / set_num_sms).
  * The GEMM's persistent grid uses at most this many SMs (default: all SMs of
  * the current device). ql_set_num_sms(n <= 0) restores the default.
- * The setting is process-wide.
+ * The budget also decides whether a GEMM with few output tiles splits its K
+ * blocks over a cluster, and over how many CTAs: that changes the grouping in
+ * which fp32 partial sums are added, so results may differ in the last bit
+ * of the output (within the GEMM tolerance). The setting is process-wide.
  * ------------------------------------------------------------------------- */
 ql_status ql_set_num_sms(int num_sms);
 int ql_get_num_sms(void);
@@ -417,13 +420,17 @@ ql_status ql_set_gemm_block_n(int block_n);
  * across a thread-block cluster when that fills the SMs, else on CTA pairs
  * while there is a tile for every other pair, else on single SMs. With
  * QL_SF_FP32 scales (and with path 1) the partial product of every 128-wide
- * K block is promoted on the CUDA cores of one SM per tile. 1 forces the
+ * K block is promoted on the CUDA cores: of one SM per tile, or, for a plain
+ * GEMM with bf16 output whose 128 x 128 tiles are too few to occupy the SMs
+ * (small M), of a cluster of 2 or 4 CTAs that split the tile's K blocks and
+ * sum their fp32 partials through distributed shared memory. 1 forces the
  * CUDA-core promotion path, 5 runs it on CTA pairs (256 x 256 tiles; plain
- * GEMMs only, measured no faster than one SM per tile) and 6 forces the
- * single-SM kernel; 2 forces the single-SM block-scaled kernel,
- * 3 the block-scaled CTA-pair kernel and 4 the cluster split-K kernel where
- * it applies (2-4 ignored for QL_SF_FP32). All give results within the GEMM
- * tolerance of each other. Process-wide; for tuning and tests. */
+ * GEMMs only, measured no faster than one SM per tile), 6 forces the
+ * single-SM kernel and 7 the cluster split-K form where it applies; 2 forces
+ * the single-SM block-scaled kernel, 3 the block-scaled CTA-pair kernel and 4
+ * the block-scaled cluster split-K kernel where it applies (2-4 ignored for
+ * QL_SF_FP32). All give results within the GEMM tolerance of each other.
+ * Process-wide; for tuning and tests. */
 ql_status ql_set_gemm_path(int path);
 
 /* Time limit of every bounded wait inside the GEMM kernel, in milliseconds

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqlinear.so")
-SOURCES = ["api.cu", "cast.cu", "gemm.cu", "gemm_mx.cu", "gemm_mx2.cu", "gemm_mx_sk.cu", "gemm_pair.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "cast.cu", "gemm.cu", "gemm_mx.cu", "gemm_mx2.cu", "gemm_mx_sk.cu", "gemm_pair.cu", "gemm_prom_sk.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

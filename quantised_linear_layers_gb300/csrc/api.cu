@@ -584,7 +584,7 @@ ql_status ql_set_gemm_block_n(int block_n) {
 }
 
 ql_status ql_set_gemm_path(int path) {
-    if (path < 0 || path > 6) return QL_ERR_INVALID_ARG;
+    if (path < 0 || path > 7) return QL_ERR_INVALID_ARG;
     g_gemm_path.store(path);
     return QL_OK;
 }

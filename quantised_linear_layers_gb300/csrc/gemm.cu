@@ -639,8 +639,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
     // CUDA-core promotion (fp32 scales, or forced): on one SM per tile; path 5
     // runs it on CTA pairs (256 x 256 tiles), which measured no faster (its two
     // accumulator stages leave the promotion hand-off exposed), 6 forces the
-    // single-SM kernel.
-    const bool promote = !ue8m0 || L.path == 1 || L.path == 5 || L.path == 6;
+    // single-SM kernel, 7 the split-K cluster form below.
+    const bool promote = !ue8m0 || L.path == 1 || L.path == 5 || L.path == 6 || L.path == 7;
     if (promote && !grouped && !L.out_fp8 && L.path == 5) return launch_gemm_pair(L, p, st, num_sms);
     if (L.a_mn || L.b_mn) {
         // MN-major operands: one 128-byte swizzle atom of M / N per CTA, so
@@ -662,6 +662,12 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
             return launch_gemm_mx(L, p, 256, st, num_sms);
         }
         return launch_t<256, false, false, true>(L, p, st, num_sms);
+    }
+    // CUDA-core promotion with too few 128 x 128 tiles to occupy the SMs (small
+    // M): split-K over a cluster (path 7 forces it where a split applies)
+    if (promote && !grouped && !L.out_f32 && (L.path == 7 || (L.path == 0 && L.block_n == 0))) {
+        const int split_p = choose_split_k(L.m, L.n, L.k, num_sms);
+        if (split_p >= 2) return launch_gemm_prom_sk(L, p, split_p, st);
     }
     if (ue8m0 && L.path == 3 && !grouped) return launch_gemm_mx2(L, p, st, num_sms);
     const int split = (ue8m0 && !grouped && !L.out_f32) ? choose_split_k(L.m, L.n, L.k, num_sms) : 1;

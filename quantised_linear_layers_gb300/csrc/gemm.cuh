@@ -67,7 +67,8 @@ struct GemmLaunch {
     int path;                 // 0 = auto, 1 = CUDA-core promotion, 2 = block-scaled MMA on one SM,
                               // 3 = block-scaled MMA on CTA pairs, 4 = split-K over a cluster
                               // (3 and 4: UE8M0 formats only), 5 = CUDA-core promotion on
-                              // CTA pairs, 6 = CUDA-core promotion on one SM
+                              // CTA pairs, 6 = CUDA-core promotion on one SM, 7 = CUDA-core
+                              // promotion split-K over a cluster
     uint32_t* dev_status;
     uint64_t wait_limit_ns;
     int stall_producer;
@@ -160,6 +161,9 @@ cudaError_t launch_gemm_pair(const GemmLaunch& L, const GemmParams& p, cudaStrea
 // size for the shape (1 = no split applies) and the launch.
 int choose_split_k(int64_t m, int64_t n, int64_t k, int num_sms);
 cudaError_t launch_gemm_mx_sk(const GemmLaunch& L, GemmParams p, int split, cudaStream_t st);
+// Split-K over a cluster with CUDA-core promotion (any fp32 scales): K-major
+// operands, bf16 output, plain GEMM; split 2 or 4.
+cudaError_t launch_gemm_prom_sk(const GemmLaunch& L, GemmParams p, int split, cudaStream_t st);
 
 // Raises `kern`'s dynamic shared-memory limit to `bytes` on the current device,
 // once per (kernel, device): the attribute is per device. Thread-safe.

@@ -41,6 +41,7 @@
 #include "bounds.cuh"
 #include "common.cuh"
 #include "gemm.cuh"
+#include "splitk.cuh"
 
 namespace ql {
 namespace {
@@ -69,23 +70,14 @@ struct SkCfg {
     static constexpr int kNumBars = 2 * kStages + 1 + 2 * kSfSlots + 2 + 1 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-    // partial exchange, inside the operand ring: receive blocks [S][128][SW]
-    // (64 KB for any S) at offset 0, then per column half two staging blocks
-    static constexpr int kRecvBytes = BM * BN * 4;
+    // the partial exchange (splitk.cuh) reuses the operand ring
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(BN + 2 * kSfCols <= kTmemCols, "tensor memory budget");
-    static_assert(kRecvBytes + 4 * (BM * (BN / 2) * 4) <= kOffSf, "exchange fits in the operand ring");
+    static_assert(splitk::kExchangeBytes <= kOffSf, "exchange fits in the operand ring");
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl)) != 0;
-}
-
-// Byte offset of 16-byte chunk c of row r in a [128][sw] fp32 block: chunks
-// are XOR-swizzled by the row's low three bits, so a warp's 32 consecutive
-// rows touching the same logical chunk spread over all banks.
-__device__ __forceinline__ uint32_t xchg_off(int r, int c, int sw) {
-    return static_cast<uint32_t>(r * sw * 4 + ((c ^ (r & 7)) << 4));
 }
 
 // Exponent words of K group g for R scale rows (as gemm_mx.cu): packed words
@@ -150,11 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kb0 = static_cast<int>((static_cast<int64_t>(rank) * p.num_kb) / split);
     const int kb1 = static_cast<int>((static_cast<int64_t>(rank + 1) * p.num_kb) / split);
     const int g0 = kb0 / 4, g1 = (kb1 + 3) / 4;      // K groups touching [kb0, kb1)
-    const int sw = BN / split;                       // columns of the slice each CTA finishes
-    const uint32_t slice_bytes = static_cast<uint32_t>(BM * sw * 4);
-    // only the tile's rows inside A travel: rows are contiguous in a slice block
-    const int64_t rows_left = p.m - static_cast<int64_t>(mb) * BM;
-    const uint32_t copy_bytes = static_cast<uint32_t>((rows_left < BM ? rows_left : BM) * sw * 4);
+    const splitk::Exchange xchg = splitk::make_exchange(smem, rbar, p, mb);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -167,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
         // armed before the cluster barrier that precedes any copy into this CTA
-        mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(split - 1) * copy_bytes);
+        mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(split - 1) * xchg.copy_bytes);
     }
     pdl_launch_dependents();
     if (warp == 0 && lane == 0) {
@@ -327,78 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before_sync();
         // every CTA's MMAs have finished: every operand ring of the cluster is idle
         cluster_sync_all();
-        uint8_t* recv = smem;
-        // this half's staging blocks (one per remote slice, at most two)
-        uint8_t* stage = smem + C::kRecvBytes + wg * 2 * slice_bytes;
-        const int lg = __ffs(sw) - 1;
-        const int first_slice = (wg * CPT) >> lg;
-        if (ok) {
-            // own slice straight into recv[rank], the others into staging[slice - first_slice]
-#pragma unroll
-            for (int c4 = 0; c4 < CPT / 4; ++c4) {
-                const int col = wg * CPT + c4 * 4;
-                const int j = col >> lg;
-                const int cc = (col - (j << lg)) >> 2;
-                uint8_t* blk = (j == rank) ? recv + rank * slice_bytes : stage + (j - first_slice) * slice_bytes;
-                *reinterpret_cast<uint4*>(blk + xchg_off(r_local, cc, sw)) =
-                    make_uint4(accb[c4 * 4], accb[c4 * 4 + 1], accb[c4 * 4 + 2], accb[c4 * 4 + 3]);
-            }
-            fence_proxy_async_smem();     // staging visible to the bulk copies (async proxy)
-        }
-        named_bar_sync(1 + wg, 128);
-        if (ok && (threadIdx.x & 127) == 0) {
-            const int nsl = CPT >> lg;                    // slices in this half (1 or 2)
-            for (int i = 0; i < nsl; ++i) {
-                const int j = first_slice + i;
-                if (j == rank) continue;
-                bulk_copy_to_cluster(mapa_shared(recv + rank * slice_bytes, static_cast<uint32_t>(j)),
-                                     stage + i * slice_bytes, copy_bytes,
-                                     mapa_shared(rbar, static_cast<uint32_t>(j)));
-            }
-            bulk_commit_group();
-        }
-        named_bar_sync(3, kMathThreads);                  // own slice complete
-        const bool got = ok && warp_wait(rbar, 0, ctl);   // the other CTAs' partials arrived
-        if (got) {
-            const int t = threadIdx.x - (kThreads - kMathThreads);
-            const int row = t & (BM - 1), part = t >> 7;
-            const int cpp = sw >> 3;                      // 16-byte chunks per thread: sw/4 over two parts
-            const int64_t grow = static_cast<int64_t>(mb) * BM + row;
-            if (grow < p.m) {
-                __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + grow * p.ldd;
-                for (int c = part * cpp; c < (part + 1) * cpp; c += 2) {
-                    float acc[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-                    for (int s = 0; s < split; ++s) {
-                        const uint8_t* blk = recv + s * slice_bytes;
-                        const float4 v0 = *reinterpret_cast<const float4*>(blk + xchg_off(row, c, sw));
-                        const float4 v1 = *reinterpret_cast<const float4*>(blk + xchg_off(row, c + 1, sw));
-                        acc[0] += v0.x; acc[1] += v0.y; acc[2] += v0.z; acc[3] += v0.w;
-                        acc[4] += v1.x; acc[5] += v1.y; acc[6] += v1.z; acc[7] += v1.w;
-                    }
-                    const int64_t col = static_cast<int64_t>(nb) * BN + rank * sw + c * 4;
-                    if (p.vec_store && col + 8 <= p.n) {
-                        __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[0], acc[1]);
-                        __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[2], acc[3]);
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[4], acc[5]);
-                        __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[6], acc[7]);
-                        uint4 u;
-                        u.x = *reinterpret_cast<uint32_t*>(&h0);
-                        u.y = *reinterpret_cast<uint32_t*>(&h1);
-                        u.z = *reinterpret_cast<uint32_t*>(&h2);
-                        u.w = *reinterpret_cast<uint32_t*>(&h3);
-                        if (QL_IN(p.bnd, 2, drow + col, 16)) *reinterpret_cast<uint4*>(drow + col) = u;
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            if (col + e < p.n && QL_IN(p.bnd, 2, drow + col + e, 2)) drow[col + e] = __float2bfloat16_rn(acc[e]);
-                    }
-                }
-            }
-        }
-        // the staging blocks must stay until the copies out of them have read them
-        if ((threadIdx.x & 127) == 0) bulk_wait_read_all();
+        splitk::exchange_and_store(accb, ok, xchg, wg, r_local, mb, nb, p, ctl);
     }
 
     tc_fence_before_sync();

@@ -49,7 +49,7 @@ def run(ops):
     m, n, k = 300, 520, 640
     a = syn.randn((m, k), seed=61).to(dev)
     w = syn.randn((n, k), seed=62, mul=0.02).to(dev)
-    for fmt, paths in ((0, (0, 5, 6)), (2, (0, 1, 2, 3, 4))):
+    for fmt, paths in ((0, (0, 5, 6, 7)), (2, (0, 1, 2, 3, 4, 7))):
         aq, sa = ops.fp8_cast_per_token(a, 128, fmt, sf_mn_major=True)
         wq, sw = ops.fp8_cast_per_block(w, fmt)
         for path in paths:

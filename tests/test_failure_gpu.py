@@ -32,8 +32,8 @@ def ops():
     o.set_gemm_path(0)
 
 
-@pytest.mark.parametrize("path,fmt", [(1, 0), (5, 0), (2, 2), (3, 2), (4, 2)],
-                         ids=["promotion", "promotion_pair", "block_scaled", "pair", "split_k"])
+@pytest.mark.parametrize("path,fmt", [(1, 0), (5, 0), (7, 0), (2, 2), (3, 2), (4, 2)],
+                         ids=["promotion", "promotion_pair", "promotion_split_k", "block_scaled", "pair", "split_k"])
 def test_bounded_wait_times_out_and_context_survives(orc, ops, path, fmt):
     m, n, k = 512, 512, 1024
     x = syn.randn((m, k), seed=syn.SEED_X).cuda()

@@ -193,8 +193,13 @@ def test_zero_k_writes_zero(ops):
     assert torch.count_nonzero(d).item() == 0
 
 
-def test_num_sms_knob_same_result(orc, ops):
-    x, w, xq, xs, wq, ws = fwd_operands(ops, 512, 1024, 1024, 0)
+@pytest.mark.parametrize("m", [2048, 512])
+def test_num_sms_knob_same_result(orc, ops, m):
+    """Half the SM budget: the persistent grid's tile order changes nothing
+    (2048 rows: no K split at either budget, bit-equal results); at 512 rows
+    the budget changes the cluster split of K (four CTAs against two), so
+    both results are held to the oracle instead."""
+    x, w, xq, xs, wq, ws = fwd_operands(ops, m, 1024, 1024, 0)
     d1 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 0)
     full = ops.get_num_sms()
     ops.set_num_sms(full // 2)
@@ -204,7 +209,12 @@ def test_num_sms_knob_same_result(orc, ops):
     finally:
         ops.set_num_sms(0)
     assert ops.get_num_sms() == full
-    assert torch.equal(d1, d2)
+    if m == 2048:
+        assert torch.equal(d1, d2)
+    else:
+        ref = oracle_fwd(orc, xq, xs, wq, ws, 0)
+        check_gemm(d1.float().cpu().numpy(), ref, "all SMs")
+        check_gemm(d2.float().cpu().numpy(), ref, "half the SMs")
 
 
 def test_gemm_rejects_misaligned(ops):
@@ -258,7 +268,8 @@ def test_wgrad_exact_pow2_scales(orc, ops, path, bn, k, packed):
     assert bad.size == 0, f"{len(bad)} mismatches; first {bad[0]} got {got[tuple(bad[0])]} ref {ref[tuple(bad[0])]}"
 
 
-@pytest.mark.parametrize("path", [1, 5, 2, 3, 4], ids=["promotion", "promotion_pair", "block_scaled", "pair", "split_k"])
+@pytest.mark.parametrize("path", [1, 5, 2, 3, 4, 7],
+                         ids=["promotion", "promotion_pair", "block_scaled", "pair", "split_k", "promotion_split_k"])
 @pytest.mark.parametrize("bn", [32, 64, 128, 256])
 def test_fwd_exact_pow2_block_scales(orc, ops, path, bn):
     """fwd form: 1x128 A scales and 128x128 B block scales, all powers of two,
@@ -352,6 +363,32 @@ def test_split_k_cluster(orc, ops, case, fmt):
     # the default path picks the same kernel for these shapes and agrees
     d2 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt) if sms == 0 else d
     assert torch.equal(d, d2)
+
+
+@pytest.mark.parametrize("fmt", [0, 2], ids=["fp32", "packed"])
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: "x".join(map(str, c[:3])) + f"_sms{c[3]}")
+def test_promotion_split_k_cluster(orc, ops, case, fmt):
+    """Split-K over a cluster with CUDA-core promotion (path 7; the default for
+    fp32 scales at small M): each CTA promotes its K blocks with any fp32
+    scales, the S partial tiles are summed through distributed shared memory,
+    and the result equals the block-scaled product within the GEMM tolerance,
+    for every cluster size, ragged M/N/K and one-row problems."""
+    m, n, k, sms = case
+    x, w, xq, xs, wq, ws = fwd_operands(ops, m, n, k, fmt, w_mul=0.02, seed_x=17, seed_w=18)
+    ops.set_num_sms(sms)
+    ops.set_gemm_path(7)
+    try:
+        d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    finally:
+        ops.set_gemm_path(0)
+        ops.set_num_sms(0)
+    assert ops.device_status() == 0
+    rows = np.arange(m) if m <= 256 else np.sort(np.random.default_rng(2).choice(m, 64, replace=False))
+    ref = oracle_fwd(orc, xq, xs, wq, ws, fmt, rows=rows)
+    check_gemm(d[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref, "promotion split-k")
+    if fmt == 0 and sms == 0:
+        # fp32 scales take this kernel by default at these shapes: the same bits
+        assert torch.equal(d, ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt))
 
 
 @pytest.mark.parametrize("n", [520, 300])
