@@ -664,8 +664,11 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int num_sms) {
         return launch_t<256, false, false, true>(L, p, st, num_sms);
     }
     // CUDA-core promotion with too few 128 x 128 tiles to occupy the SMs (small
-    // M): split-K over a cluster (path 7 forces it where a split applies)
-    if (promote && !grouped && !L.out_f32 && (L.path == 7 || (L.path == 0 && L.block_n == 0))) {
+    // M) and a long K loop (16 K blocks or more): split-K over a cluster (path 7
+    // forces it wherever a split applies). With fewer K blocks the cluster's
+    // launch and exchange cost more than the split saves (128 x 256 x 512: 10.9
+    // us on one SM per tile, 12.3 us split in two).
+    if (promote && !grouped && !L.out_f32 && (L.path == 7 || (L.path == 0 && L.block_n == 0 && p.num_kb >= 16))) {
         const int split_p = choose_split_k(L.m, L.n, L.k, num_sms);
         if (split_p >= 2) return launch_gemm_prom_sk(L, p, split_p, st);
     }

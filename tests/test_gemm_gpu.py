@@ -193,13 +193,13 @@ def test_zero_k_writes_zero(ops):
     assert torch.count_nonzero(d).item() == 0
 
 
-@pytest.mark.parametrize("m", [2048, 512])
-def test_num_sms_knob_same_result(orc, ops, m):
+@pytest.mark.parametrize("m,k", [(2048, 1024), (512, 2048)])
+def test_num_sms_knob_same_result(orc, ops, m, k):
     """Half the SM budget: the persistent grid's tile order changes nothing
-    (2048 rows: no K split at either budget, bit-equal results); at 512 rows
-    the budget changes the cluster split of K (four CTAs against two), so
-    both results are held to the oracle instead."""
-    x, w, xq, xs, wq, ws = fwd_operands(ops, m, 1024, 1024, 0)
+    (2048 x 1024 x 1024: no K split at either budget, bit-equal results); at
+    512 x 1024 x 2048 the budget changes the cluster split of K (four CTAs
+    against two), so both results are held to the oracle instead."""
+    x, w, xq, xs, wq, ws = fwd_operands(ops, m, 1024, k, 0)
     d1 = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 0)
     full = ops.get_num_sms()
     ops.set_num_sms(full // 2)
@@ -386,7 +386,7 @@ def test_promotion_split_k_cluster(orc, ops, case, fmt):
     rows = np.arange(m) if m <= 256 else np.sort(np.random.default_rng(2).choice(m, 64, replace=False))
     ref = oracle_fwd(orc, xq, xs, wq, ws, fmt, rows=rows)
     check_gemm(d[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref, "promotion split-k")
-    if fmt == 0 and sms == 0:
+    if fmt == 0 and sms == 0 and (k + 127) // 128 >= 16:
         # fp32 scales take this kernel by default at these shapes: the same bits
         assert torch.equal(d, ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt))
 
