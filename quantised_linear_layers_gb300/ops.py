@@ -440,7 +440,10 @@ def set_gemm_block_n(bn: int) -> None:
 
 
 def set_gemm_path(path: int) -> None:
-    """0 auto, 1 CUDA-core promotion, 2 block-scaled MMA (UE8M0 formats)."""
+    """GEMM kernel choice (ql_set_gemm_path): 0 auto; CUDA-core promotion: 1
+    (default kernel), 5 on CTA pairs, 6 on one SM per tile, 7 split-K over a
+    cluster where a split applies; block-scaled MMA (UE8M0 formats): 2 on one
+    SM per tile, 3 on CTA pairs, 4 split-K over a cluster where it applies."""
     _check("ql_set_gemm_path", load_library().ql_set_gemm_path(int(path)))
 
 
