@@ -391,6 +391,26 @@ def test_promotion_split_k_cluster(orc, ops, case, fmt):
         assert torch.equal(d, ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt))
 
 
+@pytest.mark.parametrize("path", [7, 6], ids=["promotion_split_k", "promotion_single_sm"])
+def test_promotion_fp32_wide_scale_range(orc, ops, path):
+    """fp32 scales spread over six decades: every row of X and of W scaled by
+    10**u, u ~ U(-3, 3), at M = 64 (the split-K cluster adds partials whose K
+    ranges carry very different scales). Held to the oracle like every GEMM."""
+    m, n, k = 64, 1024, 7168
+    x = syn.randn_row_exp(m, k, seed=91)
+    w = syn.randn_row_exp(n, k, seed=92)
+    xq, xs = ops.fp8_cast_per_token(x.cuda(), 128, 0, sf_mn_major=True)
+    wq, ws = ops.fp8_cast_per_block(w.cuda(), 0)
+    ops.set_gemm_path(path)
+    try:
+        d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, 0)
+    finally:
+        ops.set_gemm_path(0)
+    assert ops.device_status() == 0
+    ref = oracle_fwd(orc, xq, xs, wq, ws, 0)
+    check_gemm(d.float().cpu().numpy(), ref, f"path {path}, wide scale range")
+
+
 @pytest.mark.parametrize("n", [520, 300])
 @pytest.mark.parametrize("offset", [64, 4], ids=["aligned", "unaligned"])
 @pytest.mark.parametrize("out", ["bf16", "f32", "f32_acc"])
