@@ -211,15 +211,21 @@ def max_over_ranks(world, v: float) -> float:
 
 # ------------------------------------------------------------------ timing helpers
 def stats_us(ts_ms):
-    """Median, p10 and p90 (us) of per-repetition times given in ms."""
+    """Median, p10 and p90 (us) of per-repetition times given in ms, and the
+    mean of the middle 80 %. CUDA event readings on this GPU come in steps of
+    about 2.05 us, so a short kernel's median sits on one of the two steps
+    around its duration; the trimmed mean, averaging over where each launch
+    fell between steps, is the closer figure there."""
     xs = sorted(ts_ms)
     n = len(xs)
 
     def q(f):
         return xs[min(n - 1, max(0, int(round(f * (n - 1)))))]
 
+    cut = n // 10
+    mid = xs[cut:n - cut] if n - 2 * cut > 0 else xs
     return {"us": round(statistics.median(xs) * 1e3, 2), "p10": round(q(0.1) * 1e3, 2),
-            "p90": round(q(0.9) * 1e3, 2), "n": n}
+            "p90": round(q(0.9) * 1e3, 2), "mean_mid80": round(statistics.fmean(mid) * 1e3, 2), "n": n}
 
 
 class L2Flush:
