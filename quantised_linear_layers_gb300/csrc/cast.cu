@@ -31,6 +31,23 @@ __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+// Two fp32 products at once (mul.rn.f32x2: each lane rounded to nearest even,
+// subnormals kept, exactly as the scalar multiply).
+__device__ __forceinline__ float2 mul_rn2(float2 a, float2 b) {
+    const uint64_t a2 = static_cast<uint64_t>(__float_as_uint(a.x)) | (static_cast<uint64_t>(__float_as_uint(a.y)) << 32);
+    const uint64_t b2 = static_cast<uint64_t>(__float_as_uint(b.x)) | (static_cast<uint64_t>(__float_as_uint(b.y)) << 32);
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a2), "l"(b2));
+    return make_float2(__uint_as_float(static_cast<uint32_t>(r)), __uint_as_float(static_cast<uint32_t>(r >> 32)));
+}
+
+// quant4 (quant.cuh) with the four products taken two at a time.
+__device__ __forceinline__ uint32_t quant4_pk(float a, float b, float c, float d, float f) {
+    const float2 f2 = make_float2(f, f);
+    const float2 p = mul_rn2(make_float2(a, b), f2), q = mul_rn2(make_float2(c, d), f2);
+    return e4m3x2(p.x, p.y) | (e4m3x2(q.x, q.y) << 16);
+}
+
 // ---------------------------------------------------------------------------
 // Row-contiguous per-token cast (x_stride_n == 1, out_stride_n == 1).
 // One warp task = (row, chunk of 32*E elements); each lane owns E consecutive
@@ -1025,8 +1042,8 @@ __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 4 : 2) cast_block_kernel
     for (int it = 0; it < 8; ++it) {
         const int bb = it * 16 + tid / 16;
         const int a0 = (tid % 16) * 8;
-        const uint32_t lo = quant4(val(it, 0), val(it, 1), val(it, 2), val(it, 3), f);
-        const uint32_t hi = quant4(val(it, 4), val(it, 5), val(it, 6), val(it, 7), f);
+        const uint32_t lo = quant4_pk(val(it, 0), val(it, 1), val(it, 2), val(it, 3), f);
+        const uint32_t hi = quant4_pk(val(it, 4), val(it, 5), val(it, 6), val(it, 7), f);
         if (in_mode == 1) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
