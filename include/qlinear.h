@@ -419,14 +419,15 @@ ql_status ql_set_gemm_block_n(int block_n);
  * at least one such tile per pair of SMs; with fewer tiles, split over K
  * across a thread-block cluster when that fills the SMs, else on CTA pairs
  * while there is a tile for every other pair, else on single SMs. With
- * QL_SF_FP32 scales (and with path 1) the partial product of every 128-wide
- * K block is promoted on the CUDA cores: of one SM per tile, or, for a plain
- * GEMM with bf16 output whose 128 x 128 tiles are too few to occupy the SMs
- * (small M), of a cluster of 2 or 4 CTAs that split the tile's K blocks and
- * sum their fp32 partials through distributed shared memory. 1 forces the
- * CUDA-core promotion path, 5 runs it on CTA pairs (256 x 256 tiles; plain
- * GEMMs only, measured no faster than one SM per tile), 6 forces the
- * single-SM kernel and 7 the cluster split-K form where it applies; 2 forces
+ * QL_SF_FP32 scales the partial product of every 128-wide K block is
+ * promoted on the CUDA cores: on one SM per tile or, for a plain GEMM with
+ * bf16 output, at least 16 K blocks and too few 128 x 128 tiles to occupy
+ * the SMs (small M), on a cluster of 2 or 4 CTAs that split the tile's K
+ * blocks and sum their fp32 partials through distributed shared memory.
+ * 1 and 6 force the CUDA-core promotion on one SM per tile (for any scale
+ * format), 5 runs it on CTA pairs (256 x 256 tiles; plain GEMMs only,
+ * measured no faster than one SM per tile) and 7 on the cluster split-K form
+ * wherever a split applies (any number of K blocks); 2 forces
  * the single-SM block-scaled kernel, 3 the block-scaled CTA-pair kernel and 4
  * the block-scaled cluster split-K kernel where it applies (2-4 ignored for
  * QL_SF_FP32). All give results within the GEMM tolerance of each other.
