@@ -119,7 +119,20 @@ __global__ void __launch_bounds__(256, 4) cast_rows_kernel(const T* __restrict__
 
         float s, f;
         uint32_t ebyte;
-        group_scale<FMT, RECIP>(amax, s, f, ebyte);
+        if constexpr (FMT == kSfFp32 && !RECIP && kLanesPerGroup >= 2) {
+            // group_scale's two correctly rounded divisions, one per lane of
+            // a pair inside the group (a / 448 on the even lane, 448 / a on
+            // the odd one), exchanged by shuffle: same operations, one divide
+            // per lane instead of two
+            const float a = fmaxf(amax, 1e-4f);
+            const bool odd = (lane & 1) != 0;
+            const float qd = __fdiv_rn(odd ? 448.0f : a, odd ? a : 448.0f);
+            s = __shfl_sync(0xffffffffu, qd, lane & ~1);
+            f = __shfl_sync(0xffffffffu, qd, lane | 1);
+            ebyte = 0;
+        } else {
+            group_scale<FMT, RECIP>(amax, s, f, ebyte);
+        }
 
         if (e0 < n) {
             uint8_t* orow = out + row * ldo;
