@@ -1,7 +1,8 @@
 """Host logic of bench.py that needs no GPU: the DRAM-traffic record is used
 only while the kernel sources it was measured on are unchanged, the clock
 sampler's parsing of nvidia-smi lines (median SM clock, throttle reasons), and
-the roofline denominators (measured peaks, else the stated fallback)."""
+the roofline denominators (measured peaks, else the stated fallback), and the
+timing statistics."""
 import hashlib
 import json
 import os
@@ -87,3 +88,17 @@ def test_peaks_measured_else_fallback(tmp_path, monkeypatch):
         json.dumps({"hbm_gbs": 6796.2, "bf16_tflops": 1855.4, "bf16_tflops_sustained": 1700.0}))
     p = bench.peaks()
     assert p == {"hbm_gbs": 6796.2, "bf16": 1855.4, "bf16_sus": 1700.0, "source": "measured"}
+
+
+def test_timing_statistics():
+    """Median, p10/p90 and the mean of the middle 80 % of a set of repetitions:
+    readings that sit on two event steps (2.048 us apart) in a 60/40 split have
+    their median on the lower step and the trimmed mean between the two."""
+    ts = [0.006144] * 60 + [0.008192] * 40
+    st = bench.stats_us(ts)
+    assert st["n"] == 100
+    assert st["us"] == 6.14 and st["p10"] == 6.14 and st["p90"] == 8.19
+    # the middle 80 repetitions: 50 on the lower step, 30 on the upper one
+    assert abs(st["mean_mid80"] - (50 * 6.144 + 30 * 8.192) / 80) < 0.01
+    one = bench.stats_us([1.0])
+    assert one["us"] == one["mean_mid80"] == 1000.0
