@@ -1,8 +1,8 @@
 """Host logic of bench.py that needs no GPU: the DRAM-traffic record is used
 only while the kernel sources it was measured on are unchanged, the clock
-sampler's parsing of nvidia-smi lines (median SM clock, throttle reasons), and
-the roofline denominators (measured peaks, else the stated fallback), and the
-timing statistics."""
+sampler's parsing of nvidia-smi lines (median SM clock, throttle reasons), the
+roofline denominators (measured peaks, else the stated fallback) and the timing
+statistics."""
 import hashlib
 import json
 import os
