@@ -113,3 +113,41 @@ def test_random_gemm(orc, ops, case):
         ops.set_gemm_path(0)
     assert ops.device_status() == 0
     check_gemm(d.double().cpu().numpy(), ref, f"m={m} n={n} k={k} fmt{fmt} path{path} wgrad={wgrad}")
+
+
+@pytest.mark.parametrize("case", range(15))
+def test_random_gemm_small_m_long_k(orc, ops, case):
+    """Small M with 16-32 K blocks, where the split-K forms apply: the automatic
+    choice (split-K for 16 K blocks or more), the forced block-scaled (4) and
+    promotion (7) split-K forms, the CTA-pair (5) and single-SM (6) promotion
+    kernels, under random SM budgets, for the forward and weight-gradient
+    forms; every result within the GEMM tolerance of the oracle."""
+    rng = np.random.default_rng(6000 + case)
+    m = int(rng.integers(1, 260))
+    n = int(rng.integers(16, 1600))
+    k = 128 * int(rng.integers(16, 33)) - 16 * int(rng.integers(0, 8))   # 16 to 32 K blocks, ragged
+    fmt, path = case // 5, [0, 4, 5, 6, 7][case % 5]       # every (format, path) pair once
+    sms = [0, 64, 96, 128][int(rng.integers(0, 4))]
+    wgrad = case % 4 == 3
+    x = syn.randn((m, k), seed=7000 + case)
+    w = syn.randn((n, k), seed=8000 + case, mul=0.05)
+    ldk = -(-k // 16) * 16
+    aq_buf = torch.empty((m, ldk), dtype=torch.float8_e4m3fn, device="cuda")[:, :k]
+    xq, xs = ops.fp8_cast_per_token(x.cuda(), 128, fmt, out=aq_buf, sf_mn_major=True)
+    bq_buf = torch.empty((n, ldk), dtype=torch.float8_e4m3fn, device="cuda")[:, :k]
+    ops.set_gemm_path(path)
+    ops.set_num_sms(sms)
+    try:
+        if wgrad:
+            wq, ws = ops.fp8_cast_per_token(w.cuda(), 128, fmt, out=bq_buf)
+            d = ops.gemm_fp8_wgrad_fp32(xq, xs, wq, ws, fmt=fmt)
+            ref = orc.gemm(np_bytes(xq), np_sf(xs), np_bytes(wq), np_sf(ws), fmt, b_per_row=True, out="f32")
+        else:
+            wq, ws = ops.fp8_cast_per_block(w.cuda(), fmt, out=bq_buf)
+            d = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+            ref = orc.gemm(np_bytes(xq), np_sf(xs), np_bytes(wq), np_sf(ws), fmt, out="bf16")
+    finally:
+        ops.set_gemm_path(0)
+        ops.set_num_sms(0)
+    assert ops.device_status() == 0
+    check_gemm(d.double().cpu().numpy(), ref, f"m={m} n={n} k={k} fmt{fmt} path{path} sms{sms} wgrad={wgrad}")
