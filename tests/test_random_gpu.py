@@ -82,6 +82,52 @@ def test_random_cast(orc, ops, case):
     assert _scales_equal(s, os_, fmt), f"{layout} m={m} n={n}: scales differ"
 
 
+@pytest.mark.parametrize("case", range(24))
+def test_random_dual_cast(orc, ops, case):
+    """fp8_cast_per_token_dual on random shapes, input types, formats and row
+    offsets (unaligned rows read element by element): the cast of x and that
+    of x^T kept in x's layout, each bit for bit the oracle's cast."""
+    rng = np.random.default_rng(9000 + case)
+    m = int(rng.integers(1, 700))
+    n = int(rng.integers(1, 900))
+    dtype = [torch.bfloat16, torch.float32][int(rng.integers(0, 2))]
+    fmt = int(rng.integers(0, 3))
+    recip = bool(fmt == 0 and rng.integers(0, 2))
+    off = int(rng.integers(0, 2)) * int(rng.integers(1, 8))      # 0, or a column offset of 1..7
+    base = syn.randn_row_exp(m, n + off, seed=9500 + case, dtype=dtype)
+    x = base[:, off:]
+    qr, sr, qc, sc = ops.fp8_cast_per_token_dual(base.cuda()[:, off:], fmt, recip)
+    assert ops.device_status() == 0
+    oq, os_ = orc.cast_per_token(np_input(x), 128, fmt, recip=recip)
+    oqt, ost = orc.cast_per_token(np_input(x).T, 128, fmt, recip=recip)
+    what = f"m={m} n={n} {dtype} fmt{fmt} recip={recip} off={off}"
+    assert np.array_equal(np_bytes(qr), oq), what + ": row-cast bytes differ"
+    assert np.array_equal(np_bytes(qc).T, oqt), what + ": column-cast bytes differ"
+    assert _scales_equal(sr, os_, fmt) and _scales_equal(sc, ost, fmt), what + ": scales differ"
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_random_block_cast_dual(orc, ops, case):
+    """fp8_cast_per_block_dual on random shapes, input types and formats: W's
+    E4M3 bytes and 128 x 128 scale grid, and the grid of W^T's cast, bit for
+    bit the oracle's block casts of W and W^T."""
+    rng = np.random.default_rng(9800 + case)
+    m = int(rng.integers(1, 800))
+    n = int(rng.integers(1, 900))
+    dtype = [torch.bfloat16, torch.float32][int(rng.integers(0, 2))]
+    fmt = int(rng.integers(0, 3))
+    recip = bool(fmt == 0 and rng.integers(0, 2))
+    w = syn.randn((m, n), seed=9900 + case, mul=0.02, dtype=dtype)
+    q, s, st = ops.fp8_cast_per_block_dual(w.cuda(), fmt, recip=recip)
+    assert ops.device_status() == 0
+    oq, os_ = orc.cast_per_block(np_input(w), fmt, recip=recip)
+    otq, ots = orc.cast_per_block(np_input(w).T, fmt, recip=recip)
+    what = f"m={m} n={n} {dtype} fmt{fmt} recip={recip}"
+    assert np.array_equal(np_bytes(q), oq), what + ": bytes differ"
+    assert np.array_equal(np_bytes(q).T, otq), what + ": W^T bytes differ"
+    assert _scales_equal(s, os_, fmt) and _scales_equal(st, ots, fmt), what + ": scale grids differ"
+
+
 @pytest.mark.parametrize("case", range(32))
 def test_random_gemm(orc, ops, case):
     rng = np.random.default_rng(3000 + case)
