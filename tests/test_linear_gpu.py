@@ -162,3 +162,35 @@ def test_one_pass_casts_equal_separate_calls(lin, fmt):
     lin.backward(dy, w8, xc, need_dx=False, dw_out=main, accumulate=True)
     lin.wgrad(dy, x, fmt, out=main2, accumulate=True, mn_major=True)
     assert torch.equal(main, main2)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_linear_mn_major_random_shapes(orc, lin, case):
+    """The default layer path (forward_saving + backward: dual casts, NN
+    dgrad with W's bytes read MN-major, MN-major wgrad) on seeded ragged
+    shapes, token counts from 1 up: every output element within the GEMM
+    tolerance of the oracle on the oracle's own casts, which the GPU's casts
+    equal bit for bit."""
+    rng = np.random.default_rng(12000 + case)
+    T = {0: 1, 3: 7}.get(case, int(rng.integers(1, 520)))     # one token, a few tokens, then any
+    IN = int(rng.integers(16, 700))
+    OUT = int(rng.integers(16, 700))
+    fmt = [0, 1, 2][case % 3]
+    x = syn.randn_row_exp(T, IN, seed=12100 + case)
+    dy = syn.randn((T, OUT), seed=12200 + case)
+    w = syn.randn((OUT, IN), seed=12300 + case, mul=0.02)
+    w8 = lin.FP8Weight(w.cuda(), fmt, mn_major=True)
+    y, xc = lin.forward_saving(x.cuda(), w8)
+    dx, dw = lin.backward(dy.cuda(), w8, xc)
+    what = f"T={T} IN={IN} OUT={OUT} fmt{fmt}"
+    wq, ws = orc.cast_per_block(np_input(w), fmt)
+    wtq, wts = orc.cast_per_block(np_input(w).T, fmt)
+    xq, xs = orc.cast_per_token(np_input(x), 128, fmt)
+    dq, ds = orc.cast_per_token(np_input(dy), 128, fmt)
+    aq, sa = orc.cast_per_token(np_input(dy).T, 128, fmt)
+    bq, sb = orc.cast_per_token(np_input(x).T, 128, fmt)
+    # the cast of X along the tokens kept for the weight gradient, bit for bit
+    assert np.array_equal(np_bytes(xc[0]).T, bq), what + ": X's token-axis cast differs"
+    check_gemm(y.float().cpu().numpy(), orc.gemm(xq, xs, wq, ws, fmt, out="bf16"), what + " fwd")
+    check_gemm(dx.float().cpu().numpy(), orc.gemm(dq, ds, wtq, wts, fmt, out="bf16"), what + " dgrad")
+    check_gemm(dw.double().cpu().numpy(), orc.gemm(aq, sa, bq, sb, fmt, b_per_row=True, out="f32"), what + " wgrad")
