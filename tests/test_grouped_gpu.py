@@ -184,3 +184,28 @@ def test_invalid_indices_are_reported(orc, ops):
     check_gemm(got[keep], ref[keep], "rows around the invalid ones")
     # the next call is correct
     run_and_check(orc, ops, idx, xq, xs, wq, ws, 0)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_expert_layouts(orc, ops, case):
+    """Seeded random mixtures: 1 to 10 experts, each with 0 to 400 tokens
+    (empty experts included), ragged n and k, every scale format and the
+    kernel paths the grouped GEMM takes; valid rows within the GEMM tolerance,
+    padding rows untouched."""
+    rng = np.random.default_rng(13000 + case)
+    G = int(rng.integers(1, 11))
+    tokens = [int(t) for t in rng.integers(0, 401, size=G)]
+    if case % 2 == 1:
+        tokens[int(rng.integers(0, G))] = 0          # an expert without tokens
+    if sum(tokens) == 0:
+        tokens[0] = 1
+    n = int(rng.integers(16, 700))
+    k = int(rng.integers(1, 12)) * 128 - 16 * int(rng.integers(0, 8))
+    fmt = case % 3
+    path = [0, 1, 2, 3][(case // 3) % 4]
+    idx, xq, xs, wq, ws = grouped_operands(ops, tokens, n, k, fmt, seed=13100 + case, w_mul=0.05)
+    ops.set_gemm_path(path)
+    try:
+        run_and_check(orc, ops, idx, xq, xs, wq, ws, fmt)
+    finally:
+        ops.set_gemm_path(0)
