@@ -130,3 +130,39 @@ def test_output_views_untouched_outside(ops, path, n):
     p = parent.cpu().numpy()
     assert np.all(p[:, :48] == 0x5A) and np.all(p[:, 48 + n:] == 0x5A) and np.all(p[m:] == 0x5A)
     assert np.array_equal(np_bytes(view), np_bytes(q_c)) and torch.equal(sf_v, sf_c)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_fused_cast_random_shapes(orc, ops, case):
+    """Seeded random shapes, paths, input and output scale formats and group
+    widths: the fused output equals the oracle's cast of the same-tiled bf16
+    output bit for bit, and that output meets the GEMM tolerance."""
+    rng = np.random.default_rng(14000 + case)
+    m = int(rng.integers(1, 600))
+    n = int(rng.integers(16, 1200))
+    k = int(rng.integers(1, 10)) * 128 - 16 * int(rng.integers(0, 8))
+    path = [0, 1, 2, 3][case % 4]
+    fmt = [0, 1, 2][(case // 4) % 3]
+    gran = [128, 32][int(rng.integers(0, 2))]
+    out_fmt = int(rng.integers(0, 3))
+    recip = bool(out_fmt == 0 and rng.integers(0, 2))
+    xq, xs, wq, ws = operands(ops, m, n, k, fmt, seed=14100 + case)
+    ops.set_gemm_path(path)
+    ops.set_gemm_block_n(256)
+    try:
+        q, sf = ops.gemm_fp8_nt_fp8out(xq, xs, wq, ws, fmt, gran, out_fmt, recip, sf_mn_major=True)
+        y = ops.gemm_fp8_nt_bf16(xq, xs, wq, ws, fmt)
+    finally:
+        ops.set_gemm_block_n(0)
+        ops.set_gemm_path(0)
+    assert ops.device_status() == 0
+    what = f"m={m} n={n} k={k} path{path} fmt{fmt} g{gran} out{out_fmt} recip={recip}"
+    ref = orc.gemm(np_bytes(xq), np_sf(xs), np_bytes(wq), np_sf(ws), fmt)
+    check_gemm(y.float().cpu().numpy(), orc.round_output(ref, "bf16"), what + " bf16 output")
+    oq, osf = orc.cast_per_token(np_input(y), gran, out_fmt, recip)
+    assert np.array_equal(np_bytes(q), oq), what + ": E4M3 bytes differ from the cast of the bf16 output"
+    got_sf = np_sf(sf)
+    if out_fmt == 2:
+        assert np.array_equal(got_sf, osf), what
+    else:
+        assert np.array_equal(got_sf.view(np.uint32), osf.view(np.uint32)), what
