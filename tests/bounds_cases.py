@@ -75,6 +75,27 @@ def run(ops):
         w2 = syn.randn((c1, c2), seed=66, mul=0.02).to(dev)
         w2q, w2s, w2st = ops.fp8_cast_per_block_dual(w2, fmt)
         rec(f"dgrad_nn_f{fmt}", [ops.gemm_fp8_nn_bf16(dq, ds, w2q, w2st, fmt)])
+    # edges, at shapes the parity tests also run: one row, one column, cut
+    # groups and tiles in both directions; split-K with a single row
+    for shape in ((1, 512), (509, 1), (7, 33), (1, 24), (130, 36), (1, 130)):
+        xe = syn.randn_row_exp(*shape, dtype=torch.bfloat16).to(dev)
+        tag = f"{shape[0]}x{shape[1]}"
+        for fmt in (0, 2):
+            rec(f"edge_rows_{tag}_f{fmt}", ops.fp8_cast_per_token(xe, 32, fmt))
+            rec(f"edge_t_{tag}_f{fmt}", ops.fp8_cast_per_token(xe.t(), 128, fmt))
+            rec(f"edge_dual_{tag}_f{fmt}", ops.fp8_cast_per_token_dual(xe, fmt))
+            rec(f"edge_block_dual_{tag}_f{fmt}", ops.fp8_cast_per_block_dual(xe, fmt))
+    a1 = syn.randn((1, 4096), seed=71).to(dev)
+    w1 = syn.randn((512, 4096), seed=72, mul=0.02).to(dev)
+    for fmt, paths in ((0, (0, 7)), (2, (0, 4, 7))):
+        a1q, a1s = ops.fp8_cast_per_token(a1, 128, fmt, sf_mn_major=True)
+        w1q, w1s = ops.fp8_cast_per_block(w1, fmt)
+        for path in paths:
+            ops.set_gemm_path(path)
+            try:
+                rec(f"splitk_1x512x4096_f{fmt}_p{path}", [ops.gemm_fp8_nt_bf16(a1q, a1s, w1q, w1s, fmt)])
+            finally:
+                ops.set_gemm_path(0)
     # grouped GEMM (4 experts, padding rows)
     tokens = [128, 96, 112, 144]
     idx, _ = syn.contiguous_layout(tokens, 128)
